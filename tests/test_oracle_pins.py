@@ -1,0 +1,449 @@
+"""Pins for the CPU oracle: it is checked against what the pages and the
+mathematics fix, never against itself or against the CUDA path.
+
+Each test names what it pins.  Brute force uses float64 arithmetic over
+explicit enumerations (or an exhaustive per-coordinate dynamic program over
+the same candidate sets), which shares nothing with the oracle's decoder.
+"""
+import itertools
+import json
+import os
+
+import numpy as np
+import pytest
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "e8_constants.json")
+
+
+def _golden():
+    with open(GOLDEN) as f:
+        return json.load(f)
+
+
+# ------------------------------------------------------------ brute force
+
+
+def _dp_min(values, costs, par):
+    """Exhaustive minimum over per-coordinate candidates, split by the parity
+    of the summed integer parts.  values/costs/par: [N, 8, m] arrays.
+    Returns (best_even, best_odd) float64 [N]."""
+    inf = np.full(costs.shape[0], np.inf)
+    best0, best1 = np.zeros(costs.shape[0]), inf.copy()
+    for j in range(8):
+        c = costs[:, j, :]
+        p = par[:, j, :]
+        ev = np.where(p == 0, c, np.inf).min(axis=1)
+        od = np.where(p == 1, c, np.inf).min(axis=1)
+        best0, best1 = np.minimum(best0 + ev, best1 + od), np.minimum(best0 + od, best1 + ev)
+    return best0, best1
+
+
+def _candidates(u, half, bits):
+    """Candidate coordinate values per block.  Box codes: every value of the
+    coset inside the box; unbounded: a window of 6 values around u."""
+    u = u.astype(np.float64)
+    N = u.shape[0]
+    if bits:
+        L = 1 << bits
+        if half:
+            vals = np.arange(-(L - 1) / 2, (L - 1) / 2 + 0.5, 1.0)
+        else:
+            vals = np.arange(-(L // 2 - 1), L // 2 - 1 + 0.5, 1.0)
+        v = np.broadcast_to(vals, (N, 8, vals.size)).copy()
+    else:
+        base = np.floor(u) + (0.5 if half else 0.0)
+        v = base[:, :, None] + np.arange(-3, 3)[None, None, :]
+    costs = (u[:, :, None] - v) ** 2
+    ints = v - 0.5 if half else v
+    par = np.mod(np.rint(ints).astype(np.int64), 2)
+    return v, costs, par
+
+
+def brute_min_dist(u, strict, bits):
+    _, c0, p0 = _candidates(u, False, bits)
+    _, c1, p1 = _candidates(u, True, bits)
+    i_even, _ = _dp_min(None, c0, p0)
+    h_even, h_odd = _dp_min(None, c1, p1)
+    half = h_even if strict else np.minimum(h_even, h_odd)
+    return np.minimum(i_even, half)
+
+
+def enumerate_codebook(strict, bits):
+    """Every point of the box codebook (small bit widths only)."""
+    L = 1 << bits
+    pts = []
+    ivals = np.arange(-(L // 2 - 1), L // 2)
+    for p in itertools.product(ivals, repeat=8):
+        if sum(p) % 2 == 0:
+            pts.append(p)
+    hvals = np.arange(-(L - 1) / 2, (L - 1) / 2 + 0.5, 1.0)
+    for p in itertools.product(hvals, repeat=8):
+        if not strict or int(round(sum(x - 0.5 for x in p))) % 2 == 0:
+            pts.append(p)
+    return np.array(pts, dtype=np.float64)
+
+
+def in_codebook(r, strict, bits):
+    r = r.astype(np.float64)
+    frac = r - np.floor(r)
+    is_int = np.all(frac == 0.0, axis=1)
+    is_half = np.all(frac == 0.5, axis=1)
+    ok = is_int | is_half
+    s_int = np.rint(r.sum(axis=1)).astype(np.int64)
+    s_half = np.rint((r - 0.5).sum(axis=1)).astype(np.int64)
+    ok &= ~is_int | (s_int % 2 == 0)
+    if strict:
+        ok &= ~is_half | (s_half % 2 == 0)
+    if bits:
+        L = 1 << bits
+        ok &= ~is_int | np.all(np.abs(r) <= L // 2 - 1, axis=1)
+        ok &= ~is_half | np.all(np.abs(r) <= (L - 1) / 2, axis=1)
+    return ok
+
+
+# ------------------------------------------------------------- T1 decoder
+
+
+@pytest.mark.parametrize("strict", [1, 0])
+def test_t1_unbounded_matches_brute_force(orc, strict):
+    rng = np.random.default_rng(11 + strict)
+    u = rng.uniform(-3, 3, size=(20000, 8)).astype(np.float32)
+    r = orc.e8_nearest(u, strict, 0)
+    assert in_codebook(r, strict, 0).all()
+    d_orc = ((u.astype(np.float64) - r) ** 2).sum(axis=1)
+    d_min = brute_min_dist(u, strict, 0)
+    assert np.all(d_orc <= d_min + 1e-5), np.max(d_orc - d_min)
+
+
+def test_t1_dp_agrees_with_full_enumeration(orc):
+    """The factorised brute force itself against a plain enumeration (b = 2)."""
+    rng = np.random.default_rng(3)
+    u = rng.uniform(-1.6, 1.6, size=(60, 8)).astype(np.float32)
+    for strict in (1, 0):
+        cb = enumerate_codebook(strict, 2)
+        d_enum = ((u.astype(np.float64)[:, None, :] - cb[None]) ** 2).sum(-1).min(axis=1)
+        assert np.allclose(d_enum, brute_min_dist(u, strict, 2), atol=1e-12)
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+@pytest.mark.parametrize("strict", [1, 0])
+def test_t1_box_codes_match_brute_force(orc, bits, strict):
+    rng = np.random.default_rng(100 * bits + strict)
+    h = ((1 << bits) - 1) / 2
+    # inside the box, on its edges, and a little beyond it
+    u = rng.uniform(-1.05 * h, 1.05 * h, size=(4000, 8)).astype(np.float32)
+    u[:200] = np.round(u[:200] * 2) / 2  # exact half-integers / integers: tie cases
+    r = orc.e8_nearest(u, strict, bits)
+    assert in_codebook(r, strict, bits).all()
+    d_orc = ((u.astype(np.float64) - r) ** 2).sum(axis=1)
+    d_min = brute_min_dist(u, strict, bits)
+    assert np.all(d_orc <= d_min + 1e-5), np.max(d_orc - d_min)
+
+
+def test_t1_tie_rules(orc):
+    # integer coset rounds half to even: 0.5 -> 0, 1.5 -> 2 (unbounded)
+    r, c = orc.e8_block(np.array([0.5, 1.5, 0, 0, 0, 0, 0, 0], np.float32), 1, 0)
+    # both cosets are at distance 0.5; the tie goes to the integer coset
+    assert c == 0 and list(r) == [0, 2, 0, 0, 0, 0, 0, 0]
+    # the half-integer point of an integer u is u - 1/2 (ceil(u) - 1/2)
+    r, c = orc.e8_block(np.array([0.5, 0.5, 0.5, 0.5, 0.5, 0.5, 0.5, 2.0], np.float32), 0, 0)
+    assert c == 1 and list(r) == [0.5] * 7 + [1.5]
+    # parity fix-up moves the coordinate farthest from its rounding, toward u
+    r, c = orc.e8_block(np.array([0.1, 0.2, 0.3, 0.4, 0, 0, 0, 1.0], np.float32), 1, 0)
+    assert c == 0 and list(r) == [0, 0, 0, 1, 0, 0, 0, 1]
+    # equal scores: the lowest index is moved
+    r, c = orc.e8_block(np.array([0.3, 0.3, 0, 0, 0, 0, 0, 1.0], np.float32), 1, 0)
+    assert c == 0 and list(r) == [1, 0, 0, 0, 0, 0, 0, 1]
+
+
+def test_t1_fixup_at_box_edge_steps_inward(orc):
+    # b = 2, integer box [-1, 1]: u = (1.2, 0, ..., 0) rounds to 1 (odd); stepping
+    # toward u would leave the box, so the cheapest legal change is chosen.
+    u = np.array([1.2, 0.05, 0, 0, 0, 0, 0, 0], np.float32)
+    r = orc.e8_nearest(u[None], 1, 2)[0]
+    d = ((u.astype(np.float64) - r) ** 2).sum()
+    assert d <= brute_min_dist(u[None], 1, 2)[0] + 1e-6
+    assert np.all(np.abs(r) <= 1.5)
+
+
+# ---------------------------------------------------------- T2 invariants
+
+
+def test_t2_lattice_invariants_and_covering_radius(orc):
+    g = _golden()
+    rng = np.random.default_rng(5)
+    u = rng.normal(0, 3, size=(50000, 8)).astype(np.float32)
+    for strict in (1, 0):
+        r = orc.e8_nearest(u, strict, 0)
+        assert in_codebook(r, strict, 0).all()
+        d = ((u.astype(np.float64) - r) ** 2).sum(axis=1)
+        assert d.max() <= g["covering_radius_sq_e8"]["value"] + 1e-5
+
+
+def test_t2_norm2_shell_counts(orc):
+    """Points of squared norm 2 that each decoder keeps as fixed points."""
+    g = _golden()
+    ints = []
+    for i, j in itertools.combinations(range(8), 2):
+        for si in (-1, 1):
+            for sj in (-1, 1):
+                v = np.zeros(8)
+                v[i], v[j] = si, sj
+                ints.append(v)
+    halves = [np.array(s) * 0.5 for s in itertools.product((-1, 1), repeat=8)]
+    assert len(ints) == 112 and len(halves) == 256
+    for strict, key in ((1, "norm2_shell_strict"), (0, "norm2_shell_relaxed")):
+        fi = sum(np.array_equal(orc.e8_nearest(v.astype(np.float32)[None], strict, 0)[0], v) for v in ints)
+        fh = sum(np.array_equal(orc.e8_nearest(v.astype(np.float32)[None], strict, 0)[0], v) for v in halves)
+        assert fi == g[key]["integer_coset"]
+        assert fh == g[key]["half_coset"]
+    assert 112 + 128 == g["kissing_number"]["value"]
+
+
+# ------------------------------------------------------------- T3 Hadamard
+
+
+@pytest.mark.parametrize("n", [8, 64, 128])
+def test_t3_fwht_is_sylvester_hadamard(orc, n):
+    H = np.stack([orc.fwht(np.eye(n, dtype=np.float32)[j]) for j in range(n)], axis=1)
+    i = np.arange(n)
+    pop = np.vectorize(lambda v: bin(v).count("1"))(i[:, None] & i[None, :])
+    assert np.array_equal(H, (-1.0) ** pop)
+    assert np.array_equal(H @ H, n * np.eye(n))
+
+
+def test_t3_fwht_involution_and_matrix_product(orc):
+    rng = np.random.default_rng(7)
+    n = 128
+    xi = rng.integers(-1000, 1000, size=n).astype(np.float32)
+    assert np.array_equal(orc.fwht(orc.fwht(xi)), n * xi)  # exact on integers
+    x = rng.normal(size=n).astype(np.float32)
+    i = np.arange(n)
+    H = (-1.0) ** np.vectorize(lambda v: bin(v).count("1"))(i[:, None] & i[None, :])
+    ref = H @ x.astype(np.float64)
+    assert np.allclose(orc.fwht(x), ref, rtol=0, atol=1e-5 * np.abs(x).sum())
+
+
+def test_t3_zero_padded_round_trip(orc):
+    rng = np.random.default_rng(8)
+    x = np.zeros(128, np.float32)
+    x[:96] = rng.integers(-50, 50, size=96)
+    y = orc.fwht(x)
+    back = orc.fwht(y) / 128
+    assert np.array_equal(back[:96], x[:96]) and np.all(back[96:] == 0)
+
+
+# ----------------------------------------------------------------- T4 RoPE
+
+
+@pytest.mark.parametrize("theta", [1e4, 5e5, 1e6])
+@pytest.mark.parametrize("D", [96, 128])
+def test_t4_rope_table_closed_form(orc, theta, D):
+    pos = np.array([0, 1, 2, 17, 511, 4095, 32767, 131071], np.int32)
+    cs = orc.rope_table(len(pos), D, theta, positions=pos)
+    i = np.arange(D // 2)
+    ang = pos[:, None].astype(np.float64) * np.power(float(theta), -2.0 * i / D)[None, :]
+    # within one float32 ulp of the double-precision value
+    assert np.allclose(cs[..., 0], np.cos(ang), rtol=0, atol=1.2e-7)
+    assert np.allclose(cs[..., 1], np.sin(ang), rtol=0, atol=1.2e-7)
+    assert np.all(cs[0, :, 0] == 1.0) and np.all(cs[0, :, 1] == 0.0)
+    assert np.array_equal(cs[:, 0, 0], np.cos(pos.astype(np.float64)).astype(np.float32))
+
+
+def test_t4_rope_apply_matches_rotate_half_convention(orc):
+    """apply == q*cos + rotate_half(q)*sin with rotate_half(q) = (-q2, q1)."""
+    rng = np.random.default_rng(9)
+    D = 128
+    cs = orc.rope_table(64, D, 1e4)
+    for t in (0, 5, 63):
+        q = rng.normal(size=D).astype(np.float32)
+        c = np.concatenate([cs[t, :, 0], cs[t, :, 0]]).astype(np.float64)
+        s = np.concatenate([cs[t, :, 1], cs[t, :, 1]]).astype(np.float64)
+        rot = np.concatenate([-q[D // 2:], q[: D // 2]]).astype(np.float64)
+        ref = q * c + rot * s
+        assert np.allclose(orc.rope_apply(q, cs[t]), ref, atol=1e-6)
+
+
+@pytest.mark.parametrize("theta", [1e4, 5e5, 1e6])
+def test_t4_rope_remove_inverts_apply(orc, theta):
+    rng = np.random.default_rng(10)
+    D = 128
+    pos = np.array([0, 1, 1000, 65535, 131071], np.int32)
+    cs = orc.rope_table(len(pos), D, theta, positions=pos)
+    for t in range(len(pos)):
+        x = rng.normal(size=D).astype(np.float32) * 3
+        y = orc.rope_apply(x, cs[t])
+        back = orc.rope_remove(y, cs[t])
+        pair = np.sqrt(x[: D // 2] ** 2 + x[D // 2:] ** 2)
+        pair = np.concatenate([pair, pair])
+        assert np.all(np.abs(back - x) <= 4 * np.finfo(np.float32).eps * pair + 1e-30)
+        n0 = x[: D // 2].astype(np.float64) ** 2 + x[D // 2:].astype(np.float64) ** 2
+        n1 = y[: D // 2].astype(np.float64) ** 2 + y[D // 2:].astype(np.float64) ** 2
+        assert np.allclose(n0, n1, rtol=1e-6)
+        if pos[t] == 0:
+            assert np.array_equal(y, x)
+
+
+# ------------------------------------------------------------- binary16
+
+
+def test_h2f_all_codes_match_ieee(orc):
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = orc.h2f(codes)
+    ref = codes.view(np.float16).astype(np.float32)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+def test_f2h_round_to_nearest_even(orc):
+    rng = np.random.default_rng(12)
+    x = np.concatenate([
+        rng.normal(size=4000) * 10.0 ** rng.integers(-9, 5, size=4000),
+        np.arange(0, 2049, dtype=np.float64) * 2.0 ** -25,  # subnormal ties
+        [65504, 65519.99, 65520, 70000, -65520, 1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11, -0.0, 0.0],
+    ]).astype(np.float32)
+    ours = orc.f2h(x)
+    ref = x.astype(np.float16).view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+# ----------------------------------------------------------- group scale
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+@pytest.mark.parametrize("dp", [64, 128])
+def test_group_scale_is_smallest_non_clipping_half(orc, bits, dp):
+    step = dp * ((1 << bits) - 1) / 2
+    halves = np.arange(0, 0x7C00, dtype=np.uint32).astype(np.uint16).view(np.float16).astype(np.float64)
+    rng = np.random.default_rng(13)
+    amax = np.concatenate([
+        np.abs(rng.normal(size=300)) * 10.0 ** rng.integers(-8, 7, size=300),
+        halves[rng.integers(1, halves.size, size=100)] * step,  # exactly representable
+        [0.0, 1e-30, 2.0 ** -24 * step, 1.0, dp * 65504.0 * 1.41421],  # largest reachable
+    ]).astype(np.float32)
+    for a in amax:
+        v = orc.group_scale(a, bits, dp)
+        ok = halves * step >= np.float64(a)
+        expect = int(np.argmax(ok))
+        assert v == expect, (a, v, expect)
+
+
+# ----------------------------------------------------- T5 Figure-1 shape
+
+
+def test_t5_e8_mse_gain_over_integer_lattice(orc):
+    """Equal point density (det 1), high resolution: the mean squared error per
+    dimension of the E8 decoder is the normalized second moment G(E8); Z^8 gives
+    1/12.  A wrong decoder (dropped fix-up, wrong coset choice) is far off."""
+    g = _golden()["normalized_second_moment_e8"]
+    G = g["numerator"] / g["denominator"]
+    rng = np.random.default_rng(14)
+    u = rng.uniform(-40, 40, size=(200000, 8)).astype(np.float32)
+    r = orc.e8_nearest(u, 1, 0)
+    mse_e8 = ((u.astype(np.float64) - r) ** 2).mean()
+    mse_z = ((u.astype(np.float64) - np.rint(u)) ** 2).mean()
+    assert abs(mse_e8 - G) < 0.01 * G, mse_e8
+    assert abs(mse_z - 1 / 12) < 0.01 / 12
+    gain_db = 10 * np.log10(mse_z / mse_e8)
+    assert abs(gain_db - 10 * np.log10((1 / 12) / G)) < 0.06, gain_db
+
+
+@pytest.mark.parametrize("bits", [2, 3])
+def test_t5_relaxed_box_never_worse_than_scalar(orc, bits):
+    """The relaxed box codebook contains the scalar b-bit half-integer grid, so
+    per block it is never farther than scalar b-bit absmax quantisation."""
+    rng = np.random.default_rng(15 + bits)
+    h = ((1 << bits) - 1) / 2
+    u = rng.uniform(-h, h, size=(20000, 8)).astype(np.float32)
+    r = orc.e8_nearest(u, 0, bits)
+    scalar = np.clip(np.ceil(u) - 0.5, -h, h)
+    d_r = ((u.astype(np.float64) - r) ** 2).sum(1)
+    d_s = ((u.astype(np.float64) - scalar) ** 2).sum(1)
+    assert np.all(d_r <= d_s + 1e-6)
+
+
+# ------------------------------------------------------------- T7 format
+
+
+def _rand_fp16(rng, shape, scale=1.0):
+    return (rng.normal(size=shape) * scale).astype(np.float16).view(np.uint16)
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_t7_delta_round_trip_and_field_ranges(orc, bits):
+    rng = np.random.default_rng(16 + bits)
+    slices, T, D, G = 3, 77, 128, 64
+    x = _rand_fp16(rng, (slices, T, D))
+    idx, cos_, sc = orc.compress_tensor(x, T, D, bits, G, 1, 0)
+    idx_d, cos_d, sc_d = orc.compress_tensor(x, T, D, bits, G, 1, 32)
+    assert np.array_equal(sc, sc_d)
+    a = orc.decompress_tensor(idx, cos_, sc, slices, T, D, bits, G, 0)
+    b = orc.decompress_tensor(idx_d, cos_d, sc_d, slices, T, D, bits, G, 32)
+    assert np.array_equal(a, b)
+    # chunk starts are stored raw
+    rows = np.arange(slices * T) % T
+    assert np.array_equal(idx[rows % 32 == 0], idx_d[rows % 32 == 0])
+    # every field < L; integer-coset fields <= L - 2
+    L = 1 << bits
+    bitsarr = np.unpackbits(idx, axis=1, bitorder="little").reshape(idx.shape[0], D, bits)
+    fields = (bitsarr * (1 << np.arange(bits))).sum(-1)
+    assert fields.max() <= L - 1
+    coset_bit = (cos_[:, None] >> (np.arange(D) // 8)[None, :]) & 1
+    assert np.all(fields[coset_bit == 0] <= L - 2)
+
+
+def test_t7_delta_row_inverse(orc):
+    rng = np.random.default_rng(17)
+    for bits in (2, 3, 4):
+        rb = 128 * bits // 8
+        a = rng.integers(0, 256, size=rb).astype(np.uint8)
+        p = rng.integers(0, 256, size=rb).astype(np.uint8)
+        d, c = orc.delta_row(a, 0x1234, p, 0x0F0F, 128, bits)
+        back, c2 = orc.undelta_row(d, c, p, 0x0F0F, 128, bits)
+        assert np.array_equal(back, a) and c2 == 0x1234
+
+
+# ------------------------------------------- whole-row error bound (glue pin)
+
+
+@pytest.mark.parametrize("strict", [1, 0])
+@pytest.mark.parametrize("bits,D,G", [(2, 128, 64), (3, 128, 64), (3, 96, 64), (2, 128, 128), (4, 64, 32)])
+def test_row_reconstruction_error_bound(orc, strict, bits, D, G):
+    """||x - x_hat||^2 <= dp * sum_g sc_g^2 * (blocks in g) * c, c = 2 for the
+    relaxed code (it contains the scalar grid) and 4 for the strict one (one
+    fix-up step costs at most 2 more), plus binary16 output rounding.  Catches a
+    wrong Hadamard normalisation, scale divisor, code offset or packing."""
+    rng = np.random.default_rng(18 + bits + D + strict)
+    dp = orc.padded_dim(D)
+    c_blk = 4.0 if strict else 2.0
+    for trial in range(60):
+        x = _rand_fp16(rng, D, scale=float(10.0 ** rng.integers(-3, 3)))
+        idx, cw, sc = orc.encode_row(x, D, bits, G, strict)
+        xh = orc.decode_row(idx, cw, sc, D, bits, G)
+        xf = x.view(np.float16).astype(np.float64)
+        xhf = xh.view(np.float16).astype(np.float64)
+        scf = sc.view(np.float16).astype(np.float64)
+        bound = dp * (scf ** 2).sum() * (G // 8) * c_blk
+        err = ((xf - xhf) ** 2).sum()
+        slack = ((np.abs(xhf) + np.abs(xf)) * 2.0 ** -10).__pow__(2).sum() + 1e-12
+        assert err <= bound * (1 + 1e-4) + slack, (trial, err, bound)
+
+
+def test_row_exact_codebook_points_round_trip(orc):
+    """A row whose transform lands exactly on codebook points is reproduced."""
+    rng = np.random.default_rng(19)
+    bits, D, G = 3, 128, 64
+    for trial in range(20):
+        r = orc.e8_nearest(rng.uniform(-3.4, 3.4, size=(16, 8)).astype(np.float32), 0, bits).ravel()
+        # one whole half-integer block per group reaches the box edge, so the
+        # group scale comes out exactly sc
+        r[0:8] = [3.5, -0.5, 0.5, 0.5, -0.5, 0.5, 1.5, -2.5]
+        r[64:72] = [-3.5, 0.5, 2.5, -1.5, 0.5, 0.5, -0.5, 0.5]
+        sc = 2.0 ** -6
+        x = orc.fwht((r * sc).astype(np.float32))  # x = H (r * sc)
+        xb = x.astype(np.float16).view(np.uint16)
+        assert np.array_equal(xb.view(np.float16).astype(np.float32), x)  # exact in fp16
+        idx, cw, scl = orc.encode_row(xb, D, bits, G, 0)
+        xh = orc.decode_row(idx, cw, scl, D, bits, G)
+        assert np.array_equal(xh, xb)
