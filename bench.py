@@ -1,0 +1,396 @@
+#!/usr/bin/env python3
+"""Benchmark: E8 lattice KV-cache compress + decompress on one GB300 per rank.
+
+One step = the whole hot path over the Llama-3.1-8B-shaped cache (32 layers,
+batch 4, 8 KV heads, 32768 tokens, head_dim 128, fp16; K2V2, group 64, relaxed
+E8 unless --strict): compress K and V (RoPE removal, Hadamard, group scale, E8
+nearest point, 2-bit packing), then decompress the buffer back to fp16 K and V.
+
+value = fp16 K+V bytes consumed by compression plus fp16 K+V bytes produced by
+decompression, per second of device time (inputs resident in HBM; they are
+16 GiB, far larger than L2, so no flush is needed between steps).
+
+Prints one JSON line on rank 0.  `--impl reference` times the CPU oracle (the
+stand-in for the method's CPU-bound compression loop) on a bounded sample of
+the same workload instead.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+CSRC = os.path.join(ROOT, "e8_lattice_vector_gb300", "csrc")
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="llama31_8b")
+    ap.add_argument("--strict", action="store_true", help="strict E8 parity instead of relaxed")
+    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def _peak_hbm():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _kernel_src_hash():
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_record(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)[kernel]
+        if rec.get("src_hash") == _kernel_src_hash():
+            return rec
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q, "--format=csv,noheader,nounits",
+                 "-lms", "200", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    p = [x.strip() for x in line.split(",")]
+                    if len(p) < 9:
+                        continue
+                    try:
+                        sm.append(float(p[1]))
+                        smax.append(float(p[2]))
+                    except ValueError:
+                        continue
+                    for n, v in zip(names, p[5:9]):
+                        if v.lower() == "active":
+                            reasons.add(n)
+            os.unlink(self.path)
+        except Exception:
+            return None
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- our arm
+
+
+def run_ours(a):
+    import torch
+    import torch.distributed as dist
+
+    from e8_lattice_vector_gb300 import build as nqbuild
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    nqbuild.build()
+    import e8_lattice_vector_gb300 as nq
+    from e8_lattice_vector_gb300.synth import CONFIGS, make_cache
+
+    cfg = CONFIGS[a.config]
+    params = [m for m in cfg.modes if bool(m.strict) == a.strict] or list(cfg.modes)
+    params = params[0]
+    K, V = make_cache(cfg, device=dev)
+    rope = nq.RopeTable.build(cfg.tokens, cfg.head_dim, params.rope_theta, device=dev)
+    lay = nq.plan(cfg.shape, params)
+    buf = torch.empty(int(lay.total_bytes), dtype=torch.uint8, device=dev)
+    K2 = torch.empty_like(K)
+    V2 = torch.empty_like(V)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        nq.compress_kv(K, V, params, rope, out=buf)
+        if ev:
+            ev[1].record(stream)
+        nq.decompress_kv(buf, cfg.shape, params, rope, K_out=K2, V_out=V2)
+        if ev:
+            ev[2].record(stream)
+
+    for _ in range(max(a.warmup, 0)):
+        step()
+    torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(a.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(a.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    comp_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    decomp_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+
+    # ---- end to end through the public API with pinned host buffers
+    e2e = None
+    if a.e2e_steps > 0:
+        hK = torch.empty(K.shape, dtype=K.dtype, pin_memory=True)
+        hV = torch.empty(V.shape, dtype=V.dtype, pin_memory=True)
+        hK.copy_(K)
+        hV.copy_(V)
+        oK = torch.empty_like(hK, pin_memory=True)
+        oV = torch.empty_like(hV, pin_memory=True)
+
+        def e2e_step():
+            K.copy_(hK, non_blocking=True)
+            V.copy_(hV, non_blocking=True)
+            step()
+            oK.copy_(K2, non_blocking=True)
+            oV.copy_(V2, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(a.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1) / a.e2e_steps
+        if world > 1:
+            tt = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e_ms = float(tt.item())
+        e2e = {"value": round(world * 2 * cfg.fp16_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": int(hK.numel() * 2 + hV.numel() * 2),
+               "d2h_bytes_per_step": int(oK.numel() * 2 + oV.numel() * 2)}
+        del hK, hV, oK, oV
+
+    # ---- algorithmic bytes and roofline
+    rows = cfg.rows
+    fp16_row = cfg.head_dim * 2
+    rec_row = {"k": lay.k_idx_row_bytes + 2 + lay.scales_per_row * 2,
+               "v": lay.v_idx_row_bytes + 2 + lay.scales_per_row * 2}
+    alg_bytes = rows * (2 * fp16_row + rec_row["k"] + rec_row["v"])  # one direction, K + V
+    comp_avg = sum(comp_ms) / len(comp_ms)
+    decomp_avg = sum(decomp_ms) / len(decomp_ms)
+    peak, peak_kind = _peak_hbm()
+    kernels = {
+        "compress_kernel": {"ms": round(comp_avg, 4), "gbs": round(alg_bytes / (comp_avg * 1e-3) / 1e9, 1)},
+        "decompress_kernel": {"ms": round(decomp_avg, 4), "gbs": round(alg_bytes / (decomp_avg * 1e-3) / 1e9, 1)},
+    }
+    dom = "compress_kernel" if comp_avg >= decomp_avg else "decompress_kernel"
+    achieved = kernels[dom]["gbs"]
+    trec = _traffic_record(dom)
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                "traffic": (int(trec["dram_bytes_per_launch_pair"]) if trec else None),
+                "algorithmic_bytes": int(alg_bytes)}
+
+    ms_per_step = total_ms / a.steps
+    value = world * 2 * cfg.fp16_bytes / (ms_per_step * 1e-3) / 1e9
+    out = {
+        "metric": "KV compress/decompress GB/s (fp16 in) on 1 GB300; % of HBM roofline",
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": a.steps,
+        "warmup": a.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": "%s KV cache %s fp16, K%dV%d group %d %s E8, delta %s, compress+decompress round trip"
+                        % (cfg.name, list(cfg.shape), params.key_bits, params.value_bits, params.group_size,
+                           "strict" if params.strict else "relaxed", params.delta_chunk or "off"),
+            "fp16_bytes_per_direction": cfg.fp16_bytes,
+            "l2": "inputs (%.1f GiB) larger than L2; no flush" % (cfg.fp16_bytes / 2 ** 30),
+            "parallelism": "replicas" if world > 1 else "single",
+        },
+        "compress_gbs_fp16": round(cfg.fp16_bytes / (comp_avg * 1e-3) / 1e9, 2),
+        "decompress_gbs_fp16": round(cfg.fp16_bytes / (decomp_avg * 1e-3) / 1e9, 2),
+        "kernels": kernels,
+        "roofline": roofline,
+        "clocks": clk,
+        "e2e": e2e,
+        "gpu_launches": 4 * a.steps,
+    }
+    kv0 = (K[0, 0].cpu(), V[0, 0].cpu()) if rank == 0 and not a.no_cpu_baseline else None
+    del K, V, K2, V2, buf
+    torch.cuda.empty_cache()
+    if kv0 is not None:
+        out["cpu_baseline"] = cpu_baseline(cfg, params, a.cpu_seconds, kv0)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# --------------------------------------------------------- CPU oracle arm
+
+
+def _oracle_sample(cfg, params, target_s, kv0=None):
+    """A bounded sample of the workload: whole (layer 0, batch 0, head) slices of
+    K and V (given, or generated on the CPU); returns (round trip callable,
+    slices per call, seconds per slice)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from e8_lattice_vector_gb300.synth import layer_kv
+
+    T, D = cfg.tokens, cfg.head_dim
+    if kv0 is None:
+        k, v = layer_kv(cfg, 0, device="cpu")
+        kv0 = (k[0], v[0])
+    kb = kv0[0].contiguous().view(torch.int16).numpy().view(np.uint16)  # [H, T, D]
+    vb = kv0[1].contiguous().view(torch.int16).numpy().view(np.uint16)
+    cs = oracle.rope_table(T, D, params.rope_theta) if params.rope_theta > 0 else None
+
+    def round_trip(nslices):
+        for s in range(nslices):
+            h = s % kb.shape[0]
+            ki = oracle.compress_tensor(kb[h], T, D, params.key_bits, params.group_size, int(params.strict),
+                                        params.delta_chunk, cs)
+            vi = oracle.compress_tensor(vb[h], T, D, params.value_bits, params.group_size, int(params.strict),
+                                        params.delta_chunk, None)
+            oracle.decompress_tensor(*ki, 1, T, D, params.key_bits, params.group_size, params.delta_chunk, cs)
+            oracle.decompress_tensor(*vi, 1, T, D, params.value_bits, params.group_size, params.delta_chunk, None)
+
+    t0 = time.perf_counter()
+    round_trip(1)
+    per_slice = time.perf_counter() - t0
+    n = max(1, int(target_s / max(per_slice, 1e-6)))
+    return round_trip, n, per_slice
+
+
+def cpu_baseline(cfg, params, target_s, kv0=None):
+    rt, n, _ = _oracle_sample(cfg, params, target_s, kv0)
+    t0 = time.perf_counter()
+    rt(n)
+    dt = time.perf_counter() - t0
+    fp16 = 2 * 2 * n * cfg.tokens * cfg.head_dim * 2  # K+V, compressed and decompressed
+    return {"value": round(fp16 / dt / 1e9, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "%d (layer 0, batch 0, head) slices of %d tokens, K and V, compress+decompress, "
+                      "single-threaded plain C, %.1f s" % (n, cfg.tokens, dt)}
+
+
+def run_reference(a):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from e8_lattice_vector_gb300.synth import CONFIGS
+
+    cfg = CONFIGS[a.config]
+    params = [m for m in cfg.modes if bool(m.strict) == a.strict] or list(cfg.modes)
+    params = params[0]
+    per_step_s = max(1.0, a.cpu_seconds / max(a.steps, 1))
+    rt, n, _ = _oracle_sample(cfg, params, per_step_s)
+    for _ in range(max(a.warmup, 0)):
+        rt(1)
+    t0 = time.perf_counter()
+    for _ in range(a.steps):
+        rt(n)
+    dt = time.perf_counter() - t0
+    fp16 = 2 * 2 * n * cfg.tokens * cfg.head_dim * 2
+    value = fp16 * a.steps / dt / 1e9
+    sample = ("%d slices of %d tokens per step (layer 0, batch 0), K and V, compress+decompress, "
+              "single-threaded plain C" % (n, cfg.tokens))
+    out = {
+        "impl": "reference",
+        "metric": "KV compress/decompress GB/s (fp16 in) on 1 GB300; % of HBM roofline",
+        "value": round(value, 5), "unit": "GB/s", "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": round(dt / a.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "%s KV cache (sampled), K%dV%d group %d %s E8" % (
+            cfg.name, params.key_bits, params.value_bits, params.group_size,
+            "strict" if params.strict else "relaxed")},
+        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    a = _args()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)
+
+
+if __name__ == "__main__":
+    main()

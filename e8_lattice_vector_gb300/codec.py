@@ -1,0 +1,177 @@
+"""Python face of libnq: E8 lattice KV-cache compression on the GPU.
+
+    params = CodecParams(key_bits=2, value_bits=2, strict=False, rope_theta=5e5)
+    rope = RopeTable.build(tokens, head_dim, params.rope_theta, device="cuda")
+    buf = compress_kv(K, V, params, rope)           # uint8 device buffer
+    K2, V2 = decompress_kv(buf, shape_of(K), params, rope)
+
+K and V are contiguous fp16 CUDA tensors [layers, batch, kv_heads, tokens,
+head_dim] (a 4-D [layers, kv_heads, tokens, head_dim] tensor means batch 1).
+All work is enqueued on the current torch CUDA stream.
+"""
+import ctypes
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib
+
+__all__ = ["CodecParams", "RopeTable", "plan", "shape_of", "compress_kv", "decompress_kv",
+           "e8_nearest", "sections"]
+
+
+@dataclass(frozen=True)
+class CodecParams:
+    key_bits: int = 2
+    value_bits: int = 2
+    group_size: int = 64
+    strict: bool = False
+    delta_chunk: int = 0
+    rope_theta: float = 1e4
+
+    def c(self):
+        return _lib.Params(self.key_bits, self.value_bits, self.group_size, int(bool(self.strict)),
+                           self.delta_chunk, float(self.rope_theta))
+
+
+def shape_of(x):
+    """nq shape tuple (layers, batch, kv_heads, tokens, head_dim) of a K/V tensor."""
+    if x.dim() == 4:
+        L, H, T, D = x.shape
+        return (L, 1, H, T, D)
+    if x.dim() == 5:
+        return tuple(x.shape)
+    raise ValueError("K/V must be 4-D [L,H,T,D] or 5-D [L,B,H,T,D], got %s" % (tuple(x.shape),))
+
+
+def _cshape(shape):
+    return _lib.Shape(*[int(v) for v in shape])
+
+
+def plan(shape, params):
+    lay = _lib.Layout()
+    _lib.check("nq_plan", _lib.lib().nq_plan(ctypes_ref(_cshape(shape)), ctypes_ref(params.c()), ctypes_ref(lay)))
+    return lay
+
+
+def ctypes_ref(obj):
+    return ctypes.byref(obj)
+
+
+def _stream_handle(device):
+    return ctypes_void(torch.cuda.current_stream(device).cuda_stream)
+
+
+def ctypes_void(v):
+    return ctypes.c_void_p(int(v))
+
+
+class RopeTable:
+    """Device copy of the (cos, sin) table that nq_rope_table builds on the host
+    for given positions, theta and head_dim.  Build once, reuse for every call
+    on those tokens."""
+
+    def __init__(self, host, device_tensor, tokens, head_dim, theta):
+        self.host = host
+        self.device = device_tensor
+        self.tokens, self.head_dim, self.theta = tokens, head_dim, theta
+
+    @staticmethod
+    def host_table(tokens, head_dim, theta, positions=None):
+        host = torch.empty((tokens, head_dim // 2, 2), dtype=torch.float32)
+        pos = None
+        if positions is not None:
+            pos = torch.as_tensor(positions, dtype=torch.int32).contiguous()
+            if pos.numel() != tokens:
+                raise ValueError("positions must have `tokens` entries")
+        st = _lib.lib().nq_rope_table(None if pos is None else ctypes_void(pos.data_ptr()), int(tokens),
+                                      int(head_dim), float(theta), ctypes_void(host.data_ptr()))
+        _lib.check("nq_rope_table", st)
+        return host
+
+    @classmethod
+    def build(cls, tokens, head_dim, theta, positions=None, device="cuda"):
+        host = cls.host_table(tokens, head_dim, theta, positions)
+        return cls(host, host.to(device), tokens, head_dim, theta)
+
+
+def _rope_ptr(rope, params, tokens, head_dim):
+    if params.rope_theta <= 0:
+        return None
+    if rope is None:
+        raise ValueError("rope_theta > 0 needs a RopeTable for these tokens")
+    if rope.tokens != tokens or rope.head_dim != head_dim or rope.theta != params.rope_theta:
+        raise ValueError("RopeTable (%d tokens, head_dim %d, theta %g) does not match the call"
+                         % (rope.tokens, rope.head_dim, rope.theta))
+    return ctypes_void(rope.device.data_ptr())
+
+
+def _check_kv(x, name):
+    if not (x.is_cuda and x.dtype == torch.float16 and x.is_contiguous()):
+        raise ValueError("%s must be a contiguous fp16 CUDA tensor" % name)
+
+
+def compress_kv(K, V, params, rope=None, out=None):
+    """Compress K and V; returns (or fills) a uint8 device buffer of
+    plan(...).total_bytes bytes."""
+    _check_kv(K, "K")
+    _check_kv(V, "V")
+    shape = shape_of(K)
+    if shape_of(V) != shape:
+        raise ValueError("K and V shapes differ")
+    lay = plan(shape, params)
+    if out is None:
+        out = torch.empty(max(int(lay.total_bytes), 16), dtype=torch.uint8, device=K.device)
+    rp = _rope_ptr(rope, params, shape[3], shape[4])
+    st = _lib.lib().nq_compress_kv(ctypes_void(K.data_ptr()), ctypes_void(V.data_ptr()), rp,
+                                   ctypes_ref(_cshape(shape)), ctypes_ref(params.c()),
+                                   ctypes_void(out.data_ptr()), int(out.numel()), _stream_handle(K.device))
+    _lib.check("nq_compress_kv", st)
+    return out
+
+
+def decompress_kv(buf, shape, params, rope=None, K_out=None, V_out=None):
+    """Decompress a buffer produced by compress_kv; returns (K, V) fp16 tensors
+    of `shape` ([L,B,H,T,D])."""
+    shape = tuple(int(v) for v in shape)
+    if K_out is None:
+        K_out = torch.empty(shape, dtype=torch.float16, device=buf.device)
+    if V_out is None:
+        V_out = torch.empty(shape, dtype=torch.float16, device=buf.device)
+    _check_kv(K_out, "K_out")
+    _check_kv(V_out, "V_out")
+    rp = _rope_ptr(rope, params, shape[3], shape[4])
+    st = _lib.lib().nq_decompress_kv(ctypes_void(buf.data_ptr()), int(buf.numel()), rp,
+                                     ctypes_ref(_cshape(shape)), ctypes_ref(params.c()),
+                                     ctypes_void(K_out.data_ptr()), ctypes_void(V_out.data_ptr()),
+                                     _stream_handle(buf.device))
+    _lib.check("nq_decompress_kv", st)
+    return K_out, V_out
+
+
+def e8_nearest(u, strict, bits):
+    """Nearest E8 codebook point of each 8-block of a float32 CUDA tensor [..., 8]."""
+    if not (u.is_cuda and u.dtype == torch.float32 and u.is_contiguous() and u.shape[-1] == 8):
+        raise ValueError("u must be a contiguous float32 CUDA tensor [..., 8]")
+    out = torch.empty_like(u)
+    st = _lib.lib().nq_e8_nearest(ctypes_void(u.data_ptr()), ctypes_void(out.data_ptr()), u.numel() // 8,
+                                  int(bool(strict)), int(bits), _stream_handle(u.device))
+    _lib.check("nq_e8_nearest", st)
+    return out
+
+
+def sections(buf, lay):
+    """Views of the six sections of a compressed buffer (uint8 idx rows, int16
+    coset words, fp16 scales), following the layout from plan()."""
+    rows = int(lay.rows)
+
+    def view(off, nbytes):
+        return buf[int(off): int(off) + nbytes]
+
+    out = {}
+    for t, rb in (("k", int(lay.k_idx_row_bytes)), ("v", int(lay.v_idx_row_bytes))):
+        out[t + "_idx"] = view(getattr(lay, t + "_idx"), rows * rb).view(rows, rb)
+        out[t + "_coset"] = view(getattr(lay, t + "_coset"), rows * 2).view(torch.int16)
+        spr = int(lay.scales_per_row)
+        out[t + "_scale"] = view(getattr(lay, t + "_scale"), rows * spr * 2).view(torch.float16).view(rows, spr)
+    return out

@@ -1,0 +1,254 @@
+// nq_api.cu -- the C ABI of libnq: argument validation, the compressed-buffer
+// layout, the RoPE table, and dispatch to the kernels.
+#include <cmath>
+#include <cstring>
+
+#include "nq_internal.h"
+
+namespace nq {
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+uint64_t align256(uint64_t v) { return (v + 255u) & ~uint64_t(255u); }
+
+int padded_dim(int head_dim) { return head_dim <= 64 ? 64 : 128; }
+
+int check(const nq_shape* s, const nq_params* p) {
+    if (!s || !p) return NQ_ERR_ARG;
+    if (s->layers < 0 || s->batch < 0 || s->kv_heads < 0 || s->tokens < 0) return NQ_ERR_ARG;
+    if (s->head_dim != 64 && s->head_dim != 96 && s->head_dim != 128) return NQ_ERR_UNSUPPORTED;
+    if (p->key_bits < 2 || p->key_bits > 4 || p->value_bits < 2 || p->value_bits > 4)
+        return NQ_ERR_UNSUPPORTED;
+    const int dp = padded_dim(s->head_dim);
+    if (p->group_size != 32 && p->group_size != 64 && p->group_size != 128) return NQ_ERR_UNSUPPORTED;
+    if (p->group_size > dp) return NQ_ERR_UNSUPPORTED;
+    if (p->strict != 0 && p->strict != 1) return NQ_ERR_ARG;
+    if (p->delta_chunk < 0 || (p->delta_chunk % 32) != 0) return NQ_ERR_ARG;
+    if (!std::isfinite(p->rope_theta)) return NQ_ERR_ARG;
+    return NQ_OK;
+}
+
+void make_layout(const nq_shape* s, const nq_params* p, nq_layout* L) {
+    const int dp = padded_dim(s->head_dim);
+    const uint64_t rows = uint64_t(s->layers) * s->batch * s->kv_heads * s->tokens;
+    std::memset(L, 0, sizeof(*L));
+    L->version = NQ_FORMAT_VERSION;
+    L->padded_dim = uint32_t(dp);
+    L->rows = rows;
+    L->k_idx_row_bytes = uint64_t(dp) * p->key_bits / 8;
+    L->v_idx_row_bytes = uint64_t(dp) * p->value_bits / 8;
+    L->scales_per_row = uint64_t(dp / p->group_size);
+    uint64_t off = 0;
+    L->k_idx = off;
+    off = align256(off + rows * L->k_idx_row_bytes);
+    L->k_coset = off;
+    off = align256(off + rows * 2);
+    L->k_scale = off;
+    off = align256(off + rows * L->scales_per_row * 2);
+    L->v_idx = off;
+    off = align256(off + rows * L->v_idx_row_bytes);
+    L->v_coset = off;
+    off = align256(off + rows * 2);
+    L->v_scale = off;
+    off = align256(off + rows * L->scales_per_row * 2);
+    L->total_bytes = off;
+}
+
+}  // namespace
+
+int grid_capacity(const void* kernel) {
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess)
+        return -1;
+    if (per_sm <= 0) return -1;  // the kernel cannot be resident at all
+    return sms * per_sm;
+}
+
+// ------------------------------------------------------------ e8 test entry
+
+template <int BITS, bool STRICT>
+__global__ void e8_nearest_kernel(const float* __restrict__ u, float* __restrict__ out, int64_t n) {
+    for (int64_t b = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; b < n;
+         b += int64_t(gridDim.x) * blockDim.x) {
+        float v[8], r[8];
+        float umax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            v[j] = u[8 * b + j];
+            umax = fmaxf(umax, fabsf(v[j]));
+        }
+        if constexpr (BITS > 0) {
+            using C = Code<BITS>;
+            if (umax < C::H) {
+                // the path compression takes for in-box blocks
+                unsigned c;
+                const unsigned code = e8_fast<BITS, STRICT>(v, c);
+                const float off = c ? C::H : C::HI0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    r[j] = __fsub_rn(float((code >> (j * BITS)) & C::MASK), off);
+            } else {
+                e8_general(v, STRICT, C::HI0, C::H, r);
+            }
+        } else {
+            e8_general(v, STRICT, INFINITY, INFINITY, r);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) out[8 * b + j] = r[j];
+    }
+}
+
+template <int BITS>
+static int launch_e8(const float* u, float* out, int64_t n, bool strict, cudaStream_t st) {
+    const int64_t want = (n + 255) / 256;
+    const int grid = int(std::min<int64_t>(want, 4096));
+    if (strict)
+        e8_nearest_kernel<BITS, true><<<grid, 256, 0, st>>>(u, out, n);
+    else
+        e8_nearest_kernel<BITS, false><<<grid, 256, 0, st>>>(u, out, n);
+    return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
+}
+
+int launch_e8_nearest(const float* u, float* out, int64_t n, bool strict, int bits, cudaStream_t st) {
+    switch (bits) {
+        case 0:
+            return launch_e8<0>(u, out, n, strict, st);
+        case 2:
+            return launch_e8<2>(u, out, n, strict, st);
+        case 3:
+            return launch_e8<3>(u, out, n, strict, st);
+        case 4:
+            return launch_e8<4>(u, out, n, strict, st);
+        default:
+            return NQ_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace nq
+
+// =================================================================== C ABI
+
+extern "C" {
+
+int nq_plan(const nq_shape* shape, const nq_params* params, nq_layout* out) {
+    const int st = nq::check(shape, params);
+    if (st != NQ_OK) return st;
+    if (!out) return NQ_ERR_ARG;
+    nq::make_layout(shape, params, out);
+    return NQ_OK;
+}
+
+int nq_rope_table(const int32_t* positions, int32_t tokens, int32_t head_dim, float rope_theta,
+                  float* table) {
+    if (tokens < 0 || head_dim <= 0 || (head_dim & 1) || !(rope_theta > 0.0f) ||
+        !std::isfinite(rope_theta))
+        return NQ_ERR_ARG;
+    if (tokens > 0 && !table) return NQ_ERR_ARG;
+    const int half = head_dim / 2;
+    for (int32_t t = 0; t < tokens; ++t) {
+        const double p = positions ? double(positions[t]) : double(t);
+        float* row = table + size_t(t) * size_t(head_dim);
+        for (int i = 0; i < half; ++i) {
+            const double angle = p * std::pow(double(rope_theta), -2.0 * double(i) / double(head_dim));
+            row[2 * i] = float(std::cos(angle));
+            row[2 * i + 1] = float(std::sin(angle));
+        }
+    }
+    return NQ_OK;
+}
+
+int nq_compress_kv(const void* k_f16, const void* v_f16, const float* rope_table,
+                   const nq_shape* shape, const nq_params* params, void* out, size_t out_bytes,
+                   void* stream) {
+    int st = nq::check(shape, params);
+    if (st != NQ_OK) return st;
+    nq_layout L;
+    nq::make_layout(shape, params, &L);
+    if (L.rows == 0) return NQ_OK;
+    const bool rope = params->rope_theta > 0.0f;
+    if (!k_f16 || !v_f16 || !out || (rope && !rope_table)) return NQ_ERR_ARG;
+    if (!nq::aligned16(k_f16) || !nq::aligned16(v_f16) || !nq::aligned16(out) ||
+        (rope && !nq::aligned16(rope_table)))
+        return NQ_ERR_ARG;
+    if (out_bytes < L.total_bytes) return NQ_ERR_SIZE;
+    nq::LaunchArgs a;
+    a.slices = int64_t(shape->layers) * shape->batch * shape->kv_heads;
+    a.tokens = shape->tokens;
+    a.group = params->group_size;
+    a.delta_chunk = params->delta_chunk;
+    a.stream = static_cast<cudaStream_t>(stream);
+    uint8_t* base = static_cast<uint8_t*>(out);
+    st = nq::launch_compress_tensor(a, shape->head_dim, params->key_bits, params->strict != 0, k_f16,
+                                    rope ? rope_table : nullptr, base + L.k_idx,
+                                    reinterpret_cast<uint16_t*>(base + L.k_coset),
+                                    reinterpret_cast<uint16_t*>(base + L.k_scale));
+    if (st != NQ_OK) return st;
+    return nq::launch_compress_tensor(a, shape->head_dim, params->value_bits, params->strict != 0,
+                                      v_f16, nullptr, base + L.v_idx,
+                                      reinterpret_cast<uint16_t*>(base + L.v_coset),
+                                      reinterpret_cast<uint16_t*>(base + L.v_scale));
+}
+
+int nq_decompress_kv(const void* in, size_t in_bytes, const float* rope_table,
+                     const nq_shape* shape, const nq_params* params, void* k_f16_out,
+                     void* v_f16_out, void* stream) {
+    int st = nq::check(shape, params);
+    if (st != NQ_OK) return st;
+    nq_layout L;
+    nq::make_layout(shape, params, &L);
+    if (L.rows == 0) return NQ_OK;
+    const bool rope = params->rope_theta > 0.0f;
+    if (!in || !k_f16_out || !v_f16_out || (rope && !rope_table)) return NQ_ERR_ARG;
+    if (!nq::aligned16(in) || !nq::aligned16(k_f16_out) || !nq::aligned16(v_f16_out) ||
+        (rope && !nq::aligned16(rope_table)))
+        return NQ_ERR_ARG;
+    if (in_bytes < L.total_bytes) return NQ_ERR_SIZE;
+    nq::LaunchArgs a;
+    a.slices = int64_t(shape->layers) * shape->batch * shape->kv_heads;
+    a.tokens = shape->tokens;
+    a.group = params->group_size;
+    a.delta_chunk = params->delta_chunk;
+    a.stream = static_cast<cudaStream_t>(stream);
+    const uint8_t* base = static_cast<const uint8_t*>(in);
+    st = nq::launch_decompress_tensor(a, shape->head_dim, params->key_bits, base + L.k_idx,
+                                      reinterpret_cast<const uint16_t*>(base + L.k_coset),
+                                      reinterpret_cast<const uint16_t*>(base + L.k_scale),
+                                      rope ? rope_table : nullptr, k_f16_out);
+    if (st != NQ_OK) return st;
+    return nq::launch_decompress_tensor(a, shape->head_dim, params->value_bits, base + L.v_idx,
+                                        reinterpret_cast<const uint16_t*>(base + L.v_coset),
+                                        reinterpret_cast<const uint16_t*>(base + L.v_scale), nullptr,
+                                        v_f16_out);
+}
+
+int nq_e8_nearest(const float* u, float* out, int64_t n_blocks, int strict, int bits, void* stream) {
+    if (n_blocks < 0 || (strict != 0 && strict != 1)) return NQ_ERR_ARG;
+    if (bits != 0 && (bits < 2 || bits > 4)) return NQ_ERR_UNSUPPORTED;
+    if (n_blocks == 0) return NQ_OK;
+    if (!u || !out) return NQ_ERR_ARG;
+    return nq::launch_e8_nearest(u, out, n_blocks, strict != 0, bits,
+                                 static_cast<cudaStream_t>(stream));
+}
+
+const char* nq_strerror(int status) {
+    switch (status) {
+        case NQ_OK:
+            return "ok";
+        case NQ_ERR_ARG:
+            return "invalid argument (null, misaligned or out-of-range value)";
+        case NQ_ERR_UNSUPPORTED:
+            return "unsupported head_dim, bit width or group size";
+        case NQ_ERR_SIZE:
+            return "caller buffer smaller than the planned size";
+        case NQ_ERR_CUDA:
+            return "CUDA launch or runtime error";
+        default:
+            return "unknown status";
+    }
+}
+
+}  // extern "C"

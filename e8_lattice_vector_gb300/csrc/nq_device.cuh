@@ -1,0 +1,305 @@
+// nq_device.cuh -- device building blocks of the E8 KV-cache codec (sm_103a).
+//
+// Arithmetic contract: every floating-point operation that decides a code is
+// written with an explicit IEEE intrinsic (__fadd_rn, __fmul_rn, __fmaf_rn ...)
+// and the library is built with --fmad=false, so the compiler fuses nothing on
+// its own.  The op order is the one the method's steps define:
+//   RoPE removal   x_i' = fma(x_i, c, x_j*s),  x_j' = fma(x_j, c, -(x_i*s))
+//   Hadamard       textbook butterflies, stages h = 1, 2, 4, ..., Dp/2
+//   scaling        u = y * inv,  inv = 1 / (sc * Dp)
+//   E8 distances   d = fma(e_j, e_j, d) over j = 0..7, plus 1 - 2*score for a
+//                  parity fix-up, as fma(-2, score, 1) added to d.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace nq {
+
+constexpr unsigned kFull = 0xffffffffu;
+// 1.5 * 2^23: for |x| < 2^22, (x + kMagic) rounds x to the nearest integer
+// with ties to even (kMagic is even) and keeps that integer in the low
+// mantissa bits; (x + kMagic) - kMagic is then rint(x) exactly.
+constexpr float kMagic = 12582912.0f;
+
+template <int BITS>
+struct Code {
+    static constexpr int L = 1 << BITS;
+    static constexpr unsigned MASK = L - 1;
+    static constexpr int BLOCK_BITS = 8 * BITS;
+    static constexpr float HI0 = float(L / 2 - 1);   // integer-coset box edge
+    static constexpr float H = float(L - 1) * 0.5f;  // half-coset box edge
+    static constexpr unsigned OFF0 = L / 2 - 1;      // code of integer 0
+    // high bit of each of the 8 fields of a block code (SWAR mod-2^b ops)
+    static constexpr unsigned FIELD_HI =
+        (1u << (BITS - 1)) * (1u | (1u << BITS) | (1u << 2 * BITS) | (1u << 3 * BITS) |
+                              (1u << 4 * BITS) | (1u << 5 * BITS) | (1u << 6 * BITS) |
+                              (1u << 7 * BITS));
+};
+
+// Field-wise (a - b) mod 2^b and (a + b) mod 2^b of 8 packed b-bit fields.
+template <int BITS>
+__device__ __forceinline__ unsigned swar_sub(unsigned a, unsigned b) {
+    constexpr unsigned H = Code<BITS>::FIELD_HI;
+    return ((a | H) - (b & ~H)) ^ ((a ^ ~b) & H);
+}
+template <int BITS>
+__device__ __forceinline__ unsigned swar_add(unsigned a, unsigned b) {
+    constexpr unsigned H = Code<BITS>::FIELD_HI;
+    return ((a & ~H) + (b & ~H)) ^ ((a ^ b) & H);
+}
+
+// ------------------------------------------------------------------ Hadamard
+
+template <int N>
+__device__ __forceinline__ void fwht(float (&y)[N]) {
+#pragma unroll
+    for (int h = 1; h < N; h *= 2) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            if ((i & h) == 0) {
+                float a = y[i], b = y[i + h];
+                y[i] = __fadd_rn(a, b);
+                y[i + h] = __fsub_rn(a, b);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------- scale
+
+// Smallest binary16 v with v * step >= amax (step = Dp * (2^b - 1) / 2), as
+// bits.  Candidate: amax / step rounded to fp16; it is at most one fp16 step
+// away from the answer, and the products v * step are exact in fp32.
+__device__ __forceinline__ unsigned short group_scale(float amax, float step) {
+    if (!(amax > 0.0f)) return 0;
+    float q = __fdiv_rn(amax, step);
+    unsigned short v = __half_as_ushort(__float2half_rn(q));
+    if (__fmul_rn(__half2float(__ushort_as_half(v)), step) < amax) {
+        ++v;
+    } else if (v > 0 && __fmul_rn(__half2float(__ushort_as_half((unsigned short)(v - 1))), step) >= amax) {
+        --v;
+    }
+    return v;
+}
+
+// ------------------------------------------------------------- E8 decoder
+
+// General decoder for one coset: rounding clamped into [-hi, hi] (hi = +inf
+// for the unbounded lattice), optional even-sum fix-up on the coordinate of
+// largest score (|e| for a step toward u, -|e| for a step away from it, first
+// index on ties).  Writes the point, returns the squared distance.
+__device__ __forceinline__ float coset_general(const float (&u)[8], bool half, bool parity,
+                                               float hi, float (&r)[8]) {
+    float e[8];
+    int sum = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        float v = half ? __fsub_rn(ceilf(u[j]), 0.5f) : rintf(u[j]);
+        v = fminf(fmaxf(v, -hi), hi);
+        r[j] = v;
+        e[j] = __fsub_rn(u[j], v);
+        sum += __float2int_rn(half ? __fsub_rn(v, 0.5f) : v);
+    }
+    float d = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) d = __fmaf_rn(e[j], e[j], d);
+    if (parity && (sum & 1)) {
+        int k = 0;
+        float best = 0.0f, best_dir = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float dir = (e[j] >= 0.0f) ? 1.0f : -1.0f;
+            float score = fabsf(e[j]);
+            float moved = __fadd_rn(r[j], dir);
+            if (moved > hi || moved < -hi) {
+                dir = -dir;
+                score = -score;
+            }
+            if (j == 0 || score > best) {
+                k = j;
+                best = score;
+                best_dir = dir;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (j == k) r[j] = __fadd_rn(r[j], best_dir);
+        d = __fadd_rn(d, __fmaf_rn(-2.0f, best, 1.0f));
+    }
+    return d;
+}
+
+// Nearest codebook point, general path.  Returns the coset (0 / 1).
+__device__ __forceinline__ int e8_general(const float (&u)[8], bool strict, float hi0, float h,
+                                          float (&r)[8]) {
+    float r0[8], r1[8];
+    float d0 = coset_general(u, false, true, hi0, r0);
+    float d1 = coset_general(u, true, strict, h, r1);
+    bool c = d1 < d0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) r[j] = c ? r1[j] : r0[j];
+    return c ? 1 : 0;
+}
+
+// Fast path, valid when every |u_j| < (2^b - 1)/2 (then no rounding leaves the
+// box and the half-integer fix-up never needs to turn around).  Computes the
+// same codes as the general path:
+//   e~0 = rint(u) - u  (exact, never -0), the half-integer point is
+//   rint(u) + 1/2 if e~0 < 0 else rint(u) - 1/2  (= ceil(u) - 1/2), and its
+//   residual e~1 = e~0 -+ 1/2 (exact), the integer score is
+//   min(|e~0|, hi0 - |u|) (the turned-around step at the box edge).
+// Output: block code (8 fields of b bits, coordinate j at bit j*b) and coset.
+template <int BITS, bool STRICT>
+__device__ __forceinline__ unsigned e8_fast(const float (&u)[8], unsigned& coset) {
+    using C = Code<BITS>;
+    float eb0[8], eb1[8], s0[8];
+    float d0 = 0.0f, d1 = 0.0f;
+    float smax0 = -1.0f, smax1 = -1.0f;
+    unsigned code0 = 0, negmask = 0, xpar = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        float t = __fadd_rn(u[j], kMagic);
+        float r0 = __fsub_rn(t, kMagic);
+        float e0 = __fsub_rn(r0, u[j]);
+        float e1 = __fsub_rn(e0, copysignf(0.5f, e0));
+        eb0[j] = e0;
+        eb1[j] = e1;
+        d0 = __fmaf_rn(e0, e0, d0);
+        d1 = __fmaf_rn(e1, e1, d1);
+        unsigned m = (__float_as_uint(t) + C::OFF0) & C::MASK;
+        code0 |= m << (j * BITS);
+        xpar ^= m;
+        negmask |= (__float_as_uint(e0) >> 31) << j;
+        s0[j] = fminf(fabsf(e0), __fsub_rn(C::HI0, fabsf(u[j])));
+        smax0 = fmaxf(smax0, s0[j]);
+        smax1 = fmaxf(smax1, fabsf(e1));
+    }
+    // half-integer codes: m1 = m0 + [e~0 < 0]
+    unsigned inc = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) inc |= ((negmask >> j) & 1u) << (j * BITS);
+    const bool odd0 = (xpar & 1u) != 0;
+    const bool odd1 = STRICT && (((xpar ^ (unsigned)__popc(negmask)) & 1u) != 0);
+    float dd0 = odd0 ? __fadd_rn(d0, __fmaf_rn(-2.0f, smax0, 1.0f)) : d0;
+    float dd1 = odd1 ? __fadd_rn(d1, __fmaf_rn(-2.0f, smax1, 1.0f)) : d1;
+    const bool half = dd1 < dd0;
+    unsigned code = half ? code0 + inc : code0;
+    const bool fix = half ? odd1 : odd0;
+    if (fix) {
+        const float smax = half ? smax1 : smax0;
+        int k = 0;
+        float ek = 0.0f;
+#pragma unroll
+        for (int j = 7; j >= 0; --j) {
+            float s = half ? fabsf(eb1[j]) : s0[j];
+            float e = half ? eb1[j] : eb0[j];
+            if (s == smax) {
+                k = j;
+                ek = e;
+            }
+        }
+        // step toward u (u - r >= 0 <=> e~ <= 0), turned around at the box edge
+        const int mk = (int)((code >> (k * BITS)) & C::MASK);
+        const int mmax = half ? C::L - 1 : C::L - 2;
+        int dir = (ek <= 0.0f) ? 1 : -1;
+        if (mk + dir > mmax || mk + dir < 0) dir = -dir;
+        code += (unsigned)dir << (k * BITS);
+    }
+    coset = half ? 1u : 0u;
+    return code;
+}
+
+// Block code of a general-path point.
+template <int BITS>
+__device__ __forceinline__ unsigned pack_point(const float (&r)[8], int coset) {
+    using C = Code<BITS>;
+    const float off = coset ? C::H : C::HI0;
+    unsigned code = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) code |= (unsigned)__float2int_rn(__fadd_rn(r[j], off)) << (j * BITS);
+    return code;
+}
+
+// ------------------------------------------------------------ fp16 <-> fp32
+
+__device__ __forceinline__ void h8_to_f(const uint4& v, float* y) {
+    const __half2* h = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        float2 f = __half22float2(h[q]);
+        y[2 * q] = f.x;
+        y[2 * q + 1] = f.y;
+    }
+}
+
+__device__ __forceinline__ uint4 f_to_h8(const float* y) {
+    uint4 v;
+    __half2* h = reinterpret_cast<__half2*>(&v);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) h[q] = __floats2half2_rn(y[2 * q], y[2 * q + 1]);
+    return v;
+}
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_stream(uint4* p, const uint4& v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+// ----------------------------------------------------------- row records
+
+// Block codes <-> the row's idx bytes (coordinate i's field at bit i*b).
+// NB = number of 8-blocks in the row (Dp / 8).  Words are little-endian.
+template <int BITS, int NB>
+struct RowPack {
+    static constexpr int WORDS = NB * BITS / 4;  // 32-bit words per row
+    __device__ static __forceinline__ void pack(const unsigned (&blk)[NB], unsigned (&w)[WORDS]) {
+        if constexpr (BITS == 2) {
+#pragma unroll
+            for (int i = 0; i < WORDS; ++i) w[i] = blk[2 * i] | (blk[2 * i + 1] << 16);
+        } else if constexpr (BITS == 4) {
+#pragma unroll
+            for (int i = 0; i < WORDS; ++i) w[i] = blk[i];
+        } else {  // 24-bit blocks: 4 blocks -> 3 words
+#pragma unroll
+            for (int g = 0; g < NB / 4; ++g) {
+                unsigned b0 = blk[4 * g], b1 = blk[4 * g + 1], b2 = blk[4 * g + 2], b3 = blk[4 * g + 3];
+                w[3 * g] = b0 | (b1 << 24);
+                w[3 * g + 1] = (b1 >> 8) | (b2 << 16);
+                w[3 * g + 2] = (b2 >> 16) | (b3 << 8);
+            }
+        }
+    }
+    __device__ static __forceinline__ void unpack(const unsigned (&w)[WORDS], unsigned (&blk)[NB]) {
+        if constexpr (BITS == 2) {
+#pragma unroll
+            for (int i = 0; i < WORDS; ++i) {
+                blk[2 * i] = w[i] & 0xffffu;
+                blk[2 * i + 1] = w[i] >> 16;
+            }
+        } else if constexpr (BITS == 4) {
+#pragma unroll
+            for (int i = 0; i < WORDS; ++i) blk[i] = w[i];
+        } else {
+#pragma unroll
+            for (int g = 0; g < NB / 4; ++g) {
+                unsigned w0 = w[3 * g], w1 = w[3 * g + 1], w2 = w[3 * g + 2];
+                blk[4 * g] = w0 & 0xffffffu;
+                blk[4 * g + 1] = (w0 >> 24) | ((w1 & 0xffffu) << 8);
+                blk[4 * g + 2] = (w1 >> 16) | ((w2 & 0xffu) << 16);
+                blk[4 * g + 3] = w2 >> 8;
+            }
+        }
+    }
+};
+
+}  // namespace nq

@@ -1,0 +1,44 @@
+// nq_internal.h -- declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "../../include/nq.h"
+#include "nq_device.cuh"
+
+namespace nq {
+
+constexpr int kThreads = 256;
+constexpr int kWarpsPerBlock = kThreads / 32;
+
+template <int D>
+struct PaddedDim {
+    static constexpr int value = D <= 64 ? 64 : 128;
+};
+
+struct LaunchArgs {
+    int64_t slices;  // layers * batch * kv_heads
+    int tokens;
+    int group;
+    int delta_chunk;
+    cudaStream_t stream;
+};
+
+// Blocks of kThreads that fit on the current device at once for `kernel`;
+// -1 when the device or the kernel cannot be queried.
+int grid_capacity(const void* kernel);
+
+int launch_compress_tensor(const LaunchArgs& a, int head_dim, int bits, bool strict, const void* x,
+                           const float* rope, uint8_t* idx, uint16_t* coset, uint16_t* scales);
+
+int launch_decompress_tensor(const LaunchArgs& a, int head_dim, int bits, const uint8_t* idx,
+                             const uint16_t* coset, const uint16_t* scales, const float* rope,
+                             void* x_out);
+
+int launch_e8_nearest(const float* u, float* out, int64_t n_blocks, bool strict, int bits,
+                      cudaStream_t stream);
+
+}  // namespace nq

@@ -1,0 +1,151 @@
+/*
+ * nq.h -- C ABI of libnq: E8 lattice KV-cache compression on GB300 (sm_103a).
+ *
+ * The method (NexusQuant write-ups, "E8 walkthrough" post and the paper "E8
+ * Lattice Key Quantization for Low-Bit KV-Cache Compression"): after prefill,
+ * keys have their rotary embedding removed; keys and values get a
+ * Walsh-Hadamard rotation over head_dim (zero-padded to a power of two), a
+ * per-group absmax scale, and a nearest-point search in the E8 lattice per
+ * 8-float block (Conway-Sloane two-coset decoder, strict or relaxed parity);
+ * the lattice codes are packed into b-bit indices, optionally delta-coded
+ * across tokens.  Decompression inverts every step.
+ *
+ * Conventions for every entry point:
+ *  - Plain C types; no allocation and no freeing inside the library; the
+ *    caller owns every buffer.  Device pointers must be 16-byte aligned.
+ *  - Work is enqueued on `stream` (a cudaStream_t passed as void*, NULL = the
+ *    legacy default stream) and is asynchronous: a return of NQ_OK means the
+ *    launch was accepted.  Launch failures return NQ_ERR_CUDA; the CUDA error
+ *    state is left for the caller to inspect.
+ *  - Arguments are validated before anything is enqueued; on any error
+ *    nothing has been written.
+ *  - Inputs must be finite; NaN or infinite inputs give unspecified codes.
+ *
+ * Tensor layout: K and V are contiguous fp16 [layers, batch, kv_heads,
+ * tokens, head_dim] (for batch 1 this is [layers, kv_heads, tokens,
+ * head_dim]).  A "row" is one head_dim vector; rows are numbered in that
+ * order, so row = ((l * batch + b) * kv_heads + h) * tokens + t.
+ *
+ * Compressed buffer (format version NQ_FORMAT_VERSION), sections in the
+ * order below, each starting at a 256-byte aligned offset given by nq_plan:
+ *   K idx   [rows][Dp * key_bits / 8]   bytes
+ *   K coset [rows]                       uint16, bit k = coset of block k
+ *   K scale [rows][Dp / group_size]      fp16
+ *   V idx / V coset / V scale            the same with value_bits.
+ * Dp = padded head_dim (64 for head_dim 64, 128 for 96 and 128).  Within an
+ * idx row, coordinate i's code sits at bit i*b, least significant bit first,
+ * little-endian bytes; code = lattice coordinate + offset, offset = 2^(b-1)-1
+ * for the integer coset and (2^b - 1)/2 for the half-integer coset.  With
+ * delta coding on, every row whose token index is not a multiple of
+ * delta_chunk holds its codes minus the previous token's codes (per field,
+ * modulo 2^b) and its coset word XOR the previous one; scales are never
+ * delta-coded.
+ */
+#ifndef NQ_H
+#define NQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define NQ_FORMAT_VERSION 1u
+
+enum {
+    NQ_OK = 0,
+    NQ_ERR_ARG = 1,         /* null pointer, bad shape, misaligned pointer  */
+    NQ_ERR_UNSUPPORTED = 2, /* head_dim, bit width or group size not served */
+    NQ_ERR_SIZE = 3,        /* a caller buffer is smaller than required     */
+    NQ_ERR_CUDA = 4         /* a CUDA call or kernel launch failed          */
+};
+
+/* Cache shape.  head_dim in {64, 96, 128}; tokens >= 0; zero-sized tensors
+ * are accepted and do nothing. */
+typedef struct {
+    int32_t layers, batch, kv_heads, tokens, head_dim;
+} nq_shape;
+
+/* Codec parameters.
+ *  key_bits, value_bits: 2, 3 or 4 bits per coordinate ("K3V2", "K2V2").
+ *  group_size: 32, 64 or 128 coordinates per fp16 scale; must divide Dp.
+ *  strict: 1 = strict E8 (both cosets even-sum), 0 = relaxed parity (the
+ *          half-integer coset drops its even-sum rule).
+ *  delta_chunk: 0 = no temporal delta; otherwise a positive multiple of 32:
+ *          codes are delta-coded along tokens and the chain restarts at every
+ *          token index that is a multiple of delta_chunk (one chain per
+ *          (layer, batch, head) slice when delta_chunk >= tokens).
+ *  rope_theta: > 0 keys carry split-half RoPE with this base and a table from
+ *          nq_rope_table is required; <= 0 keys are treated like values. */
+typedef struct {
+    int32_t key_bits, value_bits;
+    int32_t group_size;
+    int32_t strict;
+    int32_t delta_chunk;
+    float rope_theta;
+} nq_params;
+
+/* Byte offsets and sizes of the compressed buffer's sections. */
+typedef struct {
+    uint32_t version;
+    uint32_t padded_dim;
+    uint64_t rows; /* rows per tensor */
+    uint64_t k_idx_row_bytes, v_idx_row_bytes, scales_per_row;
+    uint64_t k_idx, k_coset, k_scale, v_idx, v_coset, v_scale;
+    uint64_t total_bytes;
+} nq_layout;
+
+/* Validate shape and params and describe the compressed buffer.  Host only.
+ * Format: the section table above; the method's "lattice indices (packed
+ * uint8)" and "one FP16 scale per group" ("E8 walkthrough", sections "Bit
+ * Rate Accounting" and "Why Per-Group Scaling?"). */
+int nq_plan(const nq_shape* shape, const nq_params* params, nq_layout* out);
+
+/* RoPE (cos, sin) table for split-half rotary embedding ("E8 walkthrough",
+ * "What Makes This Hard in Practice", item 2; README "Supported models").
+ * Host only, double precision rounded once to fp32:
+ *   table[t][i][0] = cos(p_t * theta^(-2i/head_dim)),
+ *   table[t][i][1] = sin(p_t * theta^(-2i/head_dim)),  i < head_dim/2,
+ * p_t = positions[t] (host int32), or t when positions is NULL.
+ * table: caller-owned host buffer of tokens * head_dim floats.  Build it once
+ * per (positions, theta, head_dim), copy it to the device and pass it to
+ * nq_compress_kv / nq_decompress_kv. */
+int nq_rope_table(const int32_t* positions, int32_t tokens, int32_t head_dim, float rope_theta,
+                  float* table);
+
+/* Compress K and V (device fp16, layout above) into `out` (device,
+ * out_bytes >= nq_plan().total_bytes).  rope_table: device copy of the
+ * nq_rope_table() table for these tokens, required when rope_theta > 0,
+ * ignored otherwise.  Steps: RoPE removal on keys, zero-padded Hadamard
+ * rotation ("E8 quantizes 8 numbers at once", "Handling outliers"), group
+ * absmax scale, two-coset E8 nearest point ("E8 walkthrough", "The
+ * Conway-Sloane Nearest-Point Algorithm"; relaxed parity per "What Makes E8
+ * Special", "The Relaxed Parity Discovery"), b-bit packing, temporal delta
+ * ("Negative results", delta coding entry). */
+int nq_compress_kv(const void* k_f16, const void* v_f16, const float* rope_table,
+                   const nq_shape* shape, const nq_params* params, void* out, size_t out_bytes,
+                   void* stream);
+
+/* Decompress `in` (device, produced by nq_compress_kv with the same shape and
+ * params) into K and V (device fp16, layout above): undo the delta, unpack,
+ * unscale, inverse Hadamard, re-apply RoPE to keys, round to fp16 ("E8
+ * walkthrough", quantize() dequantizes the lattice point; "What Makes This
+ * Hard in Practice": RoPE removed before quantization and reapplied after). */
+int nq_decompress_kv(const void* in, size_t in_bytes, const float* rope_table,
+                     const nq_shape* shape, const nq_params* params, void* k_f16_out,
+                     void* v_f16_out, void* stream);
+
+/* Nearest point of the E8 codebook for n_blocks 8-float blocks ("E8
+ * walkthrough", nearest_point()).  u, out: device float [n_blocks][8].
+ * bits = 0: the unbounded lattice (|u| < 2^22 required); bits in 2..4: the
+ * box-constrained codebook of a b-bit code.  Test and inspection entry. */
+int nq_e8_nearest(const float* u, float* out, int64_t n_blocks, int strict, int bits, void* stream);
+
+/* Static description of a status code. */
+const char* nq_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,272 @@
+"""GPU (libnq, through its C ABI) against the CPU oracle on the same seeded
+inputs.  Codes, coset words and scales must be bit-exact; reconstructions
+within max |diff| <= 1e-3 and MSE(gpu, oracle) / mean(oracle^2) <= 1e-5."""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+RECON_ATOL = 1e-3
+RECON_REL_MSE = 1e-5
+
+
+@pytest.fixture(scope="module")
+def nq():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from e8_lattice_vector_gb300 import build as nqbuild
+
+    nqbuild.build()
+    import e8_lattice_vector_gb300 as nq
+
+    return nq
+
+
+def _bits(x):
+    """fp16 tensor -> numpy uint16 bit patterns."""
+    return x.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _oracle_compress(orc, K, V, params):
+    L, B, H, T, D = K.shape
+    cs = orc.rope_table(T, D, params.rope_theta) if params.rope_theta > 0 else None
+    k = orc.compress_tensor(_bits(K).reshape(-1, T, D), T, D, params.key_bits, params.group_size,
+                            int(params.strict), params.delta_chunk, cs)
+    v = orc.compress_tensor(_bits(V).reshape(-1, T, D), T, D, params.value_bits, params.group_size,
+                            int(params.strict), params.delta_chunk, None)
+    return k, v, cs
+
+
+def _gpu_sections(nq, buf, shape, params):
+    lay = nq.plan(shape, params)
+    s = nq.sections(buf, lay)
+    out = {}
+    for t in ("k", "v"):
+        out[t] = (s[t + "_idx"].cpu().numpy(), s[t + "_coset"].cpu().numpy().view(np.uint16),
+                  s[t + "_scale"].contiguous().view(torch.int16).cpu().numpy().view(np.uint16))
+    return out
+
+
+def _assert_recon(gpu_bits, ref_bits):
+    g = gpu_bits.view(np.float16).astype(np.float64)
+    r = ref_bits.view(np.float16).astype(np.float64)
+    assert np.max(np.abs(g - r)) <= RECON_ATOL
+    denom = max(np.mean(r ** 2), 1e-30)
+    assert np.mean((g - r) ** 2) / denom <= RECON_REL_MSE
+
+
+def _round_trip_check(nq, orc, K, V, params, expect_exact_recon=True):
+    shape = tuple(K.shape)
+    L, B, H, T, D = shape
+    rope = nq.RopeTable.build(T, D, params.rope_theta) if params.rope_theta > 0 else None
+    buf = nq.compress_kv(K, V, params, rope)
+    (k_ref, v_ref, cs) = _oracle_compress(orc, K, V, params)
+    got = _gpu_sections(nq, buf, shape, params)
+    for name, ref in (("k", k_ref), ("v", v_ref)):
+        gi, gc, gs = got[name]
+        ri, rc, rs = ref
+        assert np.array_equal(gs, rs), name + " scales"
+        assert np.array_equal(gc, rc), name + " coset words"
+        assert np.array_equal(gi, ri), name + " idx"
+    K2, V2 = nq.decompress_kv(buf, shape, params, rope)
+    torch.cuda.synchronize()
+    kd = orc.decompress_tensor(*k_ref, L * B * H, T, D, params.key_bits, params.group_size,
+                               params.delta_chunk, cs)
+    vd = orc.decompress_tensor(*v_ref, L * B * H, T, D, params.value_bits, params.group_size,
+                               params.delta_chunk, None)
+    for g, r in ((K2, kd), (V2, vd)):
+        gb = _bits(g).reshape(r.shape)
+        _assert_recon(gb, r)
+        if expect_exact_recon:
+            assert np.array_equal(gb, r)
+    return buf
+
+
+# ---------------------------------------------------------------- decoder
+
+
+@pytest.mark.parametrize("bits", [0, 2, 3, 4])
+@pytest.mark.parametrize("strict", [1, 0])
+def test_e8_nearest_bit_exact(nq, orc, bits, strict):
+    rng = np.random.default_rng(40 + bits + 7 * strict)
+    h = ((1 << bits) - 1) / 2 if bits else 3.0
+    u = rng.uniform(-1.1 * h, 1.1 * h, size=(50000, 8)).astype(np.float32)
+    u[:3000] = np.round(u[:3000] * 2) / 2  # ties
+    u[3000:4000] = 0.0
+    u[4000:4500] = -0.0
+    if bits:
+        u[4500:5000] = np.clip(u[4500:5000], -h, h)  # on the box edge
+    got = nq.e8_nearest(torch.from_numpy(u).cuda(), strict, bits).cpu().numpy()
+    ref = orc.e8_nearest(u, strict, bits)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)) or np.array_equal(got, ref)
+    mism = np.nonzero(np.any(got != ref, axis=1))[0]
+    assert mism.size == 0, (mism[:5], u[mism[:1]], got[mism[:1]], ref[mism[:1]])
+
+
+# ------------------------------------------------------------- tiny cache
+
+
+def test_tiny_cache_full_parity(nq, orc):
+    from e8_lattice_vector_gb300.synth import CONFIGS, make_cache
+
+    cfg = CONFIGS["tiny"]
+    K, V = make_cache(cfg, device="cuda")
+    for params in cfg.modes:
+        _round_trip_check(nq, orc, K, V, params)
+
+
+# ------------------------------------------------- combinations, ragged tails
+
+
+COMBOS = [
+    # shape [L,B,H,T,D], key_bits, value_bits, group, strict, delta, theta
+    ((2, 1, 3, 77, 128), 3, 2, 64, 0, 0, 1e4),
+    ((2, 1, 3, 77, 128), 2, 2, 64, 1, 0, 1e4),
+    ((1, 2, 2, 130, 128), 4, 3, 32, 1, 32, 5e5),
+    ((1, 2, 2, 130, 128), 2, 4, 128, 0, 64, 1e6),
+    ((2, 2, 2, 100, 96), 3, 2, 64, 0, 32, 1e4),
+    ((1, 1, 4, 65, 96), 2, 3, 128, 1, 0, 1e4),
+    ((1, 1, 4, 65, 64), 3, 2, 64, 1, 32, 1e4),
+    ((1, 1, 3, 40, 64), 4, 2, 32, 0, 0, 0.0),
+    ((1, 1, 2, 300, 128), 3, 2, 64, 1, 256, 1e4),
+    ((1, 1, 2, 33, 128), 2, 2, 64, 0, 512, 1e4),
+]
+
+
+@pytest.mark.parametrize("shape,kb,vb,g,strict,delta,theta", COMBOS)
+def test_combinations_parity(nq, orc, shape, kb, vb, g, strict, delta, theta):
+    from e8_lattice_vector_gb300 import CodecParams
+
+    torch.manual_seed(hash((shape, kb, vb, g, strict, delta)) % (1 << 31))
+    K = (torch.randn(shape, device="cuda") * torch.exp(torch.randn(shape[-1], device="cuda") * 0.7)).half()
+    V = torch.randn(shape, device="cuda").half()
+    params = CodecParams(kb, vb, g, bool(strict), delta, theta)
+    _round_trip_check(nq, orc, K, V, params)
+
+
+# -------------------------------------------------------------- edge cases
+
+
+def _edge_inputs(kind, shape):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7)
+    if kind == "zeros":
+        return torch.zeros(shape, device="cuda").half(), torch.zeros(shape, device="cuda").half()
+    if kind == "neg_zeros":
+        z = torch.full(shape, -0.0, device="cuda").half()
+        return z, z.clone()
+    if kind == "constant":  # every group's scale is exact: the general (clamping) path
+        return torch.full(shape, 0.75, device="cuda").half(), torch.full(shape, -3.0, device="cuda").half()
+    if kind == "fp16_max":
+        x = torch.randn(shape, generator=g, device="cuda").sign() * 65504.0
+        return x.half(), (x * 0.5).half()
+    if kind == "tiny":  # subnormal fp16 inputs and scales
+        x = torch.randn(shape, generator=g, device="cuda") * 1e-6
+        return x.half(), (x * 0.01).half()
+    if kind == "sparse":
+        x = torch.randn(shape, generator=g, device="cuda")
+        x = torch.where(torch.rand(shape, generator=g, device="cuda") < 0.9, torch.zeros_like(x), x)
+        return x.half(), (x * 3).half()
+    if kind == "quantized":  # values on a coarse grid: many exact ties
+        x = torch.round(torch.randn(shape, generator=g, device="cuda") * 4) / 4
+        return x.half(), torch.round(torch.randn(shape, generator=g, device="cuda")).half()
+    raise ValueError(kind)
+
+
+@pytest.mark.parametrize("kind", ["zeros", "neg_zeros", "constant", "fp16_max", "tiny", "sparse", "quantized"])
+@pytest.mark.parametrize("strict", [1, 0])
+def test_edge_cases_parity(nq, orc, kind, strict):
+    from e8_lattice_vector_gb300 import CodecParams
+
+    shape = (1, 1, 2, 45, 128)
+    K, V = _edge_inputs(kind, shape)
+    for kb, vb in ((3, 2), (2, 2), (4, 4)):
+        params = CodecParams(kb, vb, 64, bool(strict), 32, 1e4)
+        _round_trip_check(nq, orc, K, V, params)
+
+
+@pytest.mark.parametrize("T", [1, 2, 31, 32, 33])
+def test_short_sequences(nq, orc, T):
+    from e8_lattice_vector_gb300 import CodecParams
+
+    shape = (1, 1, 3, T, 128)
+    K = torch.randn(shape, device="cuda").half()
+    V = torch.randn(shape, device="cuda").half()
+    _round_trip_check(nq, orc, K, V, CodecParams(3, 2, 64, False, 32, 1e4))
+
+
+def test_empty_cache_is_noop(nq):
+    from e8_lattice_vector_gb300 import CodecParams
+
+    K = torch.zeros((2, 1, 8, 0, 128), device="cuda").half()
+    buf = nq.compress_kv(K, K.clone(), CodecParams(), nq.RopeTable.build(0, 128, 1e4))
+    K2, V2 = nq.decompress_kv(buf, K.shape, CodecParams(), nq.RopeTable.build(0, 128, 1e4))
+    assert K2.numel() == 0
+
+
+# ------------------------------------------- full-size caches, sampled rows
+
+
+def _sample_rows(rng, cfg, n):
+    rows = cfg.rows
+    pick = rng.choice(rows, size=n, replace=False)
+    # always include chunk boundaries and the first/last token of a slice
+    T = cfg.tokens
+    extra = np.array([0, T - 1, T, rows - 1, 255 if T > 256 else 1, 256 if T > 256 else 1])
+    return np.unique(np.concatenate([pick, extra]) % rows)
+
+
+@pytest.mark.parametrize("name", ["mistral7b", "phi3mini", "llama31_8b", "qwen25_14b"])
+def test_full_size_sampled_parity(nq, orc, name):
+    """Each full-size cache compressed and decompressed by the same library call
+    the benchmark times; a sample of rows re-computed one by one by the oracle."""
+    from e8_lattice_vector_gb300.synth import CONFIGS, make_cache
+
+    cfg = CONFIGS[name]
+    K, V = make_cache(cfg, device="cuda")
+    T, D = cfg.tokens, cfg.head_dim
+    rng = np.random.default_rng(1234)
+    rows = _sample_rows(rng, cfg, 600)
+    cs = None
+    for params in cfg.modes[:2]:
+        rope = nq.RopeTable.build(T, D, params.rope_theta)
+        if cs is None:
+            cs = rope.host.numpy()
+        buf = nq.compress_kv(K, V, params, rope)
+        got = _gpu_sections(nq, buf, cfg.shape, params)
+        Kf = K.view(-1, D)
+        Vf = V.view(-1, D)
+        rows_t = torch.from_numpy(rows).cuda()
+        prev_t = torch.from_numpy(np.maximum(rows - 1, 0)).cuda()
+        for name_t, X, bits, rope_on in (("k", Kf, params.key_bits, True), ("v", Vf, params.value_bits, False)):
+            xr = _bits(X[rows_t])
+            xp = _bits(X[prev_t])
+            gi, gc, gs = got[name_t]
+            for n, r in enumerate(rows):
+                t = int(r % T)
+                csr = cs[t] if rope_on else None
+                idx, cw, sc = orc.encode_row(xr[n], D, bits, params.group_size, int(params.strict), csr)
+                if params.delta_chunk and t % params.delta_chunk != 0:
+                    pidx, pcw, _ = orc.encode_row(xp[n], D, bits, params.group_size, int(params.strict),
+                                                  cs[t - 1] if rope_on else None)
+                    idx, cw = orc.delta_row(idx, cw, pidx, pcw, orc.padded_dim(D), bits)
+                assert np.array_equal(gs[r], sc), (name_t, r)
+                assert gc[r] == cw, (name_t, r)
+                assert np.array_equal(gi[r], idx), (name_t, r)
+        # decompression of the same rows against the oracle's decoding of the
+        # (already verified) GPU records, restored from the raw codes
+        K2, V2 = nq.decompress_kv(buf, cfg.shape, params, rope)
+        for name_t, X2, bits, rope_on in (("k", K2, params.key_bits, True), ("v", V2, params.value_bits, False)):
+            xr2 = _bits(X2.view(-1, D)[torch.from_numpy(rows).cuda()])
+            xr = _bits((K if name_t == "k" else V).view(-1, D)[torch.from_numpy(rows).cuda()])
+            ref = np.empty_like(xr2)
+            for n, r in enumerate(rows):
+                t = int(r % T)
+                csr = cs[t] if rope_on else None
+                idx, cw, sc = orc.encode_row(xr[n], D, bits, params.group_size, int(params.strict), csr)
+                ref[n] = orc.decode_row(idx, cw, sc, D, bits, params.group_size, csr)
+            _assert_recon(xr2, ref)
+            assert np.array_equal(xr2, ref)
+        del buf, K2, V2
+        torch.cuda.empty_cache()

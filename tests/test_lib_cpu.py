@@ -1,0 +1,146 @@
+"""Host-side checks of libnq that need no GPU: the library loads, exports every
+symbol include/nq.h declares, and its host-only entry points (layout, RoPE
+table, argument validation) behave as specified."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def nq():
+    from e8_lattice_vector_gb300 import build as nqbuild
+
+    nqbuild.build()
+    from e8_lattice_vector_gb300 import _lib
+
+    return _lib
+
+
+def _declared_functions():
+    with open(os.path.join(ROOT, "include", "nq.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(nq_\w+)\s*\(", text, re.M)))
+
+
+def test_exports_every_declared_symbol(nq):
+    names = _declared_functions()
+    assert len(names) >= 6
+    L = nq.lib()
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(nq.SIGNATURES)
+
+
+def test_strerror(nq):
+    L = nq.lib()
+    for s in range(5):
+        assert L.nq_strerror(s)
+    assert b"unknown" in L.nq_strerror(99)
+
+
+def _plan(nq, shape, **kw):
+    p = dict(key_bits=3, value_bits=2, group_size=64, strict=0, delta_chunk=0, rope_theta=1e4)
+    p.update(kw)
+    lay = nq.Layout()
+    st = nq.lib().nq_plan(ctypes.byref(nq.Shape(*shape)), ctypes.byref(nq.Params(**p)), ctypes.byref(lay))
+    return st, lay
+
+
+@pytest.mark.parametrize("shape,kb,vb,g", [((1, 1, 8, 512, 128), 3, 2, 64), ((2, 2, 3, 77, 96), 3, 2, 32),
+                                           ((1, 1, 1, 5, 64), 4, 4, 64), ((3, 1, 2, 100, 128), 2, 2, 128)])
+def test_plan_sizes_match_oracle_format(nq, orc, shape, kb, vb, g):
+    st, lay = _plan(nq, shape, key_bits=kb, value_bits=vb, group_size=g)
+    assert st == 0
+    rows = int(np.prod(shape[:4]))
+    D = shape[4]
+    dp = orc.padded_dim(D)
+    assert lay.version == 1 and lay.padded_dim == dp and lay.rows == rows
+    x = np.zeros((rows // shape[3], shape[3], D), np.uint16)
+    for off, bits in (("k", kb), ("v", vb)):
+        idx, cos_, sc = orc.compress_tensor(x, shape[3], D, bits, g, 0, 0)
+        assert getattr(lay, off + "_idx_row_bytes") == idx.shape[1]
+        assert lay.scales_per_row == sc.shape[1]
+    offs = [lay.k_idx, lay.k_coset, lay.k_scale, lay.v_idx, lay.v_coset, lay.v_scale, lay.total_bytes]
+    assert all(o % 256 == 0 for o in offs) and offs == sorted(offs)
+    assert lay.k_coset - lay.k_idx >= rows * lay.k_idx_row_bytes
+    assert lay.total_bytes - lay.v_scale >= rows * lay.scales_per_row * 2
+
+
+def test_plan_rejects_bad_arguments(nq):
+    ok = (1, 1, 8, 64, 128)
+    assert _plan(nq, ok)[0] == 0
+    assert _plan(nq, (1, 1, 8, 64, 80))[0] == nq.NQ_ERR_UNSUPPORTED
+    assert _plan(nq, (1, 1, 8, 64, 256))[0] == nq.NQ_ERR_UNSUPPORTED
+    assert _plan(nq, ok, key_bits=1)[0] == nq.NQ_ERR_UNSUPPORTED
+    assert _plan(nq, ok, value_bits=5)[0] == nq.NQ_ERR_UNSUPPORTED
+    assert _plan(nq, ok, group_size=48)[0] == nq.NQ_ERR_UNSUPPORTED
+    assert _plan(nq, (1, 1, 8, 64, 64), group_size=128)[0] == nq.NQ_ERR_UNSUPPORTED
+    assert _plan(nq, ok, delta_chunk=40)[0] == nq.NQ_ERR_ARG
+    assert _plan(nq, ok, delta_chunk=-32)[0] == nq.NQ_ERR_ARG
+    assert _plan(nq, ok, strict=2)[0] == nq.NQ_ERR_ARG
+    assert _plan(nq, (1, -1, 8, 64, 128))[0] == nq.NQ_ERR_ARG
+    assert _plan(nq, ok, rope_theta=float("inf"))[0] == nq.NQ_ERR_ARG
+    st, lay = _plan(nq, (0, 1, 8, 64, 128))
+    assert st == 0 and lay.rows == 0
+
+
+def test_compress_validates_before_touching_the_gpu(nq):
+    """Error paths return before any CUDA call (so they run without a GPU)."""
+    L = nq.lib()
+    shape = nq.Shape(1, 1, 8, 64, 128)
+    good = nq.Params(2, 2, 64, 0, 0, 1e4)
+    p16 = ctypes.c_void_p(16)
+    # null pointers
+    assert L.nq_compress_kv(None, p16, p16, ctypes.byref(shape), ctypes.byref(good), p16, 1 << 30, None) == nq.NQ_ERR_ARG
+    # rope on but no table
+    assert L.nq_compress_kv(p16, p16, None, ctypes.byref(shape), ctypes.byref(good), p16, 1 << 30, None) == nq.NQ_ERR_ARG
+    # misaligned
+    p17 = ctypes.c_void_p(17)
+    assert L.nq_compress_kv(p17, p16, p16, ctypes.byref(shape), ctypes.byref(good), p16, 1 << 30, None) == nq.NQ_ERR_ARG
+    # output too small
+    assert L.nq_compress_kv(p16, p16, p16, ctypes.byref(shape), ctypes.byref(good), p16, 100, None) == nq.NQ_ERR_SIZE
+    assert L.nq_decompress_kv(p16, 100, p16, ctypes.byref(shape), ctypes.byref(good), p16, p16, None) == nq.NQ_ERR_SIZE
+    bad = nq.Params(2, 7, 64, 0, 0, 1e4)
+    assert L.nq_compress_kv(p16, p16, p16, ctypes.byref(shape), ctypes.byref(bad), p16, 1 << 30, None) == nq.NQ_ERR_UNSUPPORTED
+    # empty tensors are a no-op
+    empty = nq.Shape(1, 1, 8, 0, 128)
+    assert L.nq_compress_kv(None, None, None, ctypes.byref(empty), ctypes.byref(good), None, 0, None) == 0
+    assert L.nq_e8_nearest(None, None, 0, 1, 2, None) == 0
+    assert L.nq_e8_nearest(p16, p16, 5, 1, 5, None) == nq.NQ_ERR_UNSUPPORTED
+    assert L.nq_e8_nearest(p16, p16, -1, 1, 2, None) == nq.NQ_ERR_ARG
+
+
+@pytest.mark.parametrize("T,D,theta", [(512, 128, 1e4), (2048, 96, 1e4), (300, 128, 5e5), (1000, 64, 1e6)])
+def test_rope_table_equals_oracle_bit_for_bit(nq, orc, T, D, theta):
+    host = np.zeros((T, D // 2, 2), np.float32)
+    st = nq.lib().nq_rope_table(None, T, D, theta, host.ctypes.data_as(ctypes.c_void_p))
+    assert st == 0
+    ref = orc.rope_table(T, D, theta)
+    assert np.array_equal(host.view(np.uint32), ref.view(np.uint32))
+
+
+def test_rope_table_positions_and_errors(nq, orc):
+    pos = np.array([5, 0, 131071, 77], np.int32)
+    host = np.zeros((4, 64, 2), np.float32)
+    L = nq.lib()
+    assert L.nq_rope_table(pos.ctypes.data_as(ctypes.c_void_p), 4, 128, 1e6, host.ctypes.data_as(ctypes.c_void_p)) == 0
+    assert np.array_equal(host, orc.rope_table(4, 128, 1e6, positions=pos))
+    assert L.nq_rope_table(None, 4, 127, 1e4, host.ctypes.data_as(ctypes.c_void_p)) == nq.NQ_ERR_ARG
+    assert L.nq_rope_table(None, 4, 128, 0.0, host.ctypes.data_as(ctypes.c_void_p)) == nq.NQ_ERR_ARG
+    assert L.nq_rope_table(None, 4, 128, 1e4, None) == nq.NQ_ERR_ARG
+
+
+def test_package_has_no_cpu_path():
+    """The product package never imports the oracle."""
+    pkg = os.path.join(ROOT, "e8_lattice_vector_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                with open(os.path.join(dirpath, f)) as fh:
+                    src = fh.read()
+                assert "import oracle" not in src and "from oracle" not in src and "nq_oracle" not in src, f
