@@ -233,12 +233,17 @@ __device__ __forceinline__ void h8_to_f(const uint4& v, float* y) {
     }
 }
 
+// Round to fp16 (nearest even), saturating at +-65504: a finite input never
+// comes back as an infinity.
+__device__ __forceinline__ unsigned f2_to_h2_sat(float lo, float hi) {
+    unsigned r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 __device__ __forceinline__ uint4 f_to_h8(const float* y) {
-    uint4 v;
-    __half2* h = reinterpret_cast<__half2*>(&v);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) h[q] = __floats2half2_rn(y[2 * q], y[2 * q + 1]);
-    return v;
+    return make_uint4(f2_to_h2_sat(y[0], y[1]), f2_to_h2_sat(y[2], y[3]), f2_to_h2_sat(y[4], y[5]),
+                      f2_to_h2_sat(y[6], y[7]));
 }
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {

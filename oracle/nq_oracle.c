@@ -286,7 +286,9 @@ void orc_decode_row(const uint8_t* idx, uint16_t coset, const uint16_t* scales,
     /* x = H (r * sc): H H = dp I and u = y / (sc * dp) */
     orc_fwht(y, dp);
     if (cs_row) orc_rope_apply(y, head_dim, cs_row);
-    for (int i = 0; i < head_dim; ++i) x_out[i] = orc_f2h_rn(y[i]);
+    /* Reading: the cache was finite, so the reconstruction saturates at the
+     * largest finite fp16 value instead of overflowing to infinity. */
+    for (int i = 0; i < head_dim; ++i) x_out[i] = orc_f2h_rn(fmaxf(fminf(y[i], 65504.0f), -65504.0f));
 }
 
 /* [NEG, temporal delta entry]: subtract the previous token's index.  Reading:

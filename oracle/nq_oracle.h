@@ -68,7 +68,8 @@ int orc_e8_block(const float* u, int strict, int bits, float* r);
 void orc_e8_nearest(const float* u, float* r, int64_t n_blocks, int strict, int bits);
 
 /* One row: raw codes (no delta).  x: D fp16 values; cs_row NULL for values or
- * when RoPE is off.  idx: dp*bits/8 bytes; scales: dp/group fp16. */
+ * when RoPE is off.  idx: dp*bits/8 bytes; scales: dp/group fp16.  Decoding
+ * saturates at +-65504 (a finite cache never reconstructs to infinity). */
 void orc_encode_row(const uint16_t* x, const float* cs_row, int head_dim, int bits, int group,
                     int strict, uint8_t* idx, uint16_t* coset, uint16_t* scales);
 void orc_decode_row(const uint8_t* idx, uint16_t coset, const uint16_t* scales,

@@ -447,3 +447,13 @@ def test_row_exact_codebook_points_round_trip(orc):
         idx, cw, scl = orc.encode_row(xb, D, bits, G, 0)
         xh = orc.decode_row(idx, cw, scl, D, bits, G)
         assert np.array_equal(xh, xb)
+
+
+def test_decode_saturates_at_fp16_max(orc):
+    """A cache of +-65504 values reconstructs to finite values (no infinities)."""
+    rng = np.random.default_rng(20)
+    x = (np.sign(rng.normal(size=128)) * 65504.0).astype(np.float16).view(np.uint16)
+    for bits in (2, 3, 4):
+        idx, cw, sc = orc.encode_row(x, 128, bits, 64, 1)
+        xh = orc.decode_row(idx, cw, sc, 128, bits, 64).view(np.float16)
+        assert np.all(np.isfinite(xh)) and np.max(np.abs(xh.astype(np.float64))) <= 65504.0
