@@ -27,7 +27,8 @@ class Params(ctypes.Structure):
 
 
 class Layout(ctypes.Structure):
-    _fields_ = [("version", ctypes.c_uint32), ("padded_dim", ctypes.c_uint32), ("rows", ctypes.c_uint64),
+    _fields_ = [("version", ctypes.c_uint32), ("padded_dim", ctypes.c_uint32),
+                ("tokens_padded", ctypes.c_uint32), ("reserved", ctypes.c_uint32), ("rows", ctypes.c_uint64),
                 ("k_idx_row_bytes", ctypes.c_uint64), ("v_idx_row_bytes", ctypes.c_uint64),
                 ("scales_per_row", ctypes.c_uint64),
                 ("k_idx", ctypes.c_uint64), ("k_coset", ctypes.c_uint64), ("k_scale", ctypes.c_uint64),

@@ -160,18 +160,26 @@ def e8_nearest(u, strict, bits):
     return out
 
 
-def sections(buf, lay):
+def sections(buf, lay, tokens=None):
     """Views of the six sections of a compressed buffer (uint8 idx rows, int16
-    coset words, fp16 scales), following the layout from plan()."""
+    coset words, fp16 scales), following the layout from plan().  Rows are
+    record rows (slices * tokens_padded); with `tokens` given, the views are
+    [slices, tokens, ...] with the padding rows dropped."""
     rows = int(lay.rows)
+    tp = int(lay.tokens_padded)
 
     def view(off, nbytes):
         return buf[int(off): int(off) + nbytes]
 
+    def shape(x):
+        if tokens is None or tp == 0:
+            return x
+        return x.view(rows // tp, tp, *x.shape[1:])[:, :tokens]
+
     out = {}
     for t, rb in (("k", int(lay.k_idx_row_bytes)), ("v", int(lay.v_idx_row_bytes))):
-        out[t + "_idx"] = view(getattr(lay, t + "_idx"), rows * rb).view(rows, rb)
-        out[t + "_coset"] = view(getattr(lay, t + "_coset"), rows * 2).view(torch.int16)
+        out[t + "_idx"] = shape(view(getattr(lay, t + "_idx"), rows * rb).view(rows, rb))
+        out[t + "_coset"] = shape(view(getattr(lay, t + "_coset"), rows * 2).view(torch.int16))
         spr = int(lay.scales_per_row)
-        out[t + "_scale"] = view(getattr(lay, t + "_scale"), rows * spr * 2).view(torch.float16).view(rows, spr)
+        out[t + "_scale"] = shape(view(getattr(lay, t + "_scale"), rows * spr * 2).view(torch.float16).view(rows, spr))
     return out

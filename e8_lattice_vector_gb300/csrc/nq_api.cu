@@ -1,7 +1,11 @@
 // nq_api.cu -- the C ABI of libnq: argument validation, the compressed-buffer
 // layout, the RoPE table, and dispatch to the kernels.
+#include <cudaTypedefs.h>
+
+#include <atomic>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 
 #include "nq_internal.h"
 
@@ -30,12 +34,16 @@ int check(const nq_shape* s, const nq_params* p) {
     return NQ_OK;
 }
 
+int pad_tokens(int tokens) { return (tokens + 31) / 32 * 32; }
+
 void make_layout(const nq_shape* s, const nq_params* p, nq_layout* L) {
     const int dp = padded_dim(s->head_dim);
-    const uint64_t rows = uint64_t(s->layers) * s->batch * s->kv_heads * s->tokens;
+    const uint64_t slices = uint64_t(s->layers) * s->batch * s->kv_heads;
+    const uint64_t rows = slices * uint64_t(pad_tokens(s->tokens));
     std::memset(L, 0, sizeof(*L));
     L->version = NQ_FORMAT_VERSION;
     L->padded_dim = uint32_t(dp);
+    L->tokens_padded = uint32_t(pad_tokens(s->tokens));
     L->rows = rows;
     L->k_idx_row_bytes = uint64_t(dp) * p->key_bits / 8;
     L->v_idx_row_bytes = uint64_t(dp) * p->value_bits / 8;
@@ -58,14 +66,56 @@ void make_layout(const nq_shape* s, const nq_params* p, nq_layout* L) {
 
 }  // namespace
 
-int grid_capacity(const void* kernel) {
+int grid_capacity(const void* kernel, int smem) {
     int dev = 0, sms = 0, per_sm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, size_t(smem)) != cudaSuccess)
         return -1;
     if (per_sm <= 0) return -1;  // the kernel cannot be resident at all
     return sms * per_sm;
+}
+
+bool ensure_smem(const void* kernel, int smem) {
+    // (kernel, device) pairs already configured; the attribute is per device
+    static std::mutex mu;
+    static const void* done_kernel[256];
+    static int done_dev[256];
+    static int n_done = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n_done; ++i)
+        if (done_kernel[i] == kernel && done_dev[i] == dev) return true;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return false;
+    if (n_done < 256) {
+        done_kernel[n_done] = kernel;
+        done_dev[n_done] = dev;
+        ++n_done;
+    }
+    return true;
+}
+
+bool make_row_tile_map(CUtensorMap* map, void* base, int head_dim, int tokens, int64_t slices) {
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!encode) return false;
+    const cuuint64_t dims[3] = {cuuint64_t(head_dim), cuuint64_t(tokens), cuuint64_t(slices)};
+    const cuuint64_t strides[2] = {cuuint64_t(head_dim) * 2, cuuint64_t(head_dim) * 2 * cuuint64_t(tokens)};
+    const cuuint32_t box[3] = {64, 32, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // ------------------------------------------------------------ e8 test entry
@@ -178,6 +228,7 @@ int nq_compress_kv(const void* k_f16, const void* v_f16, const float* rope_table
     nq::LaunchArgs a;
     a.slices = int64_t(shape->layers) * shape->batch * shape->kv_heads;
     a.tokens = shape->tokens;
+    a.tpad = int(L.tokens_padded);
     a.group = params->group_size;
     a.delta_chunk = params->delta_chunk;
     a.stream = static_cast<cudaStream_t>(stream);
@@ -210,6 +261,7 @@ int nq_decompress_kv(const void* in, size_t in_bytes, const float* rope_table,
     nq::LaunchArgs a;
     a.slices = int64_t(shape->layers) * shape->batch * shape->kv_heads;
     a.tokens = shape->tokens;
+    a.tpad = int(L.tokens_padded);
     a.group = params->group_size;
     a.delta_chunk = params->delta_chunk;
     a.stream = static_cast<cudaStream_t>(stream);

@@ -2,167 +2,228 @@
 // -> undo temporal delta -> unpack -> unscale -> inverse Hadamard -> RoPE
 // re-apply (keys) -> fp16 rows.
 //
-// Same work layout as compression: one thread per row, a warp per 32
-// consecutive tokens of a slice, a chunk of delta_chunk tokens per work item.
-// The delta is undone by an inclusive warp scan (field-wise addition modulo
-// 2^b, exclusive-or for the coset word) plus the running total of the chunk's
-// earlier tiles.
+// Same work layout as compression: a warp per 32-token tile of a slice, lane r
+// owns row r.  A tile's records (idx rows, coset words, scales) are contiguous
+// and 16-byte aligned thanks to the per-slice padding of the record rows, so
+// they stream through a 3-stage shared-memory ring by cp.async.  The delta is
+// undone by an inclusive warp scan (field-wise addition modulo 2^b,
+// exclusive-or for the coset word) plus the running total of the chunk's
+// earlier tiles.  The reconstructed fp16 rows are written into a swizzled
+// shared-memory tile and leave by one TMA tensor store per 64 columns, which
+// clips the rows past the end of the slice and the columns past head_dim.
 #include "nq_internal.h"
 
 namespace nq {
+
+constexpr int kStages = 3;
+constexpr int kRecIdx = 0;        // idx rows: 32 * RB <= 2048 bytes
+constexpr int kRecCoset = 2048;   // 32 coset words: 64 bytes
+constexpr int kRecScale = 2112;   // 32 * (Dp / group) fp16 <= 256 bytes
+constexpr int kRecStage = 2560;   // stage pitch
+constexpr int kOutBufs = 2;
+constexpr int kWarpSmem = kOutBufs * kTileBytes + kStages * kRecStage;  // 24064
+constexpr int kDecompressSmem = kWarpsPerBlock * kWarpSmem;
+
+template <int RB>
+__device__ __forceinline__ void load_records(const uint8_t* __restrict__ idx, const uint16_t* __restrict__ coset,
+                                             const __half* __restrict__ scales, int nsc, int64_t row0,
+                                             uint32_t stage, int lane) {
+    // idx: 32 * RB bytes = 2 * RB chunks
+    const uint8_t* ib = idx + row0 * RB;
+#pragma unroll
+    for (int g = lane; g < 2 * RB; g += 32) cp_async16(stage + kRecIdx + 16 * g, ib + 16 * g, 16);
+    if (lane < 4) cp_async16(stage + kRecCoset + 16 * lane, coset + row0 + 8 * lane, 16);
+    const int nsch = 4 * nsc;  // 32 * nsc * 2 / 16
+    if (lane < nsch) cp_async16(stage + kRecScale + 16 * lane, scales + row0 * nsc + 8 * lane, 16);
+}
+
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(map),
+                 "r"(src), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
 
 template <int D, int BITS>
 __global__ void __launch_bounds__(kThreads, 1)
     decompress_kernel(const uint8_t* __restrict__ idx, const uint16_t* __restrict__ coset,
                       const __half* __restrict__ scales, const float4* __restrict__ rope,
-                      int64_t slices, int tokens, int group, int chunk, bool delta,
-                      __half* __restrict__ x) {
+                      const __grid_constant__ CUtensorMap out_map, int64_t slices, int tokens, int tpad,
+                      int group, int chunk, bool delta) {
     constexpr int DP = PaddedDim<D>::value;
     constexpr int NB = DP / 8;
     using C = Code<BITS>;
     using RP = RowPack<BITS, NB>;
     constexpr int RB = DP * BITS / 8;
 
+    extern __shared__ __align__(1024) uint8_t smem[];
     const int lane = threadIdx.x & 31;
+    const uint32_t wbase = smem_u32(smem) + (threadIdx.x >> 5) * kWarpSmem;
+    const uint32_t outbuf = wbase;                           // kOutBufs x 8 KB, 1024-aligned
+    const uint32_t ring = wbase + kOutBufs * kTileBytes;     // kStages x kRecStage
     const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
-    const int nchunks = (tokens + chunk - 1) / chunk;
-    const int64_t items = slices * nchunks;
     const int nsc = DP / group;
     const int gshift = group == 32 ? 5 : (group == 64 ? 6 : 7);
 
-    for (int64_t item = warp; item < items; item += nwarps) {
-        const int64_t slice = item / nchunks;
-        const int t_begin = int(item - slice * nchunks) * chunk;
-        const int t_end = min(t_begin + chunk, tokens);
-        unsigned carry[NB];
-        unsigned carry_c = 0;
+    TileWalk cur(warp, nwarps, slices, tokens, chunk);
+    TileWalk pre = cur;
 #pragma unroll
-        for (int k = 0; k < NB; ++k) carry[k] = 0;
+    for (int s = 0; s < kStages - 1; ++s) {
+        if (pre.valid()) {
+            load_records<RB>(idx, coset, scales, nsc, pre.slice * tpad + pre.t0, ring + s * kRecStage, lane);
+            pre.next();
+        }
+        cp_async_commit();
+    }
 
-        for (int t0 = t_begin; t0 < t_end; t0 += 32) {
-            const int t = t0 + lane;
-            const bool active = t < t_end;
-            const int64_t row = slice * tokens + (active ? t : t_begin);
+    unsigned carry[NB];
+    unsigned carry_c = 0;
+#pragma unroll
+    for (int k = 0; k < NB; ++k) carry[k] = 0;
 
-            // ---- load the record
-            unsigned w[RP::WORDS];
-            const uint8_t* src = idx + row * RB;
-            if constexpr (RB % 16 == 0) {
+    for (int i = 0; cur.valid(); ++i) {
+        if (pre.valid()) {
+            load_records<RB>(idx, coset, scales, nsc, pre.slice * tpad + pre.t0,
+                             ring + ((i + kStages - 1) % kStages) * kRecStage, lane);
+            pre.next();
+        }
+        cp_async_commit();
+        cp_async_wait<kStages - 1>();
+        __syncwarp();
+        const uint32_t stage = ring + (i % kStages) * kRecStage;
+        const int t = cur.t0 + lane;
+
+        // ---- the lane's record
+        unsigned w[RP::WORDS];
+        if constexpr (RB % 16 == 0) {
 #pragma unroll
-                for (int q = 0; q < RB / 16; ++q) {
-                    uint4 v = ld_stream(reinterpret_cast<const uint4*>(src) + q);
-                    w[4 * q] = v.x;
-                    w[4 * q + 1] = v.y;
-                    w[4 * q + 2] = v.z;
-                    w[4 * q + 3] = v.w;
-                }
-            } else {
-#pragma unroll
-                for (int q = 0; q < RB / 8; ++q) {
-                    uint2 v = __ldg(reinterpret_cast<const uint2*>(src) + q);
-                    w[2 * q] = v.x;
-                    w[2 * q + 1] = v.y;
-                }
+            for (int q = 0; q < RB / 16; ++q) {
+                const uint4 v = lds128(stage + kRecIdx + lane * RB + 16 * q);
+                w[4 * q] = v.x;
+                w[4 * q + 1] = v.y;
+                w[4 * q + 2] = v.z;
+                w[4 * q + 3] = v.w;
             }
-            unsigned blk[NB];
-            RP::unpack(w, blk);
-            unsigned cw = __ldg(coset + row);
-
-            // ---- undo the temporal delta: inclusive scan over the tile + carry
-            if (delta) {
+        } else {
 #pragma unroll
-                for (int off = 1; off < 32; off *= 2) {
-#pragma unroll
-                    for (int k = 0; k < NB; ++k) {
-                        const unsigned v = __shfl_up_sync(kFull, blk[k], off);
-                        if (lane >= off) blk[k] = swar_add<BITS>(blk[k], v);
-                    }
-                    const unsigned vc = __shfl_up_sync(kFull, cw, off);
-                    if (lane >= off) cw ^= vc;
-                }
-#pragma unroll
-                for (int k = 0; k < NB; ++k) {
-                    blk[k] = swar_add<BITS>(blk[k], carry[k]);
-                    carry[k] = __shfl_sync(kFull, blk[k], 31);
-                }
-                cw ^= carry_c;
-                carry_c = __shfl_sync(kFull, cw, 31);
-            }
-
-            // ---- unpack, unscale: y = (code - offset) * scale  (exact)
-            float scf[DP / 32];
-#pragma unroll
-            for (int s = 0; s < DP / 32; ++s)
-                scf[s] = __half2float(__ldg(scales + row * nsc + ((32 * s) >> gshift)));
-            float y[DP];
-#pragma unroll
-            for (int k = 0; k < NB; ++k) {
-                const float off = ((cw >> k) & 1u) ? C::H : C::HI0;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const unsigned m = (blk[k] >> (j * BITS)) & C::MASK;
-                    const float mf = __fsub_rn(__uint_as_float(0x4B000000u | m), 8388608.0f);
-                    y[8 * k + j] = __fmul_rn(__fsub_rn(mf, off), scf[k / 4]);
-                }
-            }
-
-            // ---- inverse Hadamard: x = H (r * sc)
-            fwht<DP>(y);
-
-            // ---- RoPE re-apply on keys: rotate each (i, i + D/2) pair by +angle
-            if (rope != nullptr) {
-                const float4* cs = rope + int64_t(active ? t : t_begin) * (D / 4);
-#pragma unroll
-                for (int q = 0; q < D / 4; ++q) {
-                    float4 v = __ldg(cs + q);
-#pragma unroll
-                    for (int p = 0; p < 2; ++p) {
-                        const int i = 2 * q + p;
-                        const float c = p ? v.z : v.x, s = p ? v.w : v.y;
-                        const float a = y[i], b = y[i + D / 2];
-                        y[i] = __fmaf_rn(a, c, -__fmul_rn(b, s));
-                        y[i + D / 2] = __fmaf_rn(b, c, __fmul_rn(a, s));
-                    }
-                }
-            }
-
-            // ---- fp16 store
-            if (active) {
-                uint4* dst = reinterpret_cast<uint4*>(x + row * D);
-#pragma unroll
-                for (int q = 0; q < D / 8; ++q) st_stream(dst + q, f_to_h8(&y[8 * q]));
+            for (int q = 0; q < RB / 8; ++q) {
+                const uint2 v = lds64(stage + kRecIdx + lane * RB + 8 * q);
+                w[2 * q] = v.x;
+                w[2 * q + 1] = v.y;
             }
         }
+        const uint16_t* stage_gen = reinterpret_cast<const uint16_t*>(smem + (stage - smem_u32(smem)));
+        unsigned cw = stage_gen[kRecCoset / 2 + lane];
+        float scf[DP / 32];
+#pragma unroll
+        for (int s = 0; s < DP / 32; ++s)
+            scf[s] = __half2float(__ushort_as_half(stage_gen[kRecScale / 2 + lane * nsc + ((32 * s) >> gshift)]));
+        __syncwarp();  // the stage may be refilled
+        unsigned blk[NB];
+        RP::unpack(w, blk);
+
+        // ---- undo the temporal delta: inclusive scan over the tile + carry
+        if (delta) {
+#pragma unroll
+            for (int off = 1; off < 32; off *= 2) {
+#pragma unroll
+                for (int k = 0; k < NB; ++k) {
+                    const unsigned v = __shfl_up_sync(kFull, blk[k], off);
+                    if (lane >= off) blk[k] = swar_add<BITS>(blk[k], v);
+                }
+                const unsigned vc = __shfl_up_sync(kFull, cw, off);
+                if (lane >= off) cw ^= vc;
+            }
+            const bool first = cur.t0 == cur.t_begin;
+#pragma unroll
+            for (int k = 0; k < NB; ++k) {
+                if (!first) blk[k] = swar_add<BITS>(blk[k], carry[k]);
+                carry[k] = __shfl_sync(kFull, blk[k], 31);
+            }
+            if (!first) cw ^= carry_c;
+            carry_c = __shfl_sync(kFull, cw, 31);
+        }
+
+        // ---- unpack, unscale: y = (code - offset) * scale  (exact)
+        float y[DP];
+#pragma unroll
+        for (int k = 0; k < NB; ++k) {
+            const float off = ((cw >> k) & 1u) ? C::H : C::HI0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const unsigned m = (blk[k] >> (j * BITS)) & C::MASK;
+                const float mf = __fsub_rn(__uint_as_float(0x4B000000u | m), 8388608.0f);
+                y[8 * k + j] = __fmul_rn(__fsub_rn(mf, off), scf[k / 4]);
+            }
+        }
+
+        // ---- inverse Hadamard: x = H (r * sc)
+        fwht<DP>(y);
+
+        // ---- RoPE re-apply on keys: rotate each (i, i + D/2) pair by +angle
+        if (rope != nullptr) {
+            const float4* cs = rope + int64_t(t < cur.t_end ? t : cur.t_begin) * (D / 4);
+#pragma unroll
+            for (int q = 0; q < D / 4; ++q) {
+                const float4 v = __ldg(cs + q);
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    const int j = 2 * q + p;
+                    const float c = p ? v.z : v.x, s = p ? v.w : v.y;
+                    const float a = y[j], b = y[j + D / 2];
+                    y[j] = __fmaf_rn(a, c, -__fmul_rn(b, s));
+                    y[j + D / 2] = __fmaf_rn(b, c, __fmul_rn(a, s));
+                }
+            }
+        }
+
+        // ---- fp16 rows -> swizzled smem tile -> TMA tensor store
+        const uint32_t ob = outbuf + (i & 1) * kTileBytes;
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");  // ob is free
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < D / 8; ++q) sts128(ob + swz(lane, q), f_to_h8(&y[8 * q]));
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+            const int z = int(cur.slice);
+            tma_store_3d(&out_map, ob, 0, cur.t0, z);
+            if (D > 64) tma_store_3d(&out_map, ob + 4096, 64, cur.t0, z);
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+        cur.next();
     }
+    cp_async_wait<0>();
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 template <int D, int BITS>
-static int launch(const LaunchArgs& a, const uint8_t* idx, const uint16_t* coset,
-                  const __half* scales, const float4* rope, __half* x) {
+static int launch(const LaunchArgs& a, const uint8_t* idx, const uint16_t* coset, const __half* scales,
+                  const float4* rope, const CUtensorMap& map) {
     auto kern = decompress_kernel<D, BITS>;
-    const int chunk = a.delta_chunk > 0 ? a.delta_chunk : 32;
+    if (!ensure_smem(reinterpret_cast<const void*>(kern), kDecompressSmem)) return NQ_ERR_CUDA;
+    const int chunk = a.delta_chunk > 0 ? a.delta_chunk : kTileRows;
     const int64_t items = a.slices * ((a.tokens + chunk - 1) / chunk);
     const int64_t want = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
     if (want == 0) return NQ_OK;
-    const int cap = grid_capacity(reinterpret_cast<const void*>(kern));
+    const int cap = grid_capacity(reinterpret_cast<const void*>(kern), kDecompressSmem);
     if (cap <= 0) return NQ_ERR_CUDA;
     const int grid = int(std::min<int64_t>(want, cap));
-    kern<<<grid, kThreads, 0, a.stream>>>(idx, coset, scales, rope, a.slices, a.tokens, a.group,
-                                          chunk, a.delta_chunk > 0, x);
+    kern<<<grid, kThreads, kDecompressSmem, a.stream>>>(idx, coset, scales, rope, map, a.slices, a.tokens,
+                                                        a.tpad, a.group, chunk, a.delta_chunk > 0);
     return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
 }
 
 template <int D>
 static int dispatch_bits(const LaunchArgs& a, int bits, const uint8_t* idx, const uint16_t* coset,
-                         const __half* scales, const float4* rope, __half* x) {
+                         const __half* scales, const float4* rope, const CUtensorMap& map) {
     switch (bits) {
         case 2:
-            return launch<D, 2>(a, idx, coset, scales, rope, x);
+            return launch<D, 2>(a, idx, coset, scales, rope, map);
         case 3:
-            return launch<D, 3>(a, idx, coset, scales, rope, x);
+            return launch<D, 3>(a, idx, coset, scales, rope, map);
         case 4:
-            return launch<D, 4>(a, idx, coset, scales, rope, x);
+            return launch<D, 4>(a, idx, coset, scales, rope, map);
         default:
             return NQ_ERR_UNSUPPORTED;
     }
@@ -171,16 +232,17 @@ static int dispatch_bits(const LaunchArgs& a, int bits, const uint8_t* idx, cons
 int launch_decompress_tensor(const LaunchArgs& a, int head_dim, int bits, const uint8_t* idx,
                              const uint16_t* coset, const uint16_t* scales, const float* rope,
                              void* x_out) {
+    CUtensorMap map;
+    if (!make_row_tile_map(&map, x_out, head_dim, a.tokens, a.slices)) return NQ_ERR_CUDA;
     const __half* sh = reinterpret_cast<const __half*>(scales);
     const float4* r = reinterpret_cast<const float4*>(rope);
-    __half* xh = static_cast<__half*>(x_out);
     switch (head_dim) {
         case 64:
-            return dispatch_bits<64>(a, bits, idx, coset, sh, r, xh);
+            return dispatch_bits<64>(a, bits, idx, coset, sh, r, map);
         case 96:
-            return dispatch_bits<96>(a, bits, idx, coset, sh, r, xh);
+            return dispatch_bits<96>(a, bits, idx, coset, sh, r, map);
         case 128:
-            return dispatch_bits<128>(a, bits, idx, coset, sh, r, xh);
+            return dispatch_bits<128>(a, bits, idx, coset, sh, r, map);
         default:
             return NQ_ERR_UNSUPPORTED;
     }

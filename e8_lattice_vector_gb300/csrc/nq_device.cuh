@@ -260,6 +260,79 @@ __device__ __forceinline__ void st_stream(uint4* p, const uint4& v) {
                  : "memory");
 }
 
+// ------------------------------------------------------- tile staging (smem)
+
+// A tile is 32 consecutive tokens of one slice; one warp owns it, lane r owns
+// row r.  fp16 rows are staged in shared memory as two 4 KB boxes of
+// 32 rows x 128 bytes (head_dim columns 0-63 and 64-127); inside a box the
+// 16-byte chunk c of row r sits at chunk position c ^ (r & 7).  That is the
+// TMA 128-byte swizzle, so a row read or write by one lane per row is free of
+// bank conflicts, and a tensor store can move the tile out unchanged.
+constexpr int kTileRows = 32;
+constexpr int kTileBytes = 8192;
+
+__device__ __forceinline__ uint32_t swz(int r, int q) {
+    return uint32_t(((q >> 3) << 12) + (r << 7) + (((q & 7) ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte global -> shared async copy; src_bytes < 16 zero-fills the rest.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ void sts128(uint32_t a, const uint4& v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// Work items: (slice, chunk of `chunk` tokens); a warp walks its items'
+// 32-token tiles in order.  Two copies of the walk run one pipeline depth
+// apart (the one that prefetches and the one that computes).
+struct TileWalk {
+    int64_t item, items, step, slice;
+    int nchunks, chunk, tokens, t_begin, t_end, t0;
+    __device__ TileWalk(int64_t first, int64_t step_, int64_t slices, int tokens_, int chunk_)
+        : items(0), step(step_), slice(0), chunk(chunk_), tokens(tokens_), t_begin(0), t_end(0), t0(0) {
+        nchunks = (tokens_ + chunk_ - 1) / chunk_;
+        items = slices * nchunks;
+        set(first);
+    }
+    __device__ __forceinline__ void set(int64_t it) {
+        item = it;
+        if (it < items) {
+            slice = it / nchunks;
+            t_begin = int(it - slice * nchunks) * chunk;
+            t_end = min(t_begin + chunk, tokens);
+            t0 = t_begin;
+        }
+    }
+    __device__ __forceinline__ bool valid() const { return item < items; }
+    __device__ __forceinline__ void next() {
+        t0 += kTileRows;
+        if (t0 >= t_end) set(item + step);
+    }
+};
+
 // ----------------------------------------------------------- row records
 
 // Block codes <-> the row's idx bytes (coordinate i's field at bit i*b).

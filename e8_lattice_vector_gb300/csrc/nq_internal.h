@@ -1,6 +1,7 @@
 // nq_internal.h -- declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (type only; the encoder is fetched at run time)
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -22,14 +23,23 @@ struct PaddedDim {
 struct LaunchArgs {
     int64_t slices;  // layers * batch * kv_heads
     int tokens;
+    int tpad;        // record rows per slice: tokens rounded up to a multiple of 32
     int group;
     int delta_chunk;
     cudaStream_t stream;
 };
 
-// Blocks of kThreads that fit on the current device at once for `kernel`;
-// -1 when the device or the kernel cannot be queried.
-int grid_capacity(const void* kernel);
+// Blocks of kThreads that fit on the current device at once for `kernel` with
+// `smem` bytes of dynamic shared memory; -1 when it cannot be queried.
+int grid_capacity(const void* kernel, int smem);
+
+// Allow `kernel` `smem` bytes of dynamic shared memory on the current device
+// (once per device); false on a CUDA error.
+bool ensure_smem(const void* kernel, int smem);
+
+// TMA map of an fp16 [slices][tokens][head_dim] tensor as 3-D tiles of
+// 64 columns x 32 tokens x 1 slice, 128-byte swizzle.  false on failure.
+bool make_row_tile_map(CUtensorMap* map, void* base, int head_dim, int tokens, int64_t slices);
 
 int launch_compress_tensor(const LaunchArgs& a, int head_dim, int bits, bool strict, const void* x,
                            const float* rope, uint8_t* idx, uint16_t* coset, uint16_t* scales);

@@ -23,12 +23,15 @@
  *
  * Tensor layout: K and V are contiguous fp16 [layers, batch, kv_heads,
  * tokens, head_dim] (for batch 1 this is [layers, kv_heads, tokens,
- * head_dim]).  A "row" is one head_dim vector; rows are numbered in that
- * order, so row = ((l * batch + b) * kv_heads + h) * tokens + t.
+ * head_dim]).  A "row" is one head_dim vector.  A slice is one (layer,
+ * batch, head); slice s = (l * batch + b) * kv_heads + h.  In the compressed
+ * buffer every slice holds tokens_padded = 32 * ceil(tokens / 32) record
+ * rows: record row s * tokens_padded + t describes token t, and the rows for
+ * t >= tokens are zero.
  *
  * Compressed buffer (format version NQ_FORMAT_VERSION), sections in the
  * order below, each starting at a 256-byte aligned offset given by nq_plan:
- *   K idx   [rows][Dp * key_bits / 8]   bytes
+ *   K idx   [rows][Dp * key_bits / 8]   bytes   (rows = slices * tokens_padded)
  *   K coset [rows]                       uint16, bit k = coset of block k
  *   K scale [rows][Dp / group_size]      fp16
  *   V idx / V coset / V scale            the same with value_bits.
@@ -90,7 +93,9 @@ typedef struct {
 typedef struct {
     uint32_t version;
     uint32_t padded_dim;
-    uint64_t rows; /* rows per tensor */
+    uint32_t tokens_padded; /* record rows per slice: tokens rounded up to 32 */
+    uint32_t reserved;
+    uint64_t rows;          /* record rows per tensor: slices * tokens_padded */
     uint64_t k_idx_row_bytes, v_idx_row_bytes, scales_per_row;
     uint64_t k_idx, k_coset, k_scale, v_idx, v_coset, v_scale;
     uint64_t total_bytes;

@@ -39,12 +39,24 @@ def _oracle_compress(orc, K, V, params):
 
 
 def _gpu_sections(nq, buf, shape, params):
+    """Sections as logical rows [slices * tokens, ...]; checks the padding
+    rows of every slice are zero."""
     lay = nq.plan(shape, params)
-    s = nq.sections(buf, lay)
+    T = shape[3]
+    full = nq.sections(buf, lay)
+    tp = int(lay.tokens_padded)
     out = {}
     for t in ("k", "v"):
-        out[t] = (s[t + "_idx"].cpu().numpy(), s[t + "_coset"].cpu().numpy().view(np.uint16),
-                  s[t + "_scale"].contiguous().view(torch.int16).cpu().numpy().view(np.uint16))
+        arrs = []
+        for key in ("_idx", "_coset", "_scale"):
+            a = full[t + key]
+            a = a.contiguous().view(torch.int16) if a.dtype == torch.float16 else a
+            a = a.cpu().numpy()
+            a = a.reshape(a.shape[0] // tp, tp, *a.shape[1:]) if tp else a.reshape(0, 0, *a.shape[1:])
+            assert not np.any(a[:, T:]), t + key + " padding rows are not zero"
+            a = a[:, :T].reshape(-1, *a.shape[2:])
+            arrs.append(a.view(np.uint16) if a.dtype == np.int16 else a)
+        out[t] = tuple(arrs)
     return out
 
 
@@ -234,7 +246,15 @@ def test_full_size_sampled_parity(nq, orc, name):
         if cs is None:
             cs = rope.host.numpy()
         buf = nq.compress_kv(K, V, params, rope)
-        got = _gpu_sections(nq, buf, cfg.shape, params)
+        lay = nq.plan(cfg.shape, params)
+        tp = int(lay.tokens_padded)
+        full = nq.sections(buf, lay)
+        rec = torch.from_numpy((rows // T) * tp + rows % T).cuda()  # record rows of the sampled tokens
+        got = {}
+        for t in ("k", "v"):
+            got[t] = (full[t + "_idx"][rec].cpu().numpy(),
+                      full[t + "_coset"][rec].cpu().numpy().view(np.uint16),
+                      full[t + "_scale"][rec].contiguous().view(torch.int16).cpu().numpy().view(np.uint16))
         Kf = K.view(-1, D)
         Vf = V.view(-1, D)
         rows_t = torch.from_numpy(rows).cuda()
@@ -251,9 +271,9 @@ def test_full_size_sampled_parity(nq, orc, name):
                     pidx, pcw, _ = orc.encode_row(xp[n], D, bits, params.group_size, int(params.strict),
                                                   cs[t - 1] if rope_on else None)
                     idx, cw = orc.delta_row(idx, cw, pidx, pcw, orc.padded_dim(D), bits)
-                assert np.array_equal(gs[r], sc), (name_t, r)
-                assert gc[r] == cw, (name_t, r)
-                assert np.array_equal(gi[r], idx), (name_t, r)
+                assert np.array_equal(gs[n], sc), (name_t, r)
+                assert gc[n] == cw, (name_t, r)
+                assert np.array_equal(gi[n], idx), (name_t, r)
         # decompression of the same rows against the oracle's decoding of the
         # (already verified) GPU records, restored from the raw codes
         K2, V2 = nq.decompress_kv(buf, cfg.shape, params, rope)

@@ -56,11 +56,13 @@ def _plan(nq, shape, **kw):
 def test_plan_sizes_match_oracle_format(nq, orc, shape, kb, vb, g):
     st, lay = _plan(nq, shape, key_bits=kb, value_bits=vb, group_size=g)
     assert st == 0
-    rows = int(np.prod(shape[:4]))
+    slices = int(np.prod(shape[:3]))
+    tp = (shape[3] + 31) // 32 * 32
+    rows = slices * tp
     D = shape[4]
     dp = orc.padded_dim(D)
-    assert lay.version == 1 and lay.padded_dim == dp and lay.rows == rows
-    x = np.zeros((rows // shape[3], shape[3], D), np.uint16)
+    assert lay.version == 1 and lay.padded_dim == dp and lay.tokens_padded == tp and lay.rows == rows
+    x = np.zeros((slices, shape[3], D), np.uint16)
     for off, bits in (("k", kb), ("v", vb)):
         idx, cos_, sc = orc.compress_tensor(x, shape[3], D, bits, g, 0, 0)
         assert getattr(lay, off + "_idx_row_bytes") == idx.shape[1]
