@@ -78,7 +78,9 @@ class RopeTable:
 
     @staticmethod
     def host_table(tokens, head_dim, theta, positions=None):
-        host = torch.empty((tokens, head_dim // 2, 2), dtype=torch.float32)
+        """[head_dim/4, tokens, 4] float32: plane q holds (cos, sin) of pairs 2q
+        and 2q+1 for every token."""
+        host = torch.empty((head_dim // 4, tokens, 4), dtype=torch.float32)
         pos = None
         if positions is not None:
             pos = torch.as_tensor(positions, dtype=torch.int32).contiguous()
@@ -93,6 +95,11 @@ class RopeTable:
     def build(cls, tokens, head_dim, theta, positions=None, device="cuda"):
         host = cls.host_table(tokens, head_dim, theta, positions)
         return cls(host, host.to(device), tokens, head_dim, theta)
+
+    def pairs(self):
+        """The table as [tokens, head_dim/2, (cos, sin)] (numpy), token-major."""
+        h = self.host.numpy()
+        return h.transpose(1, 0, 2).reshape(self.tokens, self.head_dim // 2, 2)
 
 
 def _rope_ptr(rope, params, tokens, head_dim):

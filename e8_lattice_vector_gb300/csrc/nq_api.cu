@@ -133,10 +133,9 @@ __global__ void e8_nearest_kernel(const float* __restrict__ u, float* __restrict
         }
         if constexpr (BITS > 0) {
             using C = Code<BITS>;
-            if (umax < C::H) {
+            unsigned c, code;
+            if (umax < C::H && e8_fast<BITS, STRICT>(v, code, c)) {
                 // the path compression takes for in-box blocks
-                unsigned c;
-                const unsigned code = e8_fast<BITS, STRICT>(v, c);
                 const float off = c ? C::H : C::HI0;
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
@@ -198,14 +197,16 @@ int nq_rope_table(const int32_t* positions, int32_t tokens, int32_t head_dim, fl
         !std::isfinite(rope_theta))
         return NQ_ERR_ARG;
     if (tokens > 0 && !table) return NQ_ERR_ARG;
+    if (head_dim % 4) return NQ_ERR_ARG;
     const int half = head_dim / 2;
     for (int32_t t = 0; t < tokens; ++t) {
         const double p = positions ? double(positions[t]) : double(t);
-        float* row = table + size_t(t) * size_t(head_dim);
         for (int i = 0; i < half; ++i) {
             const double angle = p * std::pow(double(rope_theta), -2.0 * double(i) / double(head_dim));
-            row[2 * i] = float(std::cos(angle));
-            row[2 * i + 1] = float(std::sin(angle));
+            // quad q = i / 2 holds the pairs 2q and 2q + 1 of token t
+            float* quad = table + (size_t(i / 2) * size_t(tokens) + size_t(t)) * 4;
+            quad[2 * (i & 1)] = float(std::cos(angle));
+            quad[2 * (i & 1) + 1] = float(std::sin(angle));
         }
     }
     return NQ_OK;

@@ -94,10 +94,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // ---- RoPE removal on keys: rotate each (i, i + D/2) pair by -angle
         if (rope != nullptr) {
-            const float4* cs = rope + int64_t(active ? t : cur.t_begin) * (D / 4);
+            // table layout [D/4][tokens] float4: lanes read consecutive tokens
+            const float4* cs = rope + (active ? t : cur.t_begin);
 #pragma unroll
             for (int q = 0; q < D / 4; ++q) {
-                const float4 v = __ldg(cs + q);
+                const float4 v = __ldg(cs + int64_t(q) * tokens);
 #pragma unroll
                 for (int p = 0; p < 2; ++p) {
                     const int j = 2 * q + p;
@@ -118,7 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < NSUB; ++s) {
             float m = 0.0f;
 #pragma unroll
-            for (int j = 32 * s; j < 32 * s + 32; ++j) m = fmaxf(m, fabsf(y[j]));
+            for (int j = 32 * s; j < 32 * s + 32; j += 2) m = fmax3(m, fabsf(y[j]), fabsf(y[j + 1]));
             amax[s] = m;
         }
         if (group >= 64) {
@@ -150,12 +151,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 8; ++j) u[j] = __fmul_rn(y[8 * k + j], inv[k / 4]);
             unsigned c;
-            if (fast) {
-                blk[k] = e8_fast<BITS, STRICT>(u, c);
-            } else {
-                float r[8];
-                c = (unsigned)e8_general(u, STRICT, C::HI0, C::H, r);
-                blk[k] = pack_point<BITS>(r, int(c));
+            if (!(fast && e8_fast<BITS, STRICT>(u, blk[k], c))) {
+                const uint2 res = e8_slow<BITS, STRICT>(make_float4(u[0], u[1], u[2], u[3]),
+                                                        make_float4(u[4], u[5], u[6], u[7]));
+                blk[k] = res.x;
+                c = res.y;
             }
             cw |= c << k;
         }

@@ -21,8 +21,10 @@ constexpr int kRecCoset = 2048;   // 32 coset words: 64 bytes
 constexpr int kRecScale = 2112;   // 32 * (Dp / group) fp16 <= 256 bytes
 constexpr int kRecStage = 2560;   // stage pitch
 constexpr int kOutBufs = 2;
-constexpr int kWarpSmem = kOutBufs * kTileBytes + kStages * kRecStage;  // 24064
-constexpr int kDecompressSmem = kWarpsPerBlock * kWarpSmem;
+// per-warp region, a multiple of 1024 bytes: the output tiles must sit on
+// 1024-byte boundaries for the 128-byte swizzle pattern of the tensor store
+constexpr int kWarpSmem = (kOutBufs * kTileBytes + kStages * kRecStage + 1023) / 1024 * 1024;
+constexpr int kDecompressSmem = kWarpsPerBlock * kWarpSmem + 1024;  // + alignment slack
 
 template <int RB>
 __device__ __forceinline__ void load_records(const uint8_t* __restrict__ idx, const uint16_t* __restrict__ coset,
@@ -57,7 +59,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     extern __shared__ __align__(1024) uint8_t smem[];
     const int lane = threadIdx.x & 31;
-    const uint32_t wbase = smem_u32(smem) + (threadIdx.x >> 5) * kWarpSmem;
+    const uint32_t wbase = ((smem_u32(smem) + 1023u) & ~1023u) + (threadIdx.x >> 5) * kWarpSmem;
     const uint32_t outbuf = wbase;                           // kOutBufs x 8 KB, 1024-aligned
     const uint32_t ring = wbase + kOutBufs * kTileBytes;     // kStages x kRecStage
     const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -162,10 +164,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // ---- RoPE re-apply on keys: rotate each (i, i + D/2) pair by +angle
         if (rope != nullptr) {
-            const float4* cs = rope + int64_t(t < cur.t_end ? t : cur.t_begin) * (D / 4);
+            const float4* cs = rope + (t < cur.t_end ? t : cur.t_begin);  // [D/4][tokens]
 #pragma unroll
             for (int q = 0; q < D / 4; ++q) {
-                const float4 v = __ldg(cs + q);
+                const float4 v = __ldg(cs + int64_t(q) * tokens);
 #pragma unroll
                 for (int p = 0; p < 2; ++p) {
                     const int j = 2 * q + p;

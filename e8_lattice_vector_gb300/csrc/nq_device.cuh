@@ -51,19 +51,57 @@ __device__ __forceinline__ unsigned swar_add(unsigned a, unsigned b) {
 
 // ------------------------------------------------------------------ Hadamard
 
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
+    unsigned long long pa, pb, r;
+    asm("mov.b64 %0, {%1,%2};" : "=l"(pa) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1,%2};" : "=l"(pb) : "f"(b.x), "f"(b.y));
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pa), "l"(pb));
+    float2 d;
+    asm("mov.b64 {%0,%1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(r));
+    return d;
+}
+
+// Unnormalised Walsh-Hadamard transform, textbook stage order h = 1, 2, ...,
+// N/2.  Stage 1 runs on single lanes; every later stage pairs butterflies
+// (i, i+h) and (i+1, i+1+h) into one packed f32x2 add and one subtract (each
+// half is an ordinary IEEE round-to-nearest operation, so the results are
+// those of the scalar butterflies).
 template <int N>
 __device__ __forceinline__ void fwht(float (&y)[N]) {
 #pragma unroll
-    for (int h = 1; h < N; h *= 2) {
+    for (int i = 0; i < N; i += 2) {
+        const float a = y[i], b = y[i + 1];
+        y[i] = __fadd_rn(a, b);
+        y[i + 1] = __fsub_rn(a, b);
+    }
 #pragma unroll
-        for (int i = 0; i < N; ++i) {
+    for (int h = 2; h < N; h *= 2) {
+#pragma unroll
+        for (int i = 0; i < N; i += 2) {
             if ((i & h) == 0) {
-                float a = y[i], b = y[i + h];
-                y[i] = __fadd_rn(a, b);
-                y[i + h] = __fsub_rn(a, b);
+                const float2 a = make_float2(y[i], y[i + 1]);
+                const float2 b = make_float2(y[i + h], y[i + h + 1]);
+                const float2 s = __fadd2_rn(a, b);
+                const float2 d = fsub2(a, b);
+                y[i] = s.x;
+                y[i + 1] = s.y;
+                y[i + h] = d.x;
+                y[i + h + 1] = d.y;
             }
         }
     }
+}
+
+// max of three (one instruction on sm_100 and later)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
 }
 
 // ------------------------------------------------------------------- scale
@@ -145,72 +183,107 @@ __device__ __forceinline__ int e8_general(const float (&u)[8], bool strict, floa
 // Fast path, valid when every |u_j| < (2^b - 1)/2 (then no rounding leaves the
 // box and the half-integer fix-up never needs to turn around).  Computes the
 // same codes as the general path:
-//   e~0 = rint(u) - u  (exact, never -0), the half-integer point is
-//   rint(u) + 1/2 if e~0 < 0 else rint(u) - 1/2  (= ceil(u) - 1/2), and its
-//   residual e~1 = e~0 -+ 1/2 (exact), the integer score is
-//   min(|e~0|, hi0 - |u|) (the turned-around step at the box edge).
-// Output: block code (8 fields of b bits, coordinate j at bit j*b) and coset.
+//   e~0 = rint(u) - u  (exact, never -0); the half-integer point is
+//   rint(u) + 1/2 if e~0 < 0 else rint(u) - 1/2 (= ceil(u) - 1/2), so its
+//   residual is e~1 = e~0 - copysign(1/2, e~0) (exact); the integer score is
+//   min(|e~0|, hi0 - |u|) (a step that would leave the box turns around).
+// The codes are accumulated as exact integer-valued floats on the FMA pipe
+// (sum of r_j * L^j over half-blocks of 4 coordinates, < 2^16), the parities
+// by xor of the magic-rounded bit patterns, and the fix-up coordinate (first
+// maximal score) by an equality mask.  A block whose chosen coset needs a
+// fix-up with a maximal score <= 0 (every coordinate an exact integer or past
+// the box edge) is not handled here: the function returns false and the
+// caller runs the general path.
 template <int BITS, bool STRICT>
-__device__ __forceinline__ unsigned e8_fast(const float (&u)[8], unsigned& coset) {
+__device__ __forceinline__ bool e8_fast(const float (&u)[8], unsigned& code, unsigned& coset) {
     using C = Code<BITS>;
-    float eb0[8], eb1[8], s0[8];
+    constexpr float L = float(C::L);
+    constexpr float Lp[4] = {1.0f, L, L * L, L * L * L};
+    constexpr float SUML = 1.0f + L + L * L + L * L * L;
+    constexpr float TWO23 = 8388608.0f;
+    float eb1[8], s0[8];
     float d0 = 0.0f, d1 = 0.0f;
-    float smax0 = -1.0f, smax1 = -1.0f;
-    unsigned code0 = 0, negmask = 0, xpar = 0;
+    float A[2] = {0.0f, 0.0f}, Bq[2] = {0.0f, 0.0f};
+    unsigned x0 = 0, xs = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        float t = __fadd_rn(u[j], kMagic);
-        float r0 = __fsub_rn(t, kMagic);
-        float e0 = __fsub_rn(r0, u[j]);
-        float e1 = __fsub_rn(e0, copysignf(0.5f, e0));
-        eb0[j] = e0;
+        const float t = __fadd_rn(u[j], kMagic);
+        const float r0 = __fsub_rn(t, kMagic);
+        const float e0 = __fsub_rn(r0, u[j]);
+        const float cs = copysignf(0.5f, e0);
+        const float e1 = __fsub_rn(e0, cs);
         eb1[j] = e1;
         d0 = __fmaf_rn(e0, e0, d0);
         d1 = __fmaf_rn(e1, e1, d1);
-        unsigned m = (__float_as_uint(t) + C::OFF0) & C::MASK;
-        code0 |= m << (j * BITS);
-        xpar ^= m;
-        negmask |= (__float_as_uint(e0) >> 31) << j;
+        A[j >> 2] = __fmaf_rn(r0, Lp[j & 3], A[j >> 2]);
+        Bq[j >> 2] = __fmaf_rn(cs, Lp[j & 3], Bq[j >> 2]);
         s0[j] = fminf(fabsf(e0), __fsub_rn(C::HI0, fabsf(u[j])));
-        smax0 = fmaxf(smax0, s0[j]);
-        smax1 = fmaxf(smax1, fabsf(e1));
+        x0 ^= __float_as_uint(t);
+        if (STRICT) xs ^= __float_as_uint(e0);
     }
-    // half-integer codes: m1 = m0 + [e~0 < 0]
-    unsigned inc = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) inc |= ((negmask >> j) & 1u) << (j * BITS);
-    const bool odd0 = (xpar & 1u) != 0;
-    const bool odd1 = STRICT && (((xpar ^ (unsigned)__popc(negmask)) & 1u) != 0);
-    float dd0 = odd0 ? __fadd_rn(d0, __fmaf_rn(-2.0f, smax0, 1.0f)) : d0;
-    float dd1 = odd1 ? __fadd_rn(d1, __fmaf_rn(-2.0f, smax1, 1.0f)) : d1;
+    const float smax0 = fmax3(fmax3(s0[0], s0[1], s0[2]), fmax3(s0[3], s0[4], s0[5]), fmaxf(s0[6], s0[7]));
+    float smax1 = 0.0f;
+    if (STRICT)
+        smax1 = fmax3(fmax3(fabsf(eb1[0]), fabsf(eb1[1]), fabsf(eb1[2])),
+                      fmax3(fabsf(eb1[3]), fabsf(eb1[4]), fabsf(eb1[5])), fmaxf(fabsf(eb1[6]), fabsf(eb1[7])));
+    const bool odd0 = (x0 & 1u) != 0;
+    const bool odd1 = STRICT && (((x0 ^ (xs >> 31)) & 1u) != 0);  // + number of e~0 < 0
+    const float dd0 = odd0 ? __fadd_rn(d0, __fmaf_rn(-2.0f, smax0, 1.0f)) : d0;
+    const float dd1 = odd1 ? __fadd_rn(d1, __fmaf_rn(-2.0f, smax1, 1.0f)) : d1;
     const bool half = dd1 < dd0;
-    unsigned code = half ? code0 + inc : code0;
+
+    // integer codes m0 = r0 + (L/2 - 1), half-integer codes m1 = r1 + (L - 1)/2
+    unsigned c0 = 0, c1 = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        // every intermediate is an integer below 2^24 (Bq and (L-1)/2 * SUML are
+        // both odd multiples of 1/2), so all of this is exact
+        const float ap = __fadd_rn(A[h], TWO23);
+        const float f0 = __fadd_rn(ap, float(C::OFF0) * SUML);
+        const float f1 = __fsub_rn(ap, __fsub_rn(Bq[h], C::H * SUML));
+        c0 |= (__float_as_uint(f0) & 0xffffu) << (4 * BITS * h);
+        c1 |= (__float_as_uint(f1) & 0xffffu) << (4 * BITS * h);
+    }
+    unsigned c = half ? c1 : c0;
     const bool fix = half ? odd1 : odd0;
     if (fix) {
         const float smax = half ? smax1 : smax0;
-        int k = 0;
-        float ek = 0.0f;
+        if (!(smax > 0.0f)) return false;
+        unsigned eq = 0;
 #pragma unroll
-        for (int j = 7; j >= 0; --j) {
-            float s = half ? fabsf(eb1[j]) : s0[j];
-            float e = half ? eb1[j] : eb0[j];
-            if (s == smax) {
-                k = j;
-                ek = e;
-            }
+        for (int j = 0; j < 8; ++j) {
+            const float sj = (STRICT && half) ? fabsf(eb1[j]) : s0[j];
+            eq |= (sj == smax ? 1u : 0u) << j;
         }
-        // step toward u (u - r >= 0 <=> e~ <= 0), turned around at the box edge
-        const int mk = (int)((code >> (k * BITS)) & C::MASK);
-        const int mmax = half ? C::L - 1 : C::L - 2;
-        int dir = (ek <= 0.0f) ? 1 : -1;
-        if (mk + dir > mmax || mk + dir < 0) dir = -dir;
-        code += (unsigned)dir << (k * BITS);
+        const int k = __ffs(eq) - 1;
+        // field k of c1 - c0 is 1 when e~0_k < 0 (u above the rounded integer)
+        const unsigned neg = ((c1 - c0) >> (k * BITS)) & 1u;
+        // toward u: integer coset +1 when u is above r0; half coset +1 when
+        // u is above r1, i.e. when e~0_k >= 0
+        const bool up = (neg != 0) != half;
+        c = up ? c + (1u << (k * BITS)) : c - (1u << (k * BITS));
     }
+    code = c;
     coset = half ? 1u : 0u;
-    return code;
+    return true;
 }
 
 // Block code of a general-path point.
+template <int BITS>
+__device__ __forceinline__ unsigned pack_point(const float (&r)[8], int coset);
+
+// The general path as an out-of-line call (it is rare: only rows whose scaled
+// maximum reaches the box edge exactly take it), arguments and result in
+// registers.  Returns (block code, coset).
+template <int BITS, bool STRICT>
+__device__ __noinline__ uint2 e8_slow(float4 lo, float4 hi) {
+    using C = Code<BITS>;
+    const float u[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    float r[8];
+    const int c = e8_general(u, STRICT, C::HI0, C::H, r);
+    return make_uint2(pack_point<BITS>(r, c), unsigned(c));
+}
+
 template <int BITS>
 __device__ __forceinline__ unsigned pack_point(const float (&r)[8], int coset) {
     using C = Code<BITS>;

@@ -109,10 +109,12 @@ int nq_plan(const nq_shape* shape, const nq_params* params, nq_layout* out);
 
 /* RoPE (cos, sin) table for split-half rotary embedding ("E8 walkthrough",
  * "What Makes This Hard in Practice", item 2; README "Supported models").
- * Host only, double precision rounded once to fp32:
- *   table[t][i][0] = cos(p_t * theta^(-2i/head_dim)),
- *   table[t][i][1] = sin(p_t * theta^(-2i/head_dim)),  i < head_dim/2,
- * p_t = positions[t] (host int32), or t when positions is NULL.
+ * Host only, double precision rounded once to fp32.  With angle(t, i) =
+ * p_t * theta^(-2i/head_dim), i < head_dim/2, p_t = positions[t] (host int32)
+ * or t when positions is NULL, the table is head_dim/4 planes of `tokens`
+ * float4, plane q holding for every token (cos, sin) of pair 2q then of pair
+ * 2q + 1:  table[(q * tokens + t) * 4 + 2m + {0: cos, 1: sin}] for pair 2q + m.
+ * (Token-minor planes let the kernels read it with coalesced 16-byte loads.)
  * table: caller-owned host buffer of tokens * head_dim floats.  Build it once
  * per (positions, theta, head_dim), copy it to the device and pass it to
  * nq_compress_kv / nq_decompress_kv. */

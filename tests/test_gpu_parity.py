@@ -244,7 +244,7 @@ def test_full_size_sampled_parity(nq, orc, name):
     for params in cfg.modes[:2]:
         rope = nq.RopeTable.build(T, D, params.rope_theta)
         if cs is None:
-            cs = rope.host.numpy()
+            cs = rope.pairs()
         buf = nq.compress_kv(K, V, params, rope)
         lay = nq.plan(cfg.shape, params)
         tp = int(lay.tokens_padded)

@@ -119,19 +119,20 @@ def test_compress_validates_before_touching_the_gpu(nq):
 
 @pytest.mark.parametrize("T,D,theta", [(512, 128, 1e4), (2048, 96, 1e4), (300, 128, 5e5), (1000, 64, 1e6)])
 def test_rope_table_equals_oracle_bit_for_bit(nq, orc, T, D, theta):
-    host = np.zeros((T, D // 2, 2), np.float32)
+    host = np.zeros((D // 4, T, 4), np.float32)
     st = nq.lib().nq_rope_table(None, T, D, theta, host.ctypes.data_as(ctypes.c_void_p))
     assert st == 0
-    ref = orc.rope_table(T, D, theta)
-    assert np.array_equal(host.view(np.uint32), ref.view(np.uint32))
+    ref = orc.rope_table(T, D, theta)  # [T, D/2, (cos, sin)]
+    got = host.transpose(1, 0, 2).reshape(T, D // 2, 2)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
 
 
 def test_rope_table_positions_and_errors(nq, orc):
     pos = np.array([5, 0, 131071, 77], np.int32)
-    host = np.zeros((4, 64, 2), np.float32)
+    host = np.zeros((32, 4, 4), np.float32)
     L = nq.lib()
     assert L.nq_rope_table(pos.ctypes.data_as(ctypes.c_void_p), 4, 128, 1e6, host.ctypes.data_as(ctypes.c_void_p)) == 0
-    assert np.array_equal(host, orc.rope_table(4, 128, 1e6, positions=pos))
+    assert np.array_equal(host.transpose(1, 0, 2).reshape(4, 64, 2), orc.rope_table(4, 128, 1e6, positions=pos))
     assert L.nq_rope_table(None, 4, 127, 1e4, host.ctypes.data_as(ctypes.c_void_p)) == nq.NQ_ERR_ARG
     assert L.nq_rope_table(None, 4, 128, 0.0, host.ctypes.data_as(ctypes.c_void_p)) == nq.NQ_ERR_ARG
     assert L.nq_rope_table(None, 4, 128, 1e4, None) == nq.NQ_ERR_ARG
