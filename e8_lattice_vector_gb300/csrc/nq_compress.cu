@@ -110,8 +110,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
 
-        // ---- Hadamard rotation
-        fwht<DP>(y);
+        // ---- Hadamard rotation (compression stage order)
+        fwht_forward<DP>(y);
 
         // ---- group absmax -> fp16 scale -> reciprocal (per 32-subgroup)
         float amax[NSUB];

@@ -61,35 +61,52 @@ __device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
     return d;
 }
 
-// Unnormalised Walsh-Hadamard transform, textbook stage order h = 1, 2, ...,
-// N/2.  Stage 1 runs on single lanes; every later stage pairs butterflies
-// (i, i+h) and (i+1, i+1+h) into one packed f32x2 add and one subtract (each
-// half is an ordinary IEEE round-to-nearest operation, so the results are
-// those of the scalar butterflies).
+// One butterfly stage (a, b) -> (a + b, a - b) over pairs (i, i + h).  For
+// h >= 2 the butterflies (i, i+h) and (i+1, i+1+h) share one packed f32x2 add
+// and one subtract (each half is an ordinary IEEE round-to-nearest operation,
+// so the results are those of the scalar butterflies).
+template <int N>
+__device__ __forceinline__ void fwht_stage(float (&y)[N], int h) {
+    if (h == 1) {
+#pragma unroll
+        for (int i = 0; i < N; i += 2) {
+            const float a = y[i], b = y[i + 1];
+            y[i] = __fadd_rn(a, b);
+            y[i + 1] = __fsub_rn(a, b);
+        }
+        return;
+    }
+#pragma unroll
+    for (int i = 0; i < N; i += 2) {
+        if ((i & h) == 0) {
+            const float2 a = make_float2(y[i], y[i + 1]);
+            const float2 b = make_float2(y[i + h], y[i + h + 1]);
+            const float2 s = __fadd2_rn(a, b);
+            const float2 d = fsub2(a, b);
+            y[i] = s.x;
+            y[i + 1] = s.y;
+            y[i + h] = d.x;
+            y[i + h + 1] = d.y;
+        }
+    }
+}
+
+// Unnormalised Walsh-Hadamard transform in the textbook stage order h = 1, 2,
+// ..., N/2 (the decompression direction).
 template <int N>
 __device__ __forceinline__ void fwht(float (&y)[N]) {
 #pragma unroll
-    for (int i = 0; i < N; i += 2) {
-        const float a = y[i], b = y[i + 1];
-        y[i] = __fadd_rn(a, b);
-        y[i + 1] = __fsub_rn(a, b);
-    }
+    for (int h = 1; h < N; h *= 2) fwht_stage<N>(y, h);
+}
+
+// The compression direction: the textbook order with its last two stages
+// exchanged (h = 1, ..., N/8, then N/2, then N/4).
+template <int N>
+__device__ __forceinline__ void fwht_forward(float (&y)[N]) {
 #pragma unroll
-    for (int h = 2; h < N; h *= 2) {
-#pragma unroll
-        for (int i = 0; i < N; i += 2) {
-            if ((i & h) == 0) {
-                const float2 a = make_float2(y[i], y[i + 1]);
-                const float2 b = make_float2(y[i + h], y[i + h + 1]);
-                const float2 s = __fadd2_rn(a, b);
-                const float2 d = fsub2(a, b);
-                y[i] = s.x;
-                y[i + 1] = s.y;
-                y[i + h] = d.x;
-                y[i + h + 1] = d.y;
-            }
-        }
-    }
+    for (int h = 1; h < N / 4; h *= 2) fwht_stage<N>(y, h);
+    fwht_stage<N>(y, N / 2);
+    fwht_stage<N>(y, N / 4);
 }
 
 // max of three (one instruction on sm_100 and later)

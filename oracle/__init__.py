@@ -34,6 +34,7 @@ def lib():
             "orc_rope_remove": (None, [_P, _I, _P]),
             "orc_rope_apply": (None, [_P, _I, _P]),
             "orc_fwht": (None, [_P, _I]),
+            "orc_fwht_forward": (None, [_P, _I]),
             "orc_group_scale": (ctypes.c_uint16, [_F, _I, _I]),
             "orc_e8_block": (_I, [_P, _I, _I, _P]),
             "orc_e8_nearest": (None, [_P, _P, _I64, _I, _I]),
@@ -97,6 +98,12 @@ def rope_apply(x, cs_row):
 def fwht(x):
     x = _c(x, np.float32).copy()
     lib().orc_fwht(_ptr(x), x.shape[-1])
+    return x
+
+
+def fwht_forward(x):
+    x = _c(x, np.float32).copy()
+    lib().orc_fwht_forward(_ptr(x), x.shape[-1])
     return x
 
 

@@ -106,16 +106,29 @@ void orc_rope_apply(float* x, int head_dim, const float* cs_row) {
  * Hadamard matrix; H is symmetric.  Reading: the unnormalised transform is
  * used; its factor sqrt(n) is absorbed by the group scale (compression) and
  * divided out exactly as a power of two (decompression). */
-void orc_fwht(float* x, int n) {
-    for (int h = 1; h < n; h *= 2) {
-        for (int i = 0; i < n; i += 2 * h) {
-            for (int j = i; j < i + h; ++j) {
-                float a = x[j], b = x[j + h];
-                x[j] = a + b;
-                x[j + h] = a - b;
-            }
+static void butterfly_stage(float* x, int n, int h) {
+    for (int i = 0; i < n; i += 2 * h) {
+        for (int j = i; j < i + h; ++j) {
+            float a = x[j], b = x[j + h];
+            x[j] = a + b;
+            x[j + h] = a - b;
         }
     }
+}
+
+/* Textbook order h = 1, 2, 4, ..., n/2 (used by decompression). */
+void orc_fwht(float* x, int n) {
+    for (int h = 1; h < n; h *= 2) butterfly_stage(x, n, h);
+}
+
+/* Reading: every butterfly order computes H x; in fp32 the order fixes the
+ * rounding, so compression fixes one: the textbook order with its last two
+ * stages exchanged (h = 1, ..., n/8, then n/2, then n/4). */
+void orc_fwht_forward(float* x, int n) {
+    for (int h = 1; h < n / 4; h *= 2) butterfly_stage(x, n, h);
+    if (n >= 4) butterfly_stage(x, n, n / 2);
+    if (n >= 4) butterfly_stage(x, n, n / 4);
+    if (n == 2) butterfly_stage(x, n, 1);
 }
 
 /* ------------------------------------------------------------- group scale */
@@ -248,7 +261,7 @@ void orc_encode_row(const uint16_t* x, const float* cs_row, int head_dim, int bi
     float y[128];
     for (int i = 0; i < dp; ++i) y[i] = (i < head_dim) ? orc_h2f(x[i]) : 0.0f;
     if (cs_row) orc_rope_remove(y, head_dim, cs_row);
-    orc_fwht(y, dp); /* zero padding to dp happened above */
+    orc_fwht_forward(y, dp); /* zero padding to dp happened above */
 
     memset(idx, 0, (size_t)dp * bits / 8);
     uint16_t cw = 0;

@@ -52,9 +52,12 @@ void orc_rope_table(const int32_t* pos, int tokens, int head_dim, float theta, f
 void orc_rope_remove(float* x, int head_dim, const float* cs_row);
 void orc_rope_apply(float* x, int head_dim, const float* cs_row);
 
-/* Unnormalised Sylvester Walsh-Hadamard transform in place, n a power of two,
- * textbook butterfly order h = 1, 2, 4, ..., n/2. */
+/* Unnormalised Sylvester Walsh-Hadamard transform in place, n a power of two:
+ * orc_fwht in the textbook butterfly order h = 1, 2, 4, ..., n/2 (inverse
+ * direction); orc_fwht_forward with the last two stages exchanged (h = 1, ...,
+ * n/8, n/2, n/4; compression direction). */
 void orc_fwht(float* x, int n);
+void orc_fwht_forward(float* x, int n);
 
 /* Group scale: the smallest non-negative binary16 value v (returned as bits)
  * such that v * (dp * (2^bits - 1) / 2) >= amax. */

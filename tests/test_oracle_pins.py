@@ -204,8 +204,10 @@ def test_t2_norm2_shell_counts(orc):
 
 
 @pytest.mark.parametrize("n", [8, 64, 128])
-def test_t3_fwht_is_sylvester_hadamard(orc, n):
-    H = np.stack([orc.fwht(np.eye(n, dtype=np.float32)[j]) for j in range(n)], axis=1)
+@pytest.mark.parametrize("order", ["textbook", "forward"])
+def test_t3_fwht_is_sylvester_hadamard(orc, n, order):
+    f = orc.fwht if order == "textbook" else orc.fwht_forward
+    H = np.stack([f(np.eye(n, dtype=np.float32)[j]) for j in range(n)], axis=1)
     i = np.arange(n)
     pop = np.vectorize(lambda v: bin(v).count("1"))(i[:, None] & i[None, :])
     assert np.array_equal(H, (-1.0) ** pop)
@@ -217,11 +219,16 @@ def test_t3_fwht_involution_and_matrix_product(orc):
     n = 128
     xi = rng.integers(-1000, 1000, size=n).astype(np.float32)
     assert np.array_equal(orc.fwht(orc.fwht(xi)), n * xi)  # exact on integers
+    assert np.array_equal(orc.fwht(orc.fwht_forward(xi)), n * xi)
     x = rng.normal(size=n).astype(np.float32)
     i = np.arange(n)
     H = (-1.0) ** np.vectorize(lambda v: bin(v).count("1"))(i[:, None] & i[None, :])
     ref = H @ x.astype(np.float64)
-    assert np.allclose(orc.fwht(x), ref, rtol=0, atol=1e-5 * np.abs(x).sum())
+    for f in (orc.fwht, orc.fwht_forward):
+        assert np.allclose(f(x), ref, rtol=0, atol=1e-5 * np.abs(x).sum())
+    # the two orders round differently somewhere (otherwise the order would not matter)
+    xs = rng.normal(size=(200, n)).astype(np.float32) * 10.0 ** rng.integers(-3, 4, size=(200, 1))
+    assert any(not np.array_equal(orc.fwht(v), orc.fwht_forward(v)) for v in xs)
 
 
 def test_t3_zero_padded_round_trip(orc):
@@ -441,7 +448,7 @@ def test_row_exact_codebook_points_round_trip(orc):
         r[0:8] = [3.5, -0.5, 0.5, 0.5, -0.5, 0.5, 1.5, -2.5]
         r[64:72] = [-3.5, 0.5, 2.5, -1.5, 0.5, 0.5, -0.5, 0.5]
         sc = 2.0 ** -6
-        x = orc.fwht((r * sc).astype(np.float32))  # x = H (r * sc)
+        x = orc.fwht((r * sc).astype(np.float32))  # x = H (r * sc), exact here
         xb = x.astype(np.float16).view(np.uint16)
         assert np.array_equal(xb.view(np.float16).astype(np.float32), x)  # exact in fp16
         idx, cw, scl = orc.encode_row(xb, D, bits, G, 0)
