@@ -97,7 +97,7 @@ bool ensure_smem(const void* kernel, int smem) {
     return true;
 }
 
-bool make_row_tile_map(CUtensorMap* map, void* base, int head_dim, int tokens, int64_t slices) {
+bool make_row_tile_map(CUtensorMap* map, void* base, int head_dim, int tokens, int64_t slices, int box_rows) {
     static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     static std::once_flag once;
     std::call_once(once, [] {
@@ -111,7 +111,7 @@ bool make_row_tile_map(CUtensorMap* map, void* base, int head_dim, int tokens, i
     if (!encode) return false;
     const cuuint64_t dims[3] = {cuuint64_t(head_dim), cuuint64_t(tokens), cuuint64_t(slices)};
     const cuuint64_t strides[2] = {cuuint64_t(head_dim) * 2, cuuint64_t(head_dim) * 2 * cuuint64_t(tokens)};
-    const cuuint32_t box[3] = {64, 32, 1};
+    const cuuint32_t box[3] = {64, cuuint32_t(box_rows), 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

@@ -209,6 +209,230 @@ __global__ void __launch_bounds__(kThreads, 1)
     cp_async_wait<0>();
 }
 
+
+// ------------------------------------------------------- two threads per row
+//
+// head_dim 64 and 128: lanes 2r and 2r+1 share token row r of a 16-row tile
+// (PairMap): each thread holds 64 (or 32) coordinates, so the kernel fits 128
+// registers and two blocks per SM.  The Hadamard transform runs in the
+// compression stage order; its stage on bit DP/2 is in-thread with a sign
+// that leaves the odd thread's slot halves exchanged, so the last stage
+// (bit DP/4) is one symmetric shuffle exchange.  Afterwards thread hf holds
+// coordinates [hf*DP/2, (hf+1)*DP/2) in natural order, the odd thread's upper
+// quarter negated, which is folded into the sign of its reciprocal scale.
+constexpr int kPairStages = 3;
+constexpr int kPairCompressSmem = kWarpsPerBlock * kPairStages * kPairTileBytes;
+
+// The walk runs over the padded token range (tokens rounded up to 32) so that
+// every record row, padding included, is written; rows at or past `tokens`
+// are zero-filled.
+template <int D>
+__device__ __forceinline__ void load_pair_tile(const __half* __restrict__ x, const TileWalkT<kPairRows>& w,
+                                               int tokens, uint32_t stage, int lane) {
+    constexpr int CPR = D / 8;  // 16-byte chunks per row
+    const int nvalid = min(kPairRows, tokens - w.t0);
+    const __half* base = x + (w.slice * tokens + min(w.t0, tokens - 1)) * int64_t(D);
+#pragma unroll
+    for (int i = 0; i < CPR / 2; ++i) {  // 16 rows * CPR chunks / 32 lanes
+        const int g = lane + 32 * i;
+        const int r = g / CPR;
+        const int c = g - r * CPR;
+        const bool ok = r < nvalid;
+        cp_async16(stage + swz16(r, c), ok ? base + 8 * g : base, ok ? 16 : 0);
+    }
+}
+
+template <int NBYTES>
+__device__ __forceinline__ void store_words(uint8_t* dst, const unsigned* w) {
+    if constexpr (NBYTES % 16 == 0) {
+#pragma unroll
+        for (int q = 0; q < NBYTES / 16; ++q)
+            st_stream(reinterpret_cast<uint4*>(dst) + q, make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]));
+    } else if constexpr (NBYTES % 8 == 0) {
+#pragma unroll
+        for (int q = 0; q < NBYTES / 8; ++q) reinterpret_cast<uint2*>(dst)[q] = make_uint2(w[2 * q], w[2 * q + 1]);
+    } else {
+#pragma unroll
+        for (int q = 0; q < NBYTES / 4; ++q) reinterpret_cast<unsigned*>(dst)[q] = w[q];
+    }
+}
+
+template <int D, int BITS, bool STRICT>
+__global__ void __launch_bounds__(kThreads, 2)
+    compress_pair_kernel(const __half* __restrict__ x, const float4* __restrict__ rope, int64_t slices,
+                         int tokens, int tpad, int group, int chunk, bool delta, uint8_t* __restrict__ idx,
+                         uint16_t* __restrict__ coset, __half* __restrict__ scales) {
+    constexpr int DP = D;
+    using PM = PairMap<DP>;
+    constexpr int HALF = PM::HALF;
+    constexpr int Q = PM::Q;
+    constexpr int NBT = PM::NBT;
+    constexpr int NSUB = HALF / 32;  // 32-coordinate subgroups per thread
+    using C = Code<BITS>;
+    using RP = RowPack<BITS, NBT>;
+    constexpr int RB = DP * BITS / 8;  // idx bytes per row
+    constexpr int RBT = RB / 2;        // idx bytes per thread
+    constexpr float STEP = float(DP) * C::H;
+    using Walk = TileWalkT<kPairRows>;
+
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int lane = threadIdx.x & 31;
+    const int hf = lane & 1;
+    const int r = lane >> 1;
+    const float sgn = hf ? -1.0f : 1.0f;
+    const uint32_t ring = smem_u32(smem) + (threadIdx.x >> 5) * (kPairStages * kPairTileBytes);
+    const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    const int nsc = DP / group;
+    const int span = group / 32;  // 32-coordinate subgroups per scale group
+
+    Walk cur(warp, nwarps, slices, tpad, chunk);
+    Walk pre = cur;
+#pragma unroll
+    for (int s = 0; s < kPairStages - 1; ++s) {
+        if (pre.valid()) {
+            load_pair_tile<D>(x, pre, tokens, ring + s * kPairTileBytes, lane);
+            pre.next();
+        }
+        cp_async_commit();
+    }
+
+    unsigned carry[NBT];
+    unsigned carry_c = 0;
+#pragma unroll
+    for (int k = 0; k < NBT; ++k) carry[k] = 0;
+
+    for (int i = 0; cur.valid(); ++i) {
+        if (pre.valid()) {
+            load_pair_tile<D>(x, pre, tokens, ring + ((i + kPairStages - 1) % kPairStages) * kPairTileBytes, lane);
+            pre.next();
+        }
+        cp_async_commit();
+        cp_async_wait<kPairStages - 1>();
+        __syncwarp();
+        const uint32_t stage = ring + (i % kPairStages) * kPairTileBytes;
+        const int t = cur.t0 + r;
+        const bool active = t < tokens;
+
+        // ---- the thread's 64 (32) coordinates of row r
+        float y[HALF];
+#pragma unroll
+        for (int c = 0; c < NBT; ++c) h8_to_f(lds128(stage + swz16(r, PM::chunk(hf, c))), &y[8 * c]);
+        __syncwarp();  // every lane has its coordinates: the stage may be refilled
+
+        // ---- RoPE removal on keys: pairs (i, i + D/2) are slots (l, l + Q)
+        if (rope != nullptr) {
+            const float4* cs = rope + (active ? t : 0);
+#pragma unroll
+            for (int qq = 0; qq < Q / 2; ++qq) {
+                const float4 v = __ldg(cs + int64_t(hf * (Q / 2) + qq) * tokens);
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    const int l = 2 * qq + p;
+                    const float c = p ? v.z : v.x, s = p ? v.w : v.y;
+                    const float a = y[l], b = y[l + Q];
+                    y[l] = __fmaf_rn(a, c, __fmul_rn(b, s));
+                    y[l + Q] = __fmaf_rn(b, c, -__fmul_rn(a, s));
+                }
+            }
+        }
+
+        // ---- Hadamard rotation, compression order: bits below DP/4 in-thread,
+        //      bit DP/2 in-thread (signed), bit DP/4 by exchange
+#pragma unroll
+        for (int h = 1; h < Q; h *= 2) fwht_stage<HALF>(y, h);
+        stage_signed<HALF>(y, sgn);
+        stage_exchange<HALF>(y);
+
+        // ---- group absmax -> fp16 scale -> reciprocal (per 32-subgroup)
+        float amax[NSUB];
+#pragma unroll
+        for (int s = 0; s < NSUB; ++s) {
+            float m = 0.0f;
+#pragma unroll
+            for (int j = 32 * s; j < 32 * s + 32; j += 2) m = fmax3(m, fabsf(y[j]), fabsf(y[j + 1]));
+            amax[s] = m;
+        }
+        if (NSUB == 2 && span >= 2) amax[0] = amax[1] = fmaxf(amax[0], amax[1]);
+        if (span > NSUB) {
+            const float o = __shfl_xor_sync(kFull, amax[0], 1);
+#pragma unroll
+            for (int s = 0; s < NSUB; ++s) amax[s] = fmaxf(amax[s], o);
+        }
+        unsigned short sc[NSUB];
+        float inv[NSUB];
+        bool fast = true;
+#pragma unroll
+        for (int s = 0; s < NSUB; ++s) {
+            sc[s] = group_scale(amax[s], STEP);
+            const float scf = __half2float(__ushort_as_half(sc[s]));
+            inv[s] = sc[s] ? __frcp_rn(__fmul_rn(scf, float(DP))) : 0.0f;
+            fast = fast && (__fmul_rn(amax[s], inv[s]) < C::H);
+        }
+
+        // ---- E8 nearest point per 8-block -> block codes
+        unsigned blk[NBT];
+        unsigned cwl = 0;
+#pragma unroll
+        for (int k = 0; k < NBT; ++k) {
+            // slots at or above Q hold the odd thread's negated coordinates
+            const float ik = (8 * k >= Q) ? __fmul_rn(inv[(8 * k) / 32], sgn) : inv[(8 * k) / 32];
+            float u[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) u[j] = __fmul_rn(y[8 * k + j], ik);
+            unsigned c;
+            if (!(fast && e8_fast<BITS, STRICT>(u, blk[k], c))) {
+                const uint2 res = e8_slow<BITS, STRICT>(make_float4(u[0], u[1], u[2], u[3]),
+                                                        make_float4(u[4], u[5], u[6], u[7]));
+                blk[k] = res.x;
+                c = res.y;
+            }
+            cwl |= c << k;
+        }
+        unsigned cw = cwl << (hf * NBT);
+        cw |= __shfl_xor_sync(kFull, cw, 1);
+
+        // ---- temporal delta against the previous token (row r - 1: lane - 2)
+        if (delta) {
+            const bool first = cur.t0 == cur.t_begin;
+#pragma unroll
+            for (int k = 0; k < NBT; ++k) {
+                unsigned prev = __shfl_up_sync(kFull, blk[k], 2);
+                const unsigned last = __shfl_sync(kFull, blk[k], 30 + hf);
+                if (r == 0) prev = first ? 0u : carry[k];
+                if (t != cur.t_begin) blk[k] = swar_sub<BITS>(blk[k], prev);
+                carry[k] = last;  // raw codes of the tile's last token
+            }
+            unsigned pc = __shfl_up_sync(kFull, cw, 2);
+            const unsigned lastc = __shfl_sync(kFull, cw, 30);
+            if (r == 0) pc = first ? 0u : carry_c;
+            if (t != cur.t_begin) cw ^= pc;
+            carry_c = lastc;
+        }
+
+        // ---- store (padding rows past the slice get zeros)
+        if (!active) {
+#pragma unroll
+            for (int k = 0; k < NBT; ++k) blk[k] = 0;
+            cw = 0;
+#pragma unroll
+            for (int s = 0; s < NSUB; ++s) sc[s] = 0;
+        }
+        const int64_t rrow = cur.slice * tpad + t;
+        unsigned w[RP::WORDS];
+        RP::pack(blk, w);
+        store_words<RBT>(idx + rrow * RB + hf * RBT, w);
+        if (hf == 0) coset[rrow] = uint16_t(cw);
+#pragma unroll
+        for (int s = 0; s < NSUB; ++s) {
+            const int gs = hf * NSUB + s;  // global 32-subgroup
+            if (gs % span == 0) scales[rrow * nsc + gs / span] = __ushort_as_half(sc[s]);
+        }
+        cur.next();
+    }
+    cp_async_wait<0>();
+}
+
 template <int D, int BITS, bool STRICT>
 static int launch(const LaunchArgs& a, const __half* x, const float4* rope, uint8_t* idx,
                   uint16_t* coset, __half* scales) {
@@ -226,13 +450,34 @@ static int launch(const LaunchArgs& a, const __half* x, const float4* rope, uint
     return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
 }
 
+template <int D, int BITS, bool STRICT>
+static int launch_pair(const LaunchArgs& a, const __half* x, const float4* rope, uint8_t* idx,
+                       uint16_t* coset, __half* scales) {
+    auto kern = compress_pair_kernel<D, BITS, STRICT>;
+    if (!ensure_smem(reinterpret_cast<const void*>(kern), kPairCompressSmem)) return NQ_ERR_CUDA;
+    const int chunk = a.delta_chunk > 0 ? a.delta_chunk : kPairRows;
+    const int64_t items = a.slices * ((a.tpad + chunk - 1) / chunk);
+    const int64_t want = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    if (want == 0) return NQ_OK;
+    const int cap = grid_capacity(reinterpret_cast<const void*>(kern), kPairCompressSmem);
+    if (cap <= 0) return NQ_ERR_CUDA;
+    const int grid = int(std::min<int64_t>(want, cap));
+    kern<<<grid, kThreads, kPairCompressSmem, a.stream>>>(x, rope, a.slices, a.tokens, a.tpad, a.group, chunk,
+                                                          a.delta_chunk > 0, idx, coset, scales);
+    return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
+}
+
 template <int D>
 static int dispatch_bits(const LaunchArgs& a, int bits, bool strict, const __half* x,
                          const float4* rope, uint8_t* idx, uint16_t* coset, __half* scales) {
-#define NQ_CASE(B)                                                         \
-    case B:                                                                \
-        return strict ? launch<D, B, true>(a, x, rope, idx, coset, scales) \
-                      : launch<D, B, false>(a, x, rope, idx, coset, scales);
+#define NQ_CASE(B)                                                                              \
+    case B:                                                                                     \
+        if constexpr (D == 96)                                                                  \
+            return strict ? launch<D, B, true>(a, x, rope, idx, coset, scales)                  \
+                          : launch<D, B, false>(a, x, rope, idx, coset, scales);                \
+        else                                                                                    \
+            return strict ? launch_pair<D, B, true>(a, x, rope, idx, coset, scales)             \
+                          : launch_pair<D, B, false>(a, x, rope, idx, coset, scales);
     switch (bits) {
         NQ_CASE(2)
         NQ_CASE(3)

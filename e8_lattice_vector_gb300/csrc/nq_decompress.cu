@@ -199,6 +199,241 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// ------------------------------------------------------- two threads per row
+//
+// head_dim 64 and 128: lanes 2r and 2r+1 share record row r of a 16-row tile.
+// Thread hf unpacks scale-group half hf (blocks [hf*NBT, (hf+1)*NBT)); the
+// inverse Hadamard transform (textbook order) runs its bits below DP/4
+// in-thread, bit DP/4 in-thread with a sign that leaves the odd thread's slot
+// halves exchanged, and bit DP/2 as one symmetric shuffle exchange, after which
+// the slots hold the RoPE pairs (PairMap layout; the odd thread's upper slots
+// negated, undone by a sign flip of sin in the rotation and of the fp16 bits).
+constexpr int kPairRecIdx = 0;      // 16 * RB <= 1024 bytes
+constexpr int kPairRecCoset = 1024; // 16 coset words
+constexpr int kPairRecScale = 1056; // 16 * (Dp / group) fp16 <= 128 bytes
+constexpr int kPairRecStage = 1280;
+constexpr int kPairWarpSmem = (kOutBufs * kPairTileBytes + kStages * kPairRecStage + 1023) / 1024 * 1024;
+constexpr int kPairDecompressSmem = kWarpsPerBlock * kPairWarpSmem + 1024;
+
+template <int RB>
+__device__ __forceinline__ void load_pair_records(const uint8_t* __restrict__ idx,
+                                                  const uint16_t* __restrict__ coset,
+                                                  const __half* __restrict__ scales, int nsc, int64_t row0,
+                                                  uint32_t stage, int lane) {
+    const uint8_t* ib = idx + row0 * RB;  // 16 * RB bytes = RB chunks
+#pragma unroll
+    for (int g = lane; g < RB; g += 32) cp_async16(stage + kPairRecIdx + 16 * g, ib + 16 * g, 16);
+    if (lane < 2) cp_async16(stage + kPairRecCoset + 16 * lane, coset + row0 + 8 * lane, 16);
+    const int nsch = 2 * nsc;  // 16 * nsc * 2 / 16
+    if (lane < nsch) cp_async16(stage + kPairRecScale + 16 * lane, scales + row0 * nsc + 8 * lane, 16);
+}
+
+template <int NBYTES>
+__device__ __forceinline__ void lds_words(uint32_t a, unsigned* w) {
+    if constexpr (NBYTES % 16 == 0) {
+#pragma unroll
+        for (int q = 0; q < NBYTES / 16; ++q) {
+            const uint4 v = lds128(a + 16 * q);
+            w[4 * q] = v.x;
+            w[4 * q + 1] = v.y;
+            w[4 * q + 2] = v.z;
+            w[4 * q + 3] = v.w;
+        }
+    } else if constexpr (NBYTES % 8 == 0) {
+#pragma unroll
+        for (int q = 0; q < NBYTES / 8; ++q) {
+            const uint2 v = lds64(a + 8 * q);
+            w[2 * q] = v.x;
+            w[2 * q + 1] = v.y;
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < NBYTES / 4; ++q) asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w[q]) : "r"(a + 4 * q));
+    }
+}
+
+template <int D, int BITS>
+__global__ void __launch_bounds__(kThreads, 2)
+    decompress_pair_kernel(const uint8_t* __restrict__ idx, const uint16_t* __restrict__ coset,
+                           const __half* __restrict__ scales, const float4* __restrict__ rope,
+                           const __grid_constant__ CUtensorMap out_map, int64_t slices, int tokens, int tpad,
+                           int group, int chunk, bool delta) {
+    constexpr int DP = D;
+    using PM = PairMap<DP>;
+    constexpr int HALF = PM::HALF;
+    constexpr int Q = PM::Q;
+    constexpr int NBT = PM::NBT;
+    constexpr int NSUB = HALF / 32;
+    using C = Code<BITS>;
+    using RP = RowPack<BITS, NBT>;
+    constexpr int RB = DP * BITS / 8;
+    constexpr int RBT = RB / 2;
+    using Walk = TileWalkT<kPairRows>;
+
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int lane = threadIdx.x & 31;
+    const int hf = lane & 1;
+    const int r = lane >> 1;
+    const float sgn = hf ? -1.0f : 1.0f;
+    const unsigned negbits = hf ? 0x80008000u : 0u;
+    const uint32_t base = (smem_u32(smem) + 1023u) & ~1023u;
+    const uint8_t* gbase = smem + (base - smem_u32(smem));
+    const uint32_t wbase = base + (threadIdx.x >> 5) * kPairWarpSmem;
+    const uint32_t outbuf = wbase;
+    const uint32_t ring = wbase + kOutBufs * kPairTileBytes;
+    const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    const int nsc = DP / group;
+    const int span = group / 32;
+
+    Walk cur(warp, nwarps, slices, tokens, chunk);
+    Walk pre = cur;
+#pragma unroll
+    for (int s = 0; s < kStages - 1; ++s) {
+        if (pre.valid()) {
+            load_pair_records<RB>(idx, coset, scales, nsc, pre.slice * tpad + pre.t0, ring + s * kPairRecStage, lane);
+            pre.next();
+        }
+        cp_async_commit();
+    }
+
+    unsigned carry[NBT];
+    unsigned carry_c = 0;
+#pragma unroll
+    for (int k = 0; k < NBT; ++k) carry[k] = 0;
+
+    for (int i = 0; cur.valid(); ++i) {
+        if (pre.valid()) {
+            load_pair_records<RB>(idx, coset, scales, nsc, pre.slice * tpad + pre.t0,
+                                  ring + ((i + kStages - 1) % kStages) * kPairRecStage, lane);
+            pre.next();
+        }
+        cp_async_commit();
+        cp_async_wait<kStages - 1>();
+        __syncwarp();
+        const uint32_t stage = ring + (i % kStages) * kPairRecStage;
+        const uint8_t* gstage = gbase + (stage - base);
+        const int t = cur.t0 + r;
+
+        // ---- the thread's half of the record
+        unsigned w[RP::WORDS];
+        lds_words<RBT>(stage + kPairRecIdx + r * RB + hf * RBT, w);
+        const unsigned cw_full = reinterpret_cast<const uint16_t*>(gstage + kPairRecCoset)[r];
+        unsigned cw = (cw_full >> (hf * NBT)) & ((1u << NBT) - 1u);
+        float scf[NSUB];
+#pragma unroll
+        for (int s = 0; s < NSUB; ++s)
+            scf[s] = __half2float(reinterpret_cast<const __half*>(gstage + kPairRecScale)[r * nsc + (hf * NSUB + s) / span]);
+        __syncwarp();  // the stage may be refilled
+        unsigned blk[NBT];
+        RP::unpack(w, blk);
+
+        // ---- undo the temporal delta: inclusive scan over rows (lane stride 2) + carry
+        if (delta) {
+#pragma unroll
+            for (int off = 2; off < 32; off *= 2) {
+#pragma unroll
+                for (int k = 0; k < NBT; ++k) {
+                    const unsigned v = __shfl_up_sync(kFull, blk[k], off);
+                    if (lane >= off) blk[k] = swar_add<BITS>(blk[k], v);
+                }
+                const unsigned vc = __shfl_up_sync(kFull, cw, off);
+                if (lane >= off) cw ^= vc;
+            }
+            const bool first = cur.t0 == cur.t_begin;
+#pragma unroll
+            for (int k = 0; k < NBT; ++k) {
+                if (!first) blk[k] = swar_add<BITS>(blk[k], carry[k]);
+                carry[k] = __shfl_sync(kFull, blk[k], 30 + hf);
+            }
+            if (!first) cw ^= carry_c;
+            carry_c = __shfl_sync(kFull, cw, 30 + hf);
+        }
+
+        // ---- unpack, unscale: y = (code - offset) * scale  (exact)
+        float y[HALF];
+#pragma unroll
+        for (int k = 0; k < NBT; ++k) {
+            const float off = ((cw >> k) & 1u) ? C::H : C::HI0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const unsigned m = (blk[k] >> (j * BITS)) & C::MASK;
+                const float mf = __fsub_rn(__uint_as_float(0x4B000000u | m), 8388608.0f);
+                y[8 * k + j] = __fmul_rn(__fsub_rn(mf, off), scf[(8 * k) / 32]);
+            }
+        }
+
+        // ---- inverse Hadamard (textbook order): bits below DP/4 in-thread, bit
+        //      DP/4 in-thread (signed), bit DP/2 by exchange
+#pragma unroll
+        for (int h = 1; h < Q; h *= 2) fwht_stage<HALF>(y, h);
+        stage_signed<HALF>(y, sgn);
+        stage_exchange<HALF>(y);
+
+        // ---- RoPE re-apply on keys: pairs (i, i + D/2) are slots (l, l + Q)
+        if (rope != nullptr) {
+            const float4* cs = rope + (t < cur.t_end ? t : cur.t_begin);
+#pragma unroll
+            for (int qq = 0; qq < Q / 2; ++qq) {
+                const float4 v = __ldg(cs + int64_t(hf * (Q / 2) + qq) * tokens);
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    const int l = 2 * qq + p;
+                    const float c = p ? v.z : v.x;
+                    const float s = __fmul_rn(p ? v.w : v.y, sgn);  // odd thread: upper slot negated
+                    const float a = y[l], b = y[l + Q];
+                    y[l] = __fmaf_rn(a, c, -__fmul_rn(b, s));
+                    y[l + Q] = __fmaf_rn(b, c, __fmul_rn(a, s));
+                }
+            }
+        }
+
+        // ---- fp16 rows -> swizzled smem tile -> TMA tensor store (16 rows)
+        const uint32_t ob = outbuf + (i & 1) * kPairTileBytes;
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < NBT; ++c) {
+            uint4 v = f_to_h8(&y[8 * c]);
+            if (8 * c >= Q) {
+                v.x ^= negbits;
+                v.y ^= negbits;
+                v.z ^= negbits;
+                v.w ^= negbits;
+            }
+            sts128(ob + swz16(r, PM::chunk(hf, c)), v);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+            const int z = int(cur.slice);
+            tma_store_3d(&out_map, ob, 0, cur.t0, z);
+            if (D > 64) tma_store_3d(&out_map, ob + 2048, 64, cur.t0, z);
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+        cur.next();
+    }
+    cp_async_wait<0>();
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+template <int D, int BITS>
+static int launch_pair(const LaunchArgs& a, const uint8_t* idx, const uint16_t* coset, const __half* scales,
+                       const float4* rope, const CUtensorMap& map) {
+    auto kern = decompress_pair_kernel<D, BITS>;
+    if (!ensure_smem(reinterpret_cast<const void*>(kern), kPairDecompressSmem)) return NQ_ERR_CUDA;
+    const int chunk = a.delta_chunk > 0 ? a.delta_chunk : kPairRows;
+    const int64_t items = a.slices * ((a.tokens + chunk - 1) / chunk);
+    const int64_t want = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    if (want == 0) return NQ_OK;
+    const int cap = grid_capacity(reinterpret_cast<const void*>(kern), kPairDecompressSmem);
+    if (cap <= 0) return NQ_ERR_CUDA;
+    const int grid = int(std::min<int64_t>(want, cap));
+    kern<<<grid, kThreads, kPairDecompressSmem, a.stream>>>(idx, coset, scales, rope, map, a.slices, a.tokens,
+                                                            a.tpad, a.group, chunk, a.delta_chunk > 0);
+    return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
+}
+
 template <int D, int BITS>
 static int launch(const LaunchArgs& a, const uint8_t* idx, const uint16_t* coset, const __half* scales,
                   const float4* rope, const CUtensorMap& map) {
@@ -216,16 +451,25 @@ static int launch(const LaunchArgs& a, const uint8_t* idx, const uint16_t* coset
     return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
 }
 
+template <int D, int BITS>
+static int launch_any(const LaunchArgs& a, const uint8_t* idx, const uint16_t* coset, const __half* scales,
+                      const float4* rope, const CUtensorMap& map) {
+    if constexpr (D != 64)
+        return launch<D, BITS>(a, idx, coset, scales, rope, map);
+    else
+        return launch_pair<D, BITS>(a, idx, coset, scales, rope, map);
+}
+
 template <int D>
 static int dispatch_bits(const LaunchArgs& a, int bits, const uint8_t* idx, const uint16_t* coset,
                          const __half* scales, const float4* rope, const CUtensorMap& map) {
     switch (bits) {
         case 2:
-            return launch<D, 2>(a, idx, coset, scales, rope, map);
+            return launch_any<D, 2>(a, idx, coset, scales, rope, map);
         case 3:
-            return launch<D, 3>(a, idx, coset, scales, rope, map);
+            return launch_any<D, 3>(a, idx, coset, scales, rope, map);
         case 4:
-            return launch<D, 4>(a, idx, coset, scales, rope, map);
+            return launch_any<D, 4>(a, idx, coset, scales, rope, map);
         default:
             return NQ_ERR_UNSUPPORTED;
     }
@@ -235,7 +479,8 @@ int launch_decompress_tensor(const LaunchArgs& a, int head_dim, int bits, const 
                              const uint16_t* coset, const uint16_t* scales, const float* rope,
                              void* x_out) {
     CUtensorMap map;
-    if (!make_row_tile_map(&map, x_out, head_dim, a.tokens, a.slices)) return NQ_ERR_CUDA;
+    const int box_rows = head_dim != 64 ? kTileRows : kPairRows;
+    if (!make_row_tile_map(&map, x_out, head_dim, a.tokens, a.slices, box_rows)) return NQ_ERR_CUDA;
     const __half* sh = reinterpret_cast<const __half*>(scales);
     const float4* r = reinterpret_cast<const float4*>(rope);
     switch (head_dim) {

@@ -109,6 +109,48 @@ __device__ __forceinline__ void fwht_forward(float (&y)[N]) {
     fwht_stage<N>(y, N / 4);
 }
 
+// Butterfly stage on slot pairs (l, l + Q) with a per-thread sign:
+// (P, Q) -> (P + sgn*Q, P - sgn*Q).  fma(x, +-1, y) is exactly y +- x, so with
+// sgn = +1 this is the plain butterfly and with sgn = -1 it is the butterfly
+// with its two outputs exchanged.
+template <int N>
+__device__ __forceinline__ void stage_signed(float (&y)[N], float sgn) {
+    constexpr int Q = N / 2;
+#pragma unroll
+    for (int l = 0; l < Q; l += 2) {
+        const float2 p = make_float2(y[l], y[l + 1]);
+        const float2 q = make_float2(y[l + Q], y[l + Q + 1]);
+        const float2 a = __ffma2_rn(q, make_float2(sgn, sgn), p);
+        const float2 b = __ffma2_rn(q, make_float2(-sgn, -sgn), p);
+        y[l] = a.x;
+        y[l + 1] = a.y;
+        y[l + Q] = b.x;
+        y[l + Q + 1] = b.y;
+    }
+}
+
+// Exchange stage between the two threads of a row: each sends slots
+// [N/2, N) to its partner and makes (own + recv, own - recv) from slots
+// [0, N/2) and the received values.
+template <int N>
+__device__ __forceinline__ void stage_exchange(float (&y)[N]) {
+    constexpr int Q = N / 2;
+    float r[Q];
+#pragma unroll
+    for (int l = 0; l < Q; ++l) r[l] = __shfl_xor_sync(kFull, y[l + Q], 1);
+#pragma unroll
+    for (int l = 0; l < Q; l += 2) {
+        const float2 a = make_float2(y[l], y[l + 1]);
+        const float2 b = make_float2(r[l], r[l + 1]);
+        const float2 s = __fadd2_rn(a, b);
+        const float2 d = fsub2(a, b);
+        y[l] = s.x;
+        y[l + 1] = s.y;
+        y[l + Q] = d.x;
+        y[l + Q + 1] = d.y;
+    }
+}
+
 // max of three (one instruction on sm_100 and later)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float r;
@@ -365,6 +407,27 @@ __device__ __forceinline__ uint32_t swz(int r, int q) {
     return uint32_t(((q >> 3) << 12) + (r << 7) + (((q & 7) ^ (r & 7)) << 4));
 }
 
+// The same layout for a 16-row tile (boxes of 16 rows x 128 bytes = 2 KB).
+constexpr int kPairRows = 16;
+constexpr int kPairTileBytes = 4096;
+__device__ __forceinline__ uint32_t swz16(int r, int q) {
+    return uint32_t(((q >> 3) << 11) + (r << 7) + (((q & 7) ^ (r & 7)) << 4));
+}
+
+// Two threads per row (lanes 2r and 2r+1 share row r): thread hf owns the
+// coordinates hf*Q + l (slot l < Q) and DP/2 + hf*Q + (l - Q) (slot l >= Q),
+// Q = DP/4, so the RoPE partners (i, i + DP/2) sit in slots (l, l + Q).
+template <int DP>
+struct PairMap {
+    static constexpr int HALF = DP / 2;  // coordinates per thread
+    static constexpr int Q = DP / 4;
+    static constexpr int NBT = HALF / 8;  // 8-blocks (and 16-byte fp16 chunks) per thread
+    // global 16-byte chunk (8 coordinates) of the thread's slot chunk c
+    __device__ static __forceinline__ int chunk(int hf, int c) {
+        return c < Q / 8 ? hf * (Q / 8) + c : DP / 16 + hf * (Q / 8) + (c - Q / 8);
+    }
+};
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -396,12 +459,13 @@ __device__ __forceinline__ void sts128(uint32_t a, const uint4& v) {
 }
 
 // Work items: (slice, chunk of `chunk` tokens); a warp walks its items'
-// 32-token tiles in order.  Two copies of the walk run one pipeline depth
+// tiles of ROWS tokens in order.  Two copies of the walk run one pipeline depth
 // apart (the one that prefetches and the one that computes).
-struct TileWalk {
+template <int ROWS>
+struct TileWalkT {
     int64_t item, items, step, slice;
     int nchunks, chunk, tokens, t_begin, t_end, t0;
-    __device__ TileWalk(int64_t first, int64_t step_, int64_t slices, int tokens_, int chunk_)
+    __device__ TileWalkT(int64_t first, int64_t step_, int64_t slices, int tokens_, int chunk_)
         : items(0), step(step_), slice(0), chunk(chunk_), tokens(tokens_), t_begin(0), t_end(0), t0(0) {
         nchunks = (tokens_ + chunk_ - 1) / chunk_;
         items = slices * nchunks;
@@ -418,10 +482,11 @@ struct TileWalk {
     }
     __device__ __forceinline__ bool valid() const { return item < items; }
     __device__ __forceinline__ void next() {
-        t0 += kTileRows;
+        t0 += ROWS;
         if (t0 >= t_end) set(item + step);
     }
 };
+using TileWalk = TileWalkT<kTileRows>;
 
 // ----------------------------------------------------------- row records
 

@@ -38,8 +38,8 @@ int grid_capacity(const void* kernel, int smem);
 bool ensure_smem(const void* kernel, int smem);
 
 // TMA map of an fp16 [slices][tokens][head_dim] tensor as 3-D tiles of
-// 64 columns x 32 tokens x 1 slice, 128-byte swizzle.  false on failure.
-bool make_row_tile_map(CUtensorMap* map, void* base, int head_dim, int tokens, int64_t slices);
+// 64 columns x box_rows tokens x 1 slice, 128-byte swizzle.  false on failure.
+bool make_row_tile_map(CUtensorMap* map, void* base, int head_dim, int tokens, int64_t slices, int box_rows);
 
 int launch_compress_tensor(const LaunchArgs& a, int head_dim, int bits, bool strict, const void* x,
                            const float* rope, uint8_t* idx, uint16_t* coset, uint16_t* scales);

@@ -60,6 +60,13 @@ def _gpu_sections(nq, buf, shape, params):
     return out
 
 
+def _same_values(gpu_bits, ref_bits):
+    """Equal fp16 values (the sign of a zero may differ: the two-thread
+    decompression produces some coordinates as the negation of a difference,
+    which turns the oracle's -0 / +0 into the other zero)."""
+    return np.array_equal(gpu_bits.view(np.float16), ref_bits.view(np.float16))
+
+
 def _assert_recon(gpu_bits, ref_bits):
     g = gpu_bits.view(np.float16).astype(np.float64)
     r = ref_bits.view(np.float16).astype(np.float64)
@@ -91,7 +98,7 @@ def _round_trip_check(nq, orc, K, V, params, expect_exact_recon=True):
         gb = _bits(g).reshape(r.shape)
         _assert_recon(gb, r)
         if expect_exact_recon:
-            assert np.array_equal(gb, r)
+            assert _same_values(gb, r)
     return buf
 
 
@@ -287,6 +294,6 @@ def test_full_size_sampled_parity(nq, orc, name):
                 idx, cw, sc = orc.encode_row(xr[n], D, bits, params.group_size, int(params.strict), csr)
                 ref[n] = orc.decode_row(idx, cw, sc, D, bits, params.group_size, csr)
             _assert_recon(xr2, ref)
-            assert np.array_equal(xr2, ref)
+            assert _same_values(xr2, ref)
         del buf, K2, V2
         torch.cuda.empty_cache()
