@@ -66,15 +66,17 @@ void make_layout(const nq_shape* s, const nq_params* p, nq_layout* L) {
 
 }  // namespace
 
-int grid_capacity(const void* kernel, int smem) {
+int grid_capacity_threads(const void* kernel, int smem, int threads) {
     int dev = 0, sms = 0, per_sm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, size_t(smem)) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, size_t(smem)) != cudaSuccess)
         return -1;
     if (per_sm <= 0) return -1;  // the kernel cannot be resident at all
     return sms * per_sm;
 }
+
+int grid_capacity(const void* kernel, int smem) { return grid_capacity_threads(kernel, smem, kThreads); }
 
 bool ensure_smem(const void* kernel, int smem) {
     // (kernel, device) pairs already configured; the attribute is per device

@@ -227,11 +227,11 @@ constexpr int kPairCompressSmem = kWarpsPerBlock * kPairStages * kPairTileBytes;
 // every record row, padding included, is written; rows at or past `tokens`
 // are zero-filled.
 template <int D>
-__device__ __forceinline__ void load_pair_tile(const __half* __restrict__ x, const TileWalkT<kPairRows>& w,
-                                               int tokens, uint32_t stage, int lane) {
+__device__ __forceinline__ void load_pair_tile(const __half* __restrict__ x, int64_t slice, int t0, int tokens,
+                                               uint32_t stage, int lane) {
     constexpr int CPR = D / 8;  // 16-byte chunks per row
-    const int nvalid = min(kPairRows, tokens - w.t0);
-    const __half* base = x + (w.slice * tokens + min(w.t0, tokens - 1)) * int64_t(D);
+    const int nvalid = min(kPairRows, tokens - t0);
+    const __half* base = x + (slice * tokens + min(t0, tokens - 1)) * int64_t(D);
 #pragma unroll
     for (int i = 0; i < CPR / 2; ++i) {  // 16 rows * CPR chunks / 32 lanes
         const int g = lane + 32 * i;
@@ -257,11 +257,17 @@ __device__ __forceinline__ void store_words(uint8_t* dst, const unsigned* w) {
     }
 }
 
+// The per-row work after the RoPE removal, shared by both two-thread
+// kernels: Hadamard rotation (compression order), group scale, E8 search,
+// temporal delta, and the store of record row rrow.  y: the thread's
+// coordinates in PairMap slots.  t: token index of the row; first: the tile
+// starts a delta chunk at t_begin.
 template <int D, int BITS, bool STRICT>
-__global__ void __launch_bounds__(kThreads, 2)
-    compress_pair_kernel(const __half* __restrict__ x, const float4* __restrict__ rope, int64_t slices,
-                         int tokens, int tpad, int group, int chunk, bool delta, uint8_t* __restrict__ idx,
-                         uint16_t* __restrict__ coset, __half* __restrict__ scales) {
+__device__ __forceinline__ void pair_encode_row(float (&y)[D / 2], int hf, int r, float sgn, int t, bool active,
+                                                bool delta, bool first, int t_begin, int64_t rrow, int group,
+                                                unsigned (&carry)[D / 16], unsigned& carry_c,
+                                                uint8_t* __restrict__ idx, uint16_t* __restrict__ coset,
+                                                __half* __restrict__ scales) {
     constexpr int DP = D;
     using PM = PairMap<DP>;
     constexpr int HALF = PM::HALF;
@@ -273,6 +279,111 @@ __global__ void __launch_bounds__(kThreads, 2)
     constexpr int RB = DP * BITS / 8;  // idx bytes per row
     constexpr int RBT = RB / 2;        // idx bytes per thread
     constexpr float STEP = float(DP) * C::H;
+    const int nsc = DP / group;
+    const int span = group / 32;  // 32-coordinate subgroups per scale group
+
+    // ---- Hadamard rotation, compression order: bits below DP/4 in-thread,
+    //      bit DP/2 in-thread (signed), bit DP/4 by exchange
+#pragma unroll
+    for (int h = 1; h < Q; h *= 2) fwht_stage<HALF>(y, h);
+    stage_signed<HALF>(y, sgn);
+    stage_exchange<HALF>(y);
+
+    // ---- group absmax -> fp16 scale -> reciprocal (per 32-subgroup)
+    float amax[NSUB];
+#pragma unroll
+    for (int s = 0; s < NSUB; ++s) {
+        float m = 0.0f;
+#pragma unroll
+        for (int j = 32 * s; j < 32 * s + 32; j += 2) m = fmax3(m, fabsf(y[j]), fabsf(y[j + 1]));
+        amax[s] = m;
+    }
+    if (NSUB == 2 && span >= 2) amax[0] = amax[1] = fmaxf(amax[0], amax[1]);
+    if (span > NSUB) {
+        const float o = __shfl_xor_sync(kFull, amax[0], 1);
+#pragma unroll
+        for (int s = 0; s < NSUB; ++s) amax[s] = fmaxf(amax[s], o);
+    }
+    unsigned short sc[NSUB];
+    float inv[NSUB];
+    bool fast = true;
+#pragma unroll
+    for (int s = 0; s < NSUB; ++s) {
+        sc[s] = group_scale(amax[s], STEP);
+        const float scf = __half2float(__ushort_as_half(sc[s]));
+        inv[s] = sc[s] ? __frcp_rn(__fmul_rn(scf, float(DP))) : 0.0f;
+        fast = fast && (__fmul_rn(amax[s], inv[s]) < C::H);
+    }
+
+    // ---- E8 nearest point per 8-block -> block codes
+    unsigned blk[NBT];
+    unsigned cwl = 0;
+#pragma unroll
+    for (int k = 0; k < NBT; ++k) {
+        // slots at or above Q hold the odd thread's negated coordinates
+        const float ik = (8 * k >= Q) ? __fmul_rn(inv[(8 * k) / 32], sgn) : inv[(8 * k) / 32];
+        float u[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) u[j] = __fmul_rn(y[8 * k + j], ik);
+        unsigned c;
+        if (!(fast && e8_fast<BITS, STRICT>(u, blk[k], c))) {
+            const uint2 res = e8_slow<BITS, STRICT>(make_float4(u[0], u[1], u[2], u[3]),
+                                                    make_float4(u[4], u[5], u[6], u[7]));
+            blk[k] = res.x;
+            c = res.y;
+        }
+        cwl |= c << k;
+    }
+    unsigned cw = cwl << (hf * NBT);
+    cw |= __shfl_xor_sync(kFull, cw, 1);
+
+    // ---- temporal delta against the previous token (row r - 1: lane - 2)
+    if (delta) {
+        
+#pragma unroll
+        for (int k = 0; k < NBT; ++k) {
+            unsigned prev = __shfl_up_sync(kFull, blk[k], 2);
+            const unsigned last = __shfl_sync(kFull, blk[k], 30 + hf);
+            if (r == 0) prev = first ? 0u : carry[k];
+            if (t != t_begin) blk[k] = swar_sub<BITS>(blk[k], prev);
+            carry[k] = last;  // raw codes of the tile's last token
+        }
+        unsigned pc = __shfl_up_sync(kFull, cw, 2);
+        const unsigned lastc = __shfl_sync(kFull, cw, 30);
+        if (r == 0) pc = first ? 0u : carry_c;
+        if (t != t_begin) cw ^= pc;
+        carry_c = lastc;
+    }
+
+    // ---- store (padding rows past the slice get zeros)
+    if (!active) {
+#pragma unroll
+        for (int k = 0; k < NBT; ++k) blk[k] = 0;
+        cw = 0;
+#pragma unroll
+        for (int s = 0; s < NSUB; ++s) sc[s] = 0;
+    }
+            unsigned w[RP::WORDS];
+    RP::pack(blk, w);
+    store_words<RBT>(idx + rrow * RB + hf * RBT, w);
+    if (hf == 0) coset[rrow] = uint16_t(cw);
+#pragma unroll
+    for (int s = 0; s < NSUB; ++s) {
+        const int gs = hf * NSUB + s;  // global 32-subgroup
+        if (gs % span == 0) scales[rrow * nsc + gs / span] = __ushort_as_half(sc[s]);
+    }
+}
+
+template <int D, int BITS, bool STRICT>
+__global__ void __launch_bounds__(kThreads, 2)
+    compress_pair_kernel(const __half* __restrict__ x, const float4* __restrict__ rope, int64_t slices,
+                         int tokens, int tpad, int group, int chunk, bool delta, uint8_t* __restrict__ idx,
+                         uint16_t* __restrict__ coset, __half* __restrict__ scales) {
+    constexpr int DP = D;
+    using PM = PairMap<DP>;
+    constexpr int HALF = PM::HALF;
+    constexpr int Q = PM::Q;
+    constexpr int NBT = PM::NBT;
     using Walk = TileWalkT<kPairRows>;
 
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -283,15 +394,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t ring = smem_u32(smem) + (threadIdx.x >> 5) * (kPairStages * kPairTileBytes);
     const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
-    const int nsc = DP / group;
-    const int span = group / 32;  // 32-coordinate subgroups per scale group
 
     Walk cur(warp, nwarps, slices, tpad, chunk);
     Walk pre = cur;
 #pragma unroll
     for (int s = 0; s < kPairStages - 1; ++s) {
         if (pre.valid()) {
-            load_pair_tile<D>(x, pre, tokens, ring + s * kPairTileBytes, lane);
+            load_pair_tile<D>(x, pre.slice, pre.t0, tokens, ring + s * kPairTileBytes, lane);
             pre.next();
         }
         cp_async_commit();
@@ -304,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     for (int i = 0; cur.valid(); ++i) {
         if (pre.valid()) {
-            load_pair_tile<D>(x, pre, tokens, ring + ((i + kPairStages - 1) % kPairStages) * kPairTileBytes, lane);
+            load_pair_tile<D>(x, pre.slice, pre.t0, tokens, ring + ((i + kPairStages - 1) % kPairStages) * kPairTileBytes, lane);
             pre.next();
         }
         cp_async_commit();
@@ -337,96 +446,123 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
         }
 
-        // ---- Hadamard rotation, compression order: bits below DP/4 in-thread,
-        //      bit DP/2 in-thread (signed), bit DP/4 by exchange
-#pragma unroll
-        for (int h = 1; h < Q; h *= 2) fwht_stage<HALF>(y, h);
-        stage_signed<HALF>(y, sgn);
-        stage_exchange<HALF>(y);
+        pair_encode_row<D, BITS, STRICT>(y, hf, r, sgn, t, active, delta, cur.t0 == cur.t_begin, cur.t_begin,
+                                         cur.slice * tpad + t, group, carry, carry_c, idx, coset, scales);
+        cur.next();
+    }
+    cp_async_wait<0>();
+}
 
-        // ---- group absmax -> fp16 scale -> reciprocal (per 32-subgroup)
-        float amax[NSUB];
-#pragma unroll
-        for (int s = 0; s < NSUB; ++s) {
-            float m = 0.0f;
-#pragma unroll
-            for (int j = 32 * s; j < 32 * s + 32; j += 2) m = fmax3(m, fabsf(y[j]), fabsf(y[j + 1]));
-            amax[s] = m;
-        }
-        if (NSUB == 2 && span >= 2) amax[0] = amax[1] = fmaxf(amax[0], amax[1]);
-        if (span > NSUB) {
-            const float o = __shfl_xor_sync(kFull, amax[0], 1);
-#pragma unroll
-            for (int s = 0; s < NSUB; ++s) amax[s] = fmaxf(amax[s], o);
-        }
-        unsigned short sc[NSUB];
-        float inv[NSUB];
-        bool fast = true;
-#pragma unroll
-        for (int s = 0; s < NSUB; ++s) {
-            sc[s] = group_scale(amax[s], STEP);
-            const float scf = __half2float(__ushort_as_half(sc[s]));
-            inv[s] = sc[s] ? __frcp_rn(__fmul_rn(scf, float(DP))) : 0.0f;
-            fast = fast && (__fmul_rn(amax[s], inv[s]) < C::H);
-        }
+// ------------------------------------ keys: the RoPE table shared by a block
+//
+// A block of 16 warps compresses the same 16-token tile of 16 consecutive
+// slices (warp w: slice 16*g + w).  The tile's RoPE table rows (head_dim/4
+// planes x 16 tokens x 16 bytes) are staged once per block, next to the 16
+// warps' fp16 tiles, in a 3-stage ring filled by cp.async; one block barrier
+// per tile orders the refills.  Each key row then reads 512 bytes of table
+// from shared memory instead of L2.
+constexpr int kRopeWarps = 16;
+constexpr int kRopeThreads = kRopeWarps * 32;
+constexpr int kRopeStages = 3;
+template <int D>
+struct RopeStage {
+    static constexpr int TABLE = D * 4 * kPairRows;  // head_dim/4 planes x 16 tokens x 16 B
+    static constexpr int BYTES = TABLE + kRopeWarps * kPairTileBytes;
+    static constexpr int SMEM = kRopeStages * BYTES + 1024;
+};
 
-        // ---- E8 nearest point per 8-block -> block codes
-        unsigned blk[NBT];
-        unsigned cwl = 0;
+// table position of (plane q, tile row rr): the odd thread's planes (q >= D/8)
+// are shifted by 4 rows so the two threads of a row hit different banks
+template <int D>
+__device__ __forceinline__ uint32_t rope_slot(int q, int rr) {
+    return uint32_t((q * kPairRows + (rr ^ (q >= D / 8 ? 4 : 0))) * 16);
+}
+
+template <int D, int BITS, bool STRICT>
+__global__ void __launch_bounds__(kRopeThreads, 1)
+    compress_pair_rope_kernel(const __half* __restrict__ x, const float4* __restrict__ rope, int64_t slices,
+                              int tokens, int tpad, int group, int chunk, bool delta, uint8_t* __restrict__ idx,
+                              uint16_t* __restrict__ coset, __half* __restrict__ scales) {
+    constexpr int DP = D;
+    using PM = PairMap<DP>;
+    constexpr int HALF = PM::HALF;
+    constexpr int Q = PM::Q;
+    constexpr int NBT = PM::NBT;
+    using RS = RopeStage<D>;
+    using Walk = TileWalkT<kPairRows>;
+
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const uint32_t sbase = (smem_u32(smem) + 1023u) & ~1023u;
+    const int wib = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int hf = lane & 1;
+    const int r = lane >> 1;
+    const float sgn = hf ? -1.0f : 1.0f;
+    const int64_t ngroups = (slices + kRopeWarps - 1) / kRopeWarps;
+
+    // the walk runs over slice groups; the warp's slice is 16 * group + wib
+    Walk cur(blockIdx.x, gridDim.x, ngroups, tpad, chunk);
+    Walk pre = cur;
+
+    auto load_stage = [&](const Walk& w, uint32_t stage) {
+        for (int g = threadIdx.x; g < (D / 4) * kPairRows; g += kRopeThreads) {
+            const int q = g / kPairRows, rr = g - q * kPairRows;
+            const int tok = w.t0 + rr;
+            const bool ok = tok < tokens;
+            cp_async16(stage + rope_slot<D>(q, rr), rope + int64_t(q) * tokens + (ok ? tok : 0), ok ? 16 : 0);
+        }
+        const int64_t sl = w.slice * kRopeWarps + wib;
+        if (sl < slices) load_pair_tile<D>(x, sl, w.t0, tokens, stage + RS::TABLE + wib * kPairTileBytes, lane);
+    };
+
 #pragma unroll
-        for (int k = 0; k < NBT; ++k) {
-            // slots at or above Q hold the odd thread's negated coordinates
-            const float ik = (8 * k >= Q) ? __fmul_rn(inv[(8 * k) / 32], sgn) : inv[(8 * k) / 32];
-            float u[8];
+    for (int s = 0; s < kRopeStages - 1; ++s) {
+        if (pre.valid()) {
+            load_stage(pre, sbase + s * RS::BYTES);
+            pre.next();
+        }
+        cp_async_commit();
+    }
+
+    unsigned carry[NBT];
+    unsigned carry_c = 0;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) u[j] = __fmul_rn(y[8 * k + j], ik);
-            unsigned c;
-            if (!(fast && e8_fast<BITS, STRICT>(u, blk[k], c))) {
-                const uint2 res = e8_slow<BITS, STRICT>(make_float4(u[0], u[1], u[2], u[3]),
-                                                        make_float4(u[4], u[5], u[6], u[7]));
-                blk[k] = res.x;
-                c = res.y;
+    for (int k = 0; k < NBT; ++k) carry[k] = 0;
+
+    for (int i = 0; cur.valid(); ++i) {
+        cp_async_wait<kRopeStages - 2>();  // this thread's copies of tile i are done
+        __syncthreads();                    // everyone's are; everyone is done with tile i - 1
+        if (pre.valid()) {
+            load_stage(pre, sbase + ((i + kRopeStages - 1) % kRopeStages) * RS::BYTES);
+            pre.next();
+        }
+        cp_async_commit();
+        const uint32_t stage = sbase + (i % kRopeStages) * RS::BYTES;
+        const int64_t slice = cur.slice * kRopeWarps + wib;
+        if (slice < slices) {  // warp-uniform
+            const int t = cur.t0 + r;
+            const bool active = t < tokens;
+            float y[HALF];
+            const uint32_t tile = stage + RS::TABLE + wib * kPairTileBytes;
+#pragma unroll
+            for (int c = 0; c < NBT; ++c) h8_to_f(lds128(tile + swz16(r, PM::chunk(hf, c))), &y[8 * c]);
+            // RoPE removal with the block's table tile: pairs (i, i + D/2) are slots (l, l + Q)
+#pragma unroll
+            for (int qq = 0; qq < Q / 2; ++qq) {
+                const uint4 raw = lds128(stage + rope_slot<D>(hf * (Q / 2) + qq, r));
+                const float4 v = make_float4(__uint_as_float(raw.x), __uint_as_float(raw.y), __uint_as_float(raw.z),
+                                             __uint_as_float(raw.w));
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    const int l = 2 * qq + p;
+                    const float c = p ? v.z : v.x, sn = p ? v.w : v.y;
+                    const float a = y[l], b = y[l + Q];
+                    y[l] = __fmaf_rn(a, c, __fmul_rn(b, sn));
+                    y[l + Q] = __fmaf_rn(b, c, -__fmul_rn(a, sn));
+                }
             }
-            cwl |= c << k;
-        }
-        unsigned cw = cwl << (hf * NBT);
-        cw |= __shfl_xor_sync(kFull, cw, 1);
-
-        // ---- temporal delta against the previous token (row r - 1: lane - 2)
-        if (delta) {
-            const bool first = cur.t0 == cur.t_begin;
-#pragma unroll
-            for (int k = 0; k < NBT; ++k) {
-                unsigned prev = __shfl_up_sync(kFull, blk[k], 2);
-                const unsigned last = __shfl_sync(kFull, blk[k], 30 + hf);
-                if (r == 0) prev = first ? 0u : carry[k];
-                if (t != cur.t_begin) blk[k] = swar_sub<BITS>(blk[k], prev);
-                carry[k] = last;  // raw codes of the tile's last token
-            }
-            unsigned pc = __shfl_up_sync(kFull, cw, 2);
-            const unsigned lastc = __shfl_sync(kFull, cw, 30);
-            if (r == 0) pc = first ? 0u : carry_c;
-            if (t != cur.t_begin) cw ^= pc;
-            carry_c = lastc;
-        }
-
-        // ---- store (padding rows past the slice get zeros)
-        if (!active) {
-#pragma unroll
-            for (int k = 0; k < NBT; ++k) blk[k] = 0;
-            cw = 0;
-#pragma unroll
-            for (int s = 0; s < NSUB; ++s) sc[s] = 0;
-        }
-        const int64_t rrow = cur.slice * tpad + t;
-        unsigned w[RP::WORDS];
-        RP::pack(blk, w);
-        store_words<RBT>(idx + rrow * RB + hf * RBT, w);
-        if (hf == 0) coset[rrow] = uint16_t(cw);
-#pragma unroll
-        for (int s = 0; s < NSUB; ++s) {
-            const int gs = hf * NSUB + s;  // global 32-subgroup
-            if (gs % span == 0) scales[rrow * nsc + gs / span] = __ushort_as_half(sc[s]);
+            pair_encode_row<D, BITS, STRICT>(y, hf, r, sgn, t, active, delta, cur.t0 == cur.t_begin, cur.t_begin,
+                                             slice * tpad + t, group, carry, carry_c, idx, coset, scales);
         }
         cur.next();
     }
@@ -467,6 +603,31 @@ static int launch_pair(const LaunchArgs& a, const __half* x, const float4* rope,
     return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
 }
 
+template <int D, int BITS, bool STRICT>
+static int launch_pair_rope(const LaunchArgs& a, const __half* x, const float4* rope, uint8_t* idx,
+                            uint16_t* coset, __half* scales) {
+    auto kern = compress_pair_rope_kernel<D, BITS, STRICT>;
+    constexpr int smem = RopeStage<D>::SMEM;
+    if (!ensure_smem(reinterpret_cast<const void*>(kern), smem)) return NQ_ERR_CUDA;
+    const int chunk = a.delta_chunk > 0 ? a.delta_chunk : kPairRows;
+    const int64_t groups = (a.slices + kRopeWarps - 1) / kRopeWarps;
+    const int64_t items = groups * ((a.tpad + chunk - 1) / chunk);
+    if (items == 0) return NQ_OK;
+    const int cap = grid_capacity_threads(reinterpret_cast<const void*>(kern), smem, kRopeThreads);
+    if (cap <= 0) return NQ_ERR_CUDA;
+    const int grid = int(std::min<int64_t>(items, cap));
+    kern<<<grid, kRopeThreads, smem, a.stream>>>(x, rope, a.slices, a.tokens, a.tpad, a.group, chunk,
+                                                 a.delta_chunk > 0, idx, coset, scales);
+    return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
+}
+
+template <int D, int BITS, bool STRICT>
+static int launch_pair_any(const LaunchArgs& a, const __half* x, const float4* rope, uint8_t* idx,
+                           uint16_t* coset, __half* scales) {
+    return rope ? launch_pair_rope<D, BITS, STRICT>(a, x, rope, idx, coset, scales)
+                : launch_pair<D, BITS, STRICT>(a, x, rope, idx, coset, scales);
+}
+
 template <int D>
 static int dispatch_bits(const LaunchArgs& a, int bits, bool strict, const __half* x,
                          const float4* rope, uint8_t* idx, uint16_t* coset, __half* scales) {
@@ -476,8 +637,8 @@ static int dispatch_bits(const LaunchArgs& a, int bits, bool strict, const __hal
             return strict ? launch<D, B, true>(a, x, rope, idx, coset, scales)                  \
                           : launch<D, B, false>(a, x, rope, idx, coset, scales);                \
         else                                                                                    \
-            return strict ? launch_pair<D, B, true>(a, x, rope, idx, coset, scales)             \
-                          : launch_pair<D, B, false>(a, x, rope, idx, coset, scales);
+            return strict ? launch_pair_any<D, B, true>(a, x, rope, idx, coset, scales)         \
+                          : launch_pair_any<D, B, false>(a, x, rope, idx, coset, scales);
     switch (bits) {
         NQ_CASE(2)
         NQ_CASE(3)

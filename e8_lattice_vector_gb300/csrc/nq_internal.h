@@ -32,6 +32,7 @@ struct LaunchArgs {
 // Blocks of kThreads that fit on the current device at once for `kernel` with
 // `smem` bytes of dynamic shared memory; -1 when it cannot be queried.
 int grid_capacity(const void* kernel, int smem);
+int grid_capacity_threads(const void* kernel, int smem, int threads);
 
 // Allow `kernel` `smem` bytes of dynamic shared memory on the current device
 // (once per device); false on a CUDA error.
