@@ -248,11 +248,10 @@ __device__ __forceinline__ int e8_general(const float (&u)[8], bool strict, floa
 //   min(|e~0|, hi0 - |u|) (a step that would leave the box turns around).
 // The codes are accumulated as exact integer-valued floats on the FMA pipe
 // (sum of r_j * L^j over half-blocks of 4 coordinates, < 2^16), the parities
-// by xor of the magic-rounded bit patterns, and the fix-up coordinate (first
-// maximal score) by an equality mask.  A block whose chosen coset needs a
-// fix-up with a maximal score <= 0 (every coordinate an exact integer or past
-// the box edge) is not handled here: the function returns false and the
-// caller runs the general path.
+// by xor of the magic-rounded bit patterns.  A block whose chosen coset needs
+// a fix-up with a tie for the maximal score or a maximal score <= 0 (every
+// coordinate an exact integer or past the box edge) is not handled here: the
+// function returns false and the caller runs the general path.
 template <int BITS, bool STRICT>
 __device__ __forceinline__ bool e8_fast(const float (&u)[8], unsigned& code, unsigned& coset) {
     using C = Code<BITS>;
@@ -260,7 +259,7 @@ __device__ __forceinline__ bool e8_fast(const float (&u)[8], unsigned& code, uns
     constexpr float Lp[4] = {1.0f, L, L * L, L * L * L};
     constexpr float SUML = 1.0f + L + L * L + L * L * L;
     constexpr float TWO23 = 8388608.0f;
-    float eb1[8], s0[8];
+    float eb1[8], s0[8], csv[8];
     float d0 = 0.0f, d1 = 0.0f;
     float A[2] = {0.0f, 0.0f}, Bq[2] = {0.0f, 0.0f};
     unsigned x0 = 0, xs = 0;
@@ -271,6 +270,7 @@ __device__ __forceinline__ bool e8_fast(const float (&u)[8], unsigned& code, uns
         const float e0 = __fsub_rn(r0, u[j]);
         const float cs = copysignf(0.5f, e0);
         const float e1 = __fsub_rn(e0, cs);
+        csv[j] = cs;
         eb1[j] = e1;
         d0 = __fmaf_rn(e0, e0, d0);
         d1 = __fmaf_rn(e1, e1, d1);
@@ -291,36 +291,46 @@ __device__ __forceinline__ bool e8_fast(const float (&u)[8], unsigned& code, uns
     const float dd1 = odd1 ? __fadd_rn(d1, __fmaf_rn(-2.0f, smax1, 1.0f)) : d1;
     const bool half = dd1 < dd0;
 
-    // integer codes m0 = r0 + (L/2 - 1), half-integer codes m1 = r1 + (L - 1)/2
-    unsigned c0 = 0, c1 = 0;
+    // fix-up of the chosen coset: move its first maximal-score coordinate k one
+    // step toward u, i.e. add -2*cs_k*L^k to the integer code (u above rint(u)
+    // moves up) or +2*cs_k*L^k to the half-integer code.  k is found on the FMA
+    // pipe: f_j = sat((smax - s_j) * 2^127) is 0 at a maximum and 1 elsewhere
+    // (distinct scores differ by far more than 2^-127), and
+    // G = sum_j (1 - f_j) cs_j L^j picks cs_k L^k.  Ties (sum f != 7) and a
+    // non-positive maximum go to the general path.
+    float g[2] = {0.0f, 0.0f};
+    const bool fix = half ? odd1 : odd0;
+    if (fix) {
+        const float smax = half ? smax1 : smax0;
+        if (!(smax > 0.0f)) return false;
+        float cnt = 0.0f;
+        float G[2] = {0.0f, 0.0f};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float sj = (STRICT && half) ? fabsf(eb1[j]) : s0[j];
+            float f;
+            asm("mul.rn.sat.f32 %0, %1, 0f7F000000;" : "=f"(f) : "f"(__fsub_rn(smax, sj)));
+            cnt = __fadd_rn(cnt, f);
+            const float v = __fmaf_rn(-f, csv[j], csv[j]);  // cs_j at the maximum, else 0
+            G[j >> 2] = __fmaf_rn(v, Lp[j & 3], G[j >> 2]);
+        }
+        if (cnt != 7.0f) return false;
+        const float m = half ? 2.0f : -2.0f;
+        g[0] = __fmul_rn(m, G[0]);
+        g[1] = __fmul_rn(m, G[1]);
+    }
+
+    // integer codes m0 = r0 + (L/2 - 1), half-integer codes m1 = r1 + (L - 1)/2,
+    // per half-block an exact integer below 2^16 read off the float's low bits
+    unsigned c = 0;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         // every intermediate is an integer below 2^24 (Bq and (L-1)/2 * SUML are
         // both odd multiples of 1/2), so all of this is exact
         const float ap = __fadd_rn(A[h], TWO23);
-        const float f0 = __fadd_rn(ap, float(C::OFF0) * SUML);
-        const float f1 = __fsub_rn(ap, __fsub_rn(Bq[h], C::H * SUML));
-        c0 |= (__float_as_uint(f0) & 0xffffu) << (4 * BITS * h);
-        c1 |= (__float_as_uint(f1) & 0xffffu) << (4 * BITS * h);
-    }
-    unsigned c = half ? c1 : c0;
-    const bool fix = half ? odd1 : odd0;
-    if (fix) {
-        const float smax = half ? smax1 : smax0;
-        if (!(smax > 0.0f)) return false;
-        unsigned eq = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float sj = (STRICT && half) ? fabsf(eb1[j]) : s0[j];
-            eq |= (sj == smax ? 1u : 0u) << j;
-        }
-        const int k = __ffs(eq) - 1;
-        // field k of c1 - c0 is 1 when e~0_k < 0 (u above the rounded integer)
-        const unsigned neg = ((c1 - c0) >> (k * BITS)) & 1u;
-        // toward u: integer coset +1 when u is above r0; half coset +1 when
-        // u is above r1, i.e. when e~0_k >= 0
-        const bool up = (neg != 0) != half;
-        c = up ? c + (1u << (k * BITS)) : c - (1u << (k * BITS));
+        const float f0 = __fadd_rn(__fadd_rn(ap, float(C::OFF0) * SUML), g[h]);
+        const float f1 = __fadd_rn(__fsub_rn(ap, __fsub_rn(Bq[h], C::H * SUML)), g[h]);
+        c |= (__float_as_uint(half ? f1 : f0) & 0xffffu) << (4 * BITS * h);
     }
     code = c;
     coset = half ? 1u : 0u;

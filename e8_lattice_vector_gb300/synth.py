@@ -92,10 +92,12 @@ def _model_rope(k, theta, tokens):
     return k * cos + rot * sin
 
 
-def layer_kv(cfg, layer, device="cuda", tokens=None):
-    """fp16 K, V of one layer: [batch, kv_heads, tokens, head_dim]."""
+def layer_kv(cfg, layer, device="cuda", tokens=None, batch=None):
+    """fp16 K, V of one layer: [batch, kv_heads, tokens, head_dim] (`batch` and
+    `tokens` restrict the draw to a smaller sample of the same distribution)."""
     T = cfg.tokens if tokens is None else tokens
-    B, H, D = cfg.batch, cfg.kv_heads, cfg.head_dim
+    B = cfg.batch if batch is None else batch
+    H, D = cfg.kv_heads, cfg.head_dim
     g = _gen(device, cfg.seed * 1000 + layer)
     z = torch.randn((B, H, T, D), generator=g, device=device, dtype=torch.float32)
     scale = torch.exp(cfg.sigma * torch.randn((H, 1, D), generator=g, device=device))
