@@ -19,6 +19,26 @@ constexpr int kStages = 3;
 constexpr int kCompressSmem = kWarpsPerBlock * kStages * kTileBytes;
 
 // Copy the fp16 rows of a tile into a stage; rows past the chunk are zeros.
+// Scaled coordinates u = y * inv of 8-block k of a one-thread row.
+template <int N>
+__device__ __forceinline__ void row_block_u(const float (&y)[N], float inv, int k, float (&u)[8]) {
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+        const float2 p = __fmul2_rn(make_float2(y[8 * k + j], y[8 * k + j + 1]), make_float2(inv, inv));
+        u[j] = p.x;
+        u[j + 1] = p.y;
+    }
+}
+
+// The same for a two-thread row: slots at or above Q hold the odd thread's
+// negated coordinates, so their reciprocal scale carries the thread's sign.
+template <int Q, int N, int NS>
+__device__ __forceinline__ void pair_block_u(const float (&y)[N], const float (&inv)[NS], float sgn, int k,
+                                             float (&u)[8]) {
+    const float ik = (8 * k >= Q) ? __fmul_rn(inv[(8 * k) / 32], sgn) : inv[(8 * k) / 32];
+    row_block_u(y, ik, k, u);
+}
+
 template <int D>
 __device__ __forceinline__ void load_tile(const __half* __restrict__ x, const TileWalk& w, uint32_t stage,
                                           int lane) {
@@ -144,20 +164,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // ---- E8 nearest point per 8-block -> block codes
         unsigned blk[NB];
-        unsigned cw = 0;
+        unsigned cw = 0, declined = 0;
 #pragma unroll
         for (int k = 0; k < NB; ++k) {
             float u[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) u[j] = __fmul_rn(y[8 * k + j], inv[k / 4]);
+            row_block_u(y, inv[k / 4], k, u);
             unsigned c;
-            if (!(fast && e8_fast<BITS, STRICT>(u, blk[k], c))) {
+            const bool ok = e8_fast<BITS, STRICT>(u, blk[k], c);
+            cw |= c << k;
+            declined |= unsigned(!ok) << k;
+        }
+        if (!fast) declined = (1u << NB) - 1u;
+        if (declined) {
+#pragma unroll
+            for (int k = 0; k < NB; ++k) {
+                if (!((declined >> k) & 1u)) continue;
+                float u[8];
+                row_block_u(y, inv[k / 4], k, u);
                 const uint2 res = e8_slow<BITS, STRICT>(make_float4(u[0], u[1], u[2], u[3]),
                                                         make_float4(u[4], u[5], u[6], u[7]));
                 blk[k] = res.x;
-                c = res.y;
+                cw = (cw & ~(1u << k)) | (res.y << k);
             }
-            cw |= c << k;
         }
 
         // ---- temporal delta against the previous token of the chunk
@@ -316,23 +344,31 @@ __device__ __forceinline__ void pair_encode_row(float (&y)[D / 2], int hf, int r
     }
 
     // ---- E8 nearest point per 8-block -> block codes
+    // Fast path for every block without a branch, then the general path for
+    // the blocks it declined (rare), so consecutive blocks can overlap.
     unsigned blk[NBT];
-    unsigned cwl = 0;
+    unsigned cwl = 0, declined = 0;
 #pragma unroll
     for (int k = 0; k < NBT; ++k) {
-        // slots at or above Q hold the odd thread's negated coordinates
-        const float ik = (8 * k >= Q) ? __fmul_rn(inv[(8 * k) / 32], sgn) : inv[(8 * k) / 32];
         float u[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) u[j] = __fmul_rn(y[8 * k + j], ik);
+        pair_block_u<Q>(y, inv, sgn, k, u);
         unsigned c;
-        if (!(fast && e8_fast<BITS, STRICT>(u, blk[k], c))) {
+        const bool ok = e8_fast<BITS, STRICT>(u, blk[k], c);
+        cwl |= c << k;
+        declined |= unsigned(!ok) << k;
+    }
+    if (!fast) declined = (1u << NBT) - 1u;
+    if (declined) {
+#pragma unroll
+        for (int k = 0; k < NBT; ++k) {
+            if (!((declined >> k) & 1u)) continue;
+            float u[8];
+            pair_block_u<Q>(y, inv, sgn, k, u);
             const uint2 res = e8_slow<BITS, STRICT>(make_float4(u[0], u[1], u[2], u[3]),
                                                     make_float4(u[4], u[5], u[6], u[7]));
             blk[k] = res.x;
-            c = res.y;
+            cwl = (cwl & ~(1u << k)) | (res.y << k);
         }
-        cwl |= c << k;
     }
     unsigned cw = cwl << (hf * NBT);
     cw |= __shfl_xor_sync(kFull, cw, 1);

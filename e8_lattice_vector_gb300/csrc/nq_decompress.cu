@@ -45,6 +45,109 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
                  : "memory");
 }
 
+// One record row -> unscaled, inverse-transformed coordinates (before the
+// RoPE re-apply).  `stage` holds the 32-row record tile of the lane's warp.
+template <int D, int BITS>
+__device__ __forceinline__ void decode_row(uint32_t stage, const uint8_t* stage_gen, int lane, int nsc, int gshift,
+                                           bool delta, bool first, unsigned (&carry)[PaddedDim<D>::value / 8],
+                                           unsigned& carry_c, float (&y)[PaddedDim<D>::value]) {
+    constexpr int DP = PaddedDim<D>::value;
+    constexpr int NB = DP / 8;
+    using C = Code<BITS>;
+    using RP = RowPack<BITS, NB>;
+    constexpr int RB = DP * BITS / 8;
+
+    // ---- the lane's record
+    unsigned w[RP::WORDS];
+    if constexpr (RB % 16 == 0) {
+#pragma unroll
+        for (int q = 0; q < RB / 16; ++q) {
+            const uint4 v = lds128(stage + kRecIdx + lane * RB + 16 * q);
+            w[4 * q] = v.x;
+            w[4 * q + 1] = v.y;
+            w[4 * q + 2] = v.z;
+            w[4 * q + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < RB / 8; ++q) {
+            const uint2 v = lds64(stage + kRecIdx + lane * RB + 8 * q);
+            w[2 * q] = v.x;
+            w[2 * q + 1] = v.y;
+        }
+    }
+    const uint16_t* stage_h = reinterpret_cast<const uint16_t*>(stage_gen);
+    unsigned cw = stage_h[kRecCoset / 2 + lane];
+    float scf[DP / 32];
+#pragma unroll
+    for (int s = 0; s < DP / 32; ++s)
+        scf[s] = __half2float(__ushort_as_half(stage_h[kRecScale / 2 + lane * nsc + ((32 * s) >> gshift)]));
+    __syncwarp();  // the stage may be refilled
+    unsigned blk[NB];
+    RP::unpack(w, blk);
+
+    // ---- undo the temporal delta: inclusive scan over the tile + carry
+    if (delta) {
+#pragma unroll
+        for (int off = 1; off < 32; off *= 2) {
+#pragma unroll
+            for (int k = 0; k < NB; ++k) {
+                const unsigned v = __shfl_up_sync(kFull, blk[k], off);
+                if (lane >= off) blk[k] = swar_add<BITS>(blk[k], v);
+            }
+            const unsigned vc = __shfl_up_sync(kFull, cw, off);
+            if (lane >= off) cw ^= vc;
+        }
+#pragma unroll
+        for (int k = 0; k < NB; ++k) {
+            if (!first) blk[k] = swar_add<BITS>(blk[k], carry[k]);
+            carry[k] = __shfl_sync(kFull, blk[k], 31);
+        }
+        if (!first) cw ^= carry_c;
+        carry_c = __shfl_sync(kFull, cw, 31);
+    }
+
+    // ---- unpack, unscale: y = (code - offset) * scale  (exact)
+#pragma unroll
+    for (int k = 0; k < NB; ++k) unscale_block<BITS>(blk[k], (cw >> k) & 1u, scf[k / 4], &y[8 * k]);
+
+    // ---- inverse Hadamard: x = H (r * sc)
+    fwht<DP>(y);
+}
+
+// Rotate the pairs (2q, 2q + D/2) and (2q + 1, 2q + 1 + D/2) by +angle;
+// cs = (cos, sin) of both pairs.
+template <int D, int N>
+__device__ __forceinline__ void rope_apply_pairs(float (&y)[N], int q, float4 cs) {
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+        const int j = 2 * q + p;
+        const float c = p ? cs.z : cs.x, s = p ? cs.w : cs.y;
+        const float a = y[j], b = y[j + D / 2];
+        y[j] = __fmaf_rn(a, c, -__fmul_rn(b, s));
+        y[j + D / 2] = __fmaf_rn(b, c, __fmul_rn(a, s));
+    }
+}
+
+// fp16 rows -> swizzled shared-memory tile -> TMA tensor store of 32 rows
+// (the map clips rows past the slice end and columns past head_dim).  PENDING
+// = stores of the warp's other output tiles that may still be reading.
+template <int D, int PENDING, int N>
+__device__ __forceinline__ void store_rows(const float (&y)[N], uint32_t ob, int lane, const CUtensorMap* map,
+                                           int t0, int slice) {
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(PENDING) : "memory");  // ob is free
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < D / 8; ++q) sts128(ob + swz(lane, q), f_to_h8(&y[8 * q]));
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_3d(map, ob, 0, t0, slice);
+        if (D > 64) tma_store_3d(map, ob + 4096, 64, t0, slice);
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    }
+}
+
 template <int D, int BITS>
 __global__ void __launch_bounds__(kThreads, 1)
     decompress_kernel(const uint8_t* __restrict__ idx, const uint16_t* __restrict__ coset,
@@ -53,8 +156,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                       int group, int chunk, bool delta) {
     constexpr int DP = PaddedDim<D>::value;
     constexpr int NB = DP / 8;
-    using C = Code<BITS>;
-    using RP = RowPack<BITS, NB>;
     constexpr int RB = DP * BITS / 8;
 
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -95,103 +196,115 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t stage = ring + (i % kStages) * kRecStage;
         const int t = cur.t0 + lane;
 
-        // ---- the lane's record
-        unsigned w[RP::WORDS];
-        if constexpr (RB % 16 == 0) {
-#pragma unroll
-            for (int q = 0; q < RB / 16; ++q) {
-                const uint4 v = lds128(stage + kRecIdx + lane * RB + 16 * q);
-                w[4 * q] = v.x;
-                w[4 * q + 1] = v.y;
-                w[4 * q + 2] = v.z;
-                w[4 * q + 3] = v.w;
-            }
-        } else {
-#pragma unroll
-            for (int q = 0; q < RB / 8; ++q) {
-                const uint2 v = lds64(stage + kRecIdx + lane * RB + 8 * q);
-                w[2 * q] = v.x;
-                w[2 * q + 1] = v.y;
-            }
-        }
-        const uint16_t* stage_gen = reinterpret_cast<const uint16_t*>(smem + (stage - smem_u32(smem)));
-        unsigned cw = stage_gen[kRecCoset / 2 + lane];
-        float scf[DP / 32];
-#pragma unroll
-        for (int s = 0; s < DP / 32; ++s)
-            scf[s] = __half2float(__ushort_as_half(stage_gen[kRecScale / 2 + lane * nsc + ((32 * s) >> gshift)]));
-        __syncwarp();  // the stage may be refilled
-        unsigned blk[NB];
-        RP::unpack(w, blk);
-
-        // ---- undo the temporal delta: inclusive scan over the tile + carry
-        if (delta) {
-#pragma unroll
-            for (int off = 1; off < 32; off *= 2) {
-#pragma unroll
-                for (int k = 0; k < NB; ++k) {
-                    const unsigned v = __shfl_up_sync(kFull, blk[k], off);
-                    if (lane >= off) blk[k] = swar_add<BITS>(blk[k], v);
-                }
-                const unsigned vc = __shfl_up_sync(kFull, cw, off);
-                if (lane >= off) cw ^= vc;
-            }
-            const bool first = cur.t0 == cur.t_begin;
-#pragma unroll
-            for (int k = 0; k < NB; ++k) {
-                if (!first) blk[k] = swar_add<BITS>(blk[k], carry[k]);
-                carry[k] = __shfl_sync(kFull, blk[k], 31);
-            }
-            if (!first) cw ^= carry_c;
-            carry_c = __shfl_sync(kFull, cw, 31);
-        }
-
-        // ---- unpack, unscale: y = (code - offset) * scale  (exact)
+        const uint8_t* stage_gen = smem + (stage - smem_u32(smem));
         float y[DP];
-#pragma unroll
-        for (int k = 0; k < NB; ++k) {
-            const float off = ((cw >> k) & 1u) ? C::H : C::HI0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const unsigned m = (blk[k] >> (j * BITS)) & C::MASK;
-                const float mf = __fsub_rn(__uint_as_float(0x4B000000u | m), 8388608.0f);
-                y[8 * k + j] = __fmul_rn(__fsub_rn(mf, off), scf[k / 4]);
-            }
-        }
-
-        // ---- inverse Hadamard: x = H (r * sc)
-        fwht<DP>(y);
+        decode_row<D, BITS>(stage, stage_gen, lane, nsc, gshift, delta, cur.t0 == cur.t_begin, carry, carry_c, y);
 
         // ---- RoPE re-apply on keys: rotate each (i, i + D/2) pair by +angle
         if (rope != nullptr) {
             const float4* cs = rope + (t < cur.t_end ? t : cur.t_begin);  // [D/4][tokens]
 #pragma unroll
-            for (int q = 0; q < D / 4; ++q) {
-                const float4 v = __ldg(cs + int64_t(q) * tokens);
-#pragma unroll
-                for (int p = 0; p < 2; ++p) {
-                    const int j = 2 * q + p;
-                    const float c = p ? v.z : v.x, s = p ? v.w : v.y;
-                    const float a = y[j], b = y[j + D / 2];
-                    y[j] = __fmaf_rn(a, c, -__fmul_rn(b, s));
-                    y[j + D / 2] = __fmaf_rn(b, c, __fmul_rn(a, s));
-                }
-            }
+            for (int q = 0; q < D / 4; ++q) rope_apply_pairs<D>(y, q, __ldg(cs + int64_t(q) * tokens));
         }
 
-        // ---- fp16 rows -> swizzled smem tile -> TMA tensor store
-        const uint32_t ob = outbuf + (i & 1) * kTileBytes;
-        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");  // ob is free
-        __syncwarp();
+        store_rows<D, 1>(y, outbuf + (i & 1) * kTileBytes, lane, &out_map, cur.t0, int(cur.slice));
+        cur.next();
+    }
+    cp_async_wait<0>();
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// ------------------------------------------------ keys with a shared table
+//
+// Keys of head_dim 96 / 128: the 8 warps of a block decode the same 32-token
+// tile of 8 consecutive slices (slice = 8 * group + warp), so the tile's RoPE
+// table rows are staged in shared memory once per block instead of being read
+// from L2 by every warp.  Three stages (table tile + the warps' record
+// tiles), one output tile per warp; one block barrier per tile.
+constexpr int kKeyWarps = 8;
+constexpr int kKeyThreads = 32 * kKeyWarps;
+constexpr int kKeyStages = 3;
+
+template <int D>
+struct KeyStage {
+    static constexpr int TABLE = D * 4 * kTileRows;  // head_dim/4 planes x 32 tokens x 16 B
+    static constexpr int BYTES = TABLE + kKeyWarps * kRecStage;
+    static constexpr int OUT = kKeyWarps * kTileBytes;
+    static constexpr int SMEM = OUT + kKeyStages * BYTES + 1024;
+};
+
+template <int D, int BITS>
+__global__ void __launch_bounds__(kKeyThreads, 1)
+    decompress_key_kernel(const uint8_t* __restrict__ idx, const uint16_t* __restrict__ coset,
+                          const __half* __restrict__ scales, const float4* __restrict__ rope,
+                          const __grid_constant__ CUtensorMap out_map, int64_t slices, int tokens, int tpad,
+                          int group, int chunk, bool delta) {
+    constexpr int DP = PaddedDim<D>::value;
+    constexpr int NB = DP / 8;
+    constexpr int RB = DP * BITS / 8;
+    using KS = KeyStage<D>;
+
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const uint32_t base = (smem_u32(smem) + 1023u) & ~1023u;
+    const uint8_t* gbase = smem + (base - smem_u32(smem));
+    const int wib = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t outbuf = base + wib * kTileBytes;  // 1024-aligned
+    const uint32_t stages = base + KS::OUT;
+    const int nsc = DP / group;
+    const int gshift = group == 32 ? 5 : (group == 64 ? 6 : 7);
+    const int64_t ngroups = (slices + kKeyWarps - 1) / kKeyWarps;
+
+    TileWalk cur(blockIdx.x, gridDim.x, ngroups, tokens, chunk);
+    TileWalk pre = cur;
+
+    auto load_stage = [&](const TileWalk& w, uint32_t stage) {
+        for (int g = threadIdx.x; g < (D / 4) * kTileRows; g += kKeyThreads) {
+            const int q = g / kTileRows, rr = g - q * kTileRows;
+            const int tok = w.t0 + rr;
+            const bool ok = tok < tokens;
+            cp_async16(stage + 16 * g, rope + int64_t(q) * tokens + (ok ? tok : 0), ok ? 16 : 0);
+        }
+        const int64_t sl = w.slice * kKeyWarps + wib;
+        if (sl < slices) load_records<RB>(idx, coset, scales, nsc, sl * tpad + w.t0, stage + KS::TABLE + wib * kRecStage, lane);
+    };
+
 #pragma unroll
-        for (int q = 0; q < D / 8; ++q) sts128(ob + swz(lane, q), f_to_h8(&y[8 * q]));
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) {
-            const int z = int(cur.slice);
-            tma_store_3d(&out_map, ob, 0, cur.t0, z);
-            if (D > 64) tma_store_3d(&out_map, ob + 4096, 64, cur.t0, z);
-            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    for (int st = 0; st < kKeyStages - 1; ++st) {
+        if (pre.valid()) {
+            load_stage(pre, stages + st * KS::BYTES);
+            pre.next();
+        }
+        cp_async_commit();
+    }
+
+    unsigned carry[NB];
+    unsigned carry_c = 0;
+#pragma unroll
+    for (int k = 0; k < NB; ++k) carry[k] = 0;
+
+    for (int i = 0; cur.valid(); ++i) {
+        cp_async_wait<kKeyStages - 2>();  // this thread's copies of tile i are done
+        __syncthreads();                  // everyone's are; everyone is done with tile i - 1
+        if (pre.valid()) {
+            load_stage(pre, stages + ((i + kKeyStages - 1) % kKeyStages) * KS::BYTES);
+            pre.next();
+        }
+        cp_async_commit();
+        const uint32_t stage = stages + (i % kKeyStages) * KS::BYTES;
+        const int64_t slice = cur.slice * kKeyWarps + wib;
+        if (slice < slices) {  // warp-uniform
+            const uint32_t rec = stage + KS::TABLE + wib * kRecStage;
+            float y[DP];
+            decode_row<D, BITS>(rec, gbase + (rec - base), lane, nsc, gshift, delta, cur.t0 == cur.t_begin, carry,
+                                carry_c, y);
+#pragma unroll
+            for (int q = 0; q < D / 4; ++q) {
+                const uint4 raw = lds128(stage + 16 * (q * kTileRows + lane));
+                rope_apply_pairs<D>(y, q, make_float4(__uint_as_float(raw.x), __uint_as_float(raw.y),
+                                                      __uint_as_float(raw.z), __uint_as_float(raw.w)));
+            }
+            store_rows<D, 0>(y, outbuf, lane, &out_map, cur.t0, int(slice));
         }
         cur.next();
     }
@@ -353,15 +466,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         // ---- unpack, unscale: y = (code - offset) * scale  (exact)
         float y[HALF];
 #pragma unroll
-        for (int k = 0; k < NBT; ++k) {
-            const float off = ((cw >> k) & 1u) ? C::H : C::HI0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const unsigned m = (blk[k] >> (j * BITS)) & C::MASK;
-                const float mf = __fsub_rn(__uint_as_float(0x4B000000u | m), 8388608.0f);
-                y[8 * k + j] = __fmul_rn(__fsub_rn(mf, off), scf[(8 * k) / 32]);
-            }
-        }
+        for (int k = 0; k < NBT; ++k) unscale_block<BITS>(blk[k], (cw >> k) & 1u, scf[(8 * k) / 32], &y[8 * k]);
 
         // ---- inverse Hadamard (textbook order): bits below DP/4 in-thread, bit
         //      DP/4 in-thread (signed), bit DP/2 by exchange
@@ -452,12 +557,32 @@ static int launch(const LaunchArgs& a, const uint8_t* idx, const uint16_t* coset
 }
 
 template <int D, int BITS>
+static int launch_keys(const LaunchArgs& a, const uint8_t* idx, const uint16_t* coset, const __half* scales,
+                       const float4* rope, const CUtensorMap& map) {
+    auto kern = decompress_key_kernel<D, BITS>;
+    constexpr int smem = KeyStage<D>::SMEM;
+    if (!ensure_smem(reinterpret_cast<const void*>(kern), smem)) return NQ_ERR_CUDA;
+    const int chunk = a.delta_chunk > 0 ? a.delta_chunk : kTileRows;
+    const int64_t ngroups = (a.slices + kKeyWarps - 1) / kKeyWarps;
+    const int64_t items = ngroups * ((a.tokens + chunk - 1) / chunk);
+    if (items == 0) return NQ_OK;
+    const int cap = grid_capacity_threads(reinterpret_cast<const void*>(kern), smem, kKeyThreads);
+    if (cap <= 0) return NQ_ERR_CUDA;
+    const int grid = int(std::min<int64_t>(items, cap));
+    kern<<<grid, kKeyThreads, smem, a.stream>>>(idx, coset, scales, rope, map, a.slices, a.tokens, a.tpad,
+                                                a.group, chunk, a.delta_chunk > 0);
+    return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
+}
+
+template <int D, int BITS>
 static int launch_any(const LaunchArgs& a, const uint8_t* idx, const uint16_t* coset, const __half* scales,
                       const float4* rope, const CUtensorMap& map) {
-    if constexpr (D != 64)
+    if constexpr (D != 64) {
+        if (rope != nullptr) return launch_keys<D, BITS>(a, idx, coset, scales, rope, map);
         return launch<D, BITS>(a, idx, coset, scales, rope, map);
-    else
+    } else {
         return launch_pair<D, BITS>(a, idx, coset, scales, rope, map);
+    }
 }
 
 template <int D>

@@ -244,14 +244,27 @@ __device__ __forceinline__ int e8_general(const float (&u)[8], bool strict, floa
 // same codes as the general path:
 //   e~0 = rint(u) - u  (exact, never -0); the half-integer point is
 //   rint(u) + 1/2 if e~0 < 0 else rint(u) - 1/2 (= ceil(u) - 1/2), so its
-//   residual is e~1 = e~0 - copysign(1/2, e~0) (exact); the integer score is
+//   residual is e~1 = e~0 - copysign(1/2, e~0); the integer score is
 //   min(|e~0|, hi0 - |u|) (a step that would leave the box turns around).
+//
+// Coset choice.  Per coordinate |e~1| = 1/2 - |e~0| exactly, so
+// e~0^2 - e~1^2 = |e~0| - 1/4 and, with the fix-up costs 1 - 2*score,
+//   D = d0' - d1' = sum_j |e~0_j| - 2 + odd0 (1 - 2 smax0) - odd1 (1 - 2 smax1)
+// in exact arithmetic.  The general path (the method's own procedure) sums the
+// squared residuals in fp32; each of its two distances is within 1.3e-6 of the
+// exact value (eight roundings of numbers below 3, one rounding of e~1), and
+// the estimate of D formed here is within 1.2e-6 of the exact D.  So wherever
+// |estimate| > 2^-16 the sign of the estimate is the sign of the general
+// path's comparison; inside that band the function returns false and the
+// caller runs the general path.
+//
 // The codes are accumulated as exact integer-valued floats on the FMA pipe
 // (sum of r_j * L^j over half-blocks of 4 coordinates, < 2^16), the parities
-// by xor of the magic-rounded bit patterns.  A block whose chosen coset needs
-// a fix-up with a tie for the maximal score or a maximal score <= 0 (every
-// coordinate an exact integer or past the box edge) is not handled here: the
-// function returns false and the caller runs the general path.
+// by xor of the magic-rounded bit patterns.  Pairs of coordinates share packed
+// f32x2 instructions (each half an ordinary IEEE operation).  A block whose
+// chosen coset needs a fix-up with a tie for the maximal score or a maximal
+// score <= 2^-100 (every coordinate nearly an integer or past the box edge) is
+// not handled here either.
 template <int BITS, bool STRICT>
 __device__ __forceinline__ bool e8_fast(const float (&u)[8], unsigned& code, unsigned& coset) {
     using C = Code<BITS>;
@@ -259,26 +272,39 @@ __device__ __forceinline__ bool e8_fast(const float (&u)[8], unsigned& code, uns
     constexpr float Lp[4] = {1.0f, L, L * L, L * L * L};
     constexpr float SUML = 1.0f + L + L * L + L * L * L;
     constexpr float TWO23 = 8388608.0f;
+    constexpr float BAND = 1.52587890625e-05f;  // 2^-16
+    const float2 M2 = make_float2(kMagic, kMagic);
     float eb1[8], s0[8], csv[8];
-    float d0 = 0.0f, d1 = 0.0f;
-    float A[2] = {0.0f, 0.0f}, Bq[2] = {0.0f, 0.0f};
+    float2 S = make_float2(0.0f, 0.0f);
+    // A = 2^23 + (L/2 - 1) SUML + sum r0_j L^j: 2^23 plus the integer code
+    // B = sum cs_j L^j - SUML / 2, so that A - B = 2^23 plus the half code
+    constexpr float A0 = TWO23 + float(C::OFF0) * SUML;
+    constexpr float B0 = -0.5f * SUML;
+    float2 A[2] = {make_float2(A0, 0.0f), make_float2(A0, 0.0f)};
+    float2 B[2] = {make_float2(B0, 0.0f), make_float2(B0, 0.0f)};
     unsigned x0 = 0, xs = 0;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const float t = __fadd_rn(u[j], kMagic);
-        const float r0 = __fsub_rn(t, kMagic);
-        const float e0 = __fsub_rn(r0, u[j]);
-        const float cs = copysignf(0.5f, e0);
-        const float e1 = __fsub_rn(e0, cs);
-        csv[j] = cs;
-        eb1[j] = e1;
-        d0 = __fmaf_rn(e0, e0, d0);
-        d1 = __fmaf_rn(e1, e1, d1);
-        A[j >> 2] = __fmaf_rn(r0, Lp[j & 3], A[j >> 2]);
-        Bq[j >> 2] = __fmaf_rn(cs, Lp[j & 3], Bq[j >> 2]);
-        s0[j] = fminf(fabsf(e0), __fsub_rn(C::HI0, fabsf(u[j])));
-        x0 ^= __float_as_uint(t);
-        if (STRICT) xs ^= __float_as_uint(e0);
+    for (int j = 0; j < 8; j += 2) {
+        const float2 uu = make_float2(u[j], u[j + 1]);
+        const float2 t = __fadd2_rn(uu, M2);
+        const float2 r0 = fsub2(t, M2);
+        const float2 e0 = fsub2(r0, uu);
+        const float2 cs = make_float2(copysignf(0.5f, e0.x), copysignf(0.5f, e0.y));
+        const float2 lp = make_float2(Lp[j & 3], Lp[(j & 3) + 1]);
+        csv[j] = cs.x;
+        csv[j + 1] = cs.y;
+        S = __ffma2_rn(cs, e0, S);  // |e~0| / 2 per coordinate (exact products)
+        A[j >> 2] = __ffma2_rn(r0, lp, A[j >> 2]);
+        B[j >> 2] = __ffma2_rn(cs, lp, B[j >> 2]);
+        s0[j] = fminf(fabsf(e0.x), __fsub_rn(C::HI0, fabsf(uu.x)));
+        s0[j + 1] = fminf(fabsf(e0.y), __fsub_rn(C::HI0, fabsf(uu.y)));
+        x0 ^= __float_as_uint(t.x) ^ __float_as_uint(t.y);
+        if (STRICT) {
+            const float2 e1 = fsub2(e0, cs);
+            eb1[j] = e1.x;
+            eb1[j + 1] = e1.y;
+            xs ^= __float_as_uint(e0.x) ^ __float_as_uint(e0.y);
+        }
     }
     const float smax0 = fmax3(fmax3(s0[0], s0[1], s0[2]), fmax3(s0[3], s0[4], s0[5]), fmaxf(s0[6], s0[7]));
     float smax1 = 0.0f;
@@ -287,54 +313,53 @@ __device__ __forceinline__ bool e8_fast(const float (&u)[8], unsigned& code, uns
                       fmax3(fabsf(eb1[3]), fabsf(eb1[4]), fabsf(eb1[5])), fmaxf(fabsf(eb1[6]), fabsf(eb1[7])));
     const bool odd0 = (x0 & 1u) != 0;
     const bool odd1 = STRICT && (((x0 ^ (xs >> 31)) & 1u) != 0);  // + number of e~0 < 0
-    const float dd0 = odd0 ? __fadd_rn(d0, __fmaf_rn(-2.0f, smax0, 1.0f)) : d0;
-    const float dd1 = odd1 ? __fadd_rn(d1, __fmaf_rn(-2.0f, smax1, 1.0f)) : d1;
-    const bool half = dd1 < dd0;
+    float D = __fmaf_rn(2.0f, __fadd_rn(S.x, S.y), -2.0f);  // sum |e~0| - 2
+    if (odd0) D = __fadd_rn(D, __fmaf_rn(-2.0f, smax0, 1.0f));
+    if (odd1) D = __fsub_rn(D, __fmaf_rn(-2.0f, smax1, 1.0f));
+    bool ok = fabsf(D) > BAND;
+    const bool half = D > 0.0f;
 
     // fix-up of the chosen coset: move its first maximal-score coordinate k one
     // step toward u, i.e. add -2*cs_k*L^k to the integer code (u above rint(u)
     // moves up) or +2*cs_k*L^k to the half-integer code.  k is found on the FMA
-    // pipe: f_j = sat((smax - s_j) * 2^127) is 0 at a maximum and 1 elsewhere
-    // (distinct scores differ by far more than 2^-127), and
-    // G = sum_j (1 - f_j) cs_j L^j picks cs_k L^k.  Ties (sum f != 7) and a
-    // non-positive maximum go to the general path.
-    float g[2] = {0.0f, 0.0f};
+    // pipe: i_j = sat(1 - (smax - s_j) * 2^127) is 1 at a maximum and 0
+    // elsewhere (with smax > 2^-100, distinct scores differ by at least 2^-123),
+    // and G = sum_j i_j cs_j L^j picks cs_k L^k.  A tie (sum i != 1) goes to the
+    // general path.  Computed for every block (no branch), applied if needed.
     const bool fix = half ? odd1 : odd0;
-    if (fix) {
-        const float smax = half ? smax1 : smax0;
-        if (!(smax > 0.0f)) return false;
-        float cnt = 0.0f;
-        float G[2] = {0.0f, 0.0f};
+    const float smax = half ? smax1 : smax0;
+    float2 cnt = make_float2(0.0f, 0.0f);
+    float2 G[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float sj = (STRICT && half) ? fabsf(eb1[j]) : s0[j];
-            float f;
-            asm("mul.rn.sat.f32 %0, %1, 0f7F000000;" : "=f"(f) : "f"(__fsub_rn(smax, sj)));
-            cnt = __fadd_rn(cnt, f);
-            const float v = __fmaf_rn(-f, csv[j], csv[j]);  // cs_j at the maximum, else 0
-            G[j >> 2] = __fmaf_rn(v, Lp[j & 3], G[j >> 2]);
-        }
-        if (cnt != 7.0f) return false;
-        const float m = half ? 2.0f : -2.0f;
-        g[0] = __fmul_rn(m, G[0]);
-        g[1] = __fmul_rn(m, G[1]);
+    for (int j = 0; j < 8; j += 2) {
+        const float2 sj = (STRICT && half) ? make_float2(fabsf(eb1[j]), fabsf(eb1[j + 1]))
+                                           : make_float2(s0[j], s0[j + 1]);
+        const float2 dlt = fsub2(make_float2(smax, smax), sj);
+        float2 ind;
+        asm("fma.rn.sat.f32 %0, %1, 0fFF000000, 0f3F800000;" : "=f"(ind.x) : "f"(dlt.x));
+        asm("fma.rn.sat.f32 %0, %1, 0fFF000000, 0f3F800000;" : "=f"(ind.y) : "f"(dlt.y));
+        cnt = __fadd2_rn(cnt, ind);
+        const float2 cl = __fmul2_rn(make_float2(csv[j], csv[j + 1]), make_float2(Lp[j & 3], Lp[(j & 3) + 1]));
+        G[j >> 2] = __ffma2_rn(ind, cl, G[j >> 2]);
     }
+    ok = ok && (!fix || (smax > 7.88860905e-31f && __fadd_rn(cnt.x, cnt.y) == 1.0f));  // 2^-100
+    const float m = fix ? (half ? 2.0f : -2.0f) : 0.0f;
+    const float g[2] = {__fmul_rn(m, __fadd_rn(G[0].x, G[0].y)), __fmul_rn(m, __fadd_rn(G[1].x, G[1].y))};
 
     // integer codes m0 = r0 + (L/2 - 1), half-integer codes m1 = r1 + (L - 1)/2,
-    // per half-block an exact integer below 2^16 read off the float's low bits
+    // per half-block an exact integer below 2^16 in the low bits of 2^23 + m
+    // (every intermediate is a multiple of 1/2 below 2^24, so all of this is exact)
     unsigned c = 0;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-        // every intermediate is an integer below 2^24 (Bq and (L-1)/2 * SUML are
-        // both odd multiples of 1/2), so all of this is exact
-        const float ap = __fadd_rn(A[h], TWO23);
-        const float f0 = __fadd_rn(__fadd_rn(ap, float(C::OFF0) * SUML), g[h]);
-        const float f1 = __fadd_rn(__fsub_rn(ap, __fsub_rn(Bq[h], C::H * SUML)), g[h]);
-        c |= (__float_as_uint(half ? f1 : f0) & 0xffffu) << (4 * BITS * h);
+        const float Ah = __fadd_rn(A[h].x, A[h].y);
+        const float Bh = half ? __fadd_rn(B[h].x, B[h].y) : 0.0f;
+        const float f = __fadd_rn(__fsub_rn(Ah, Bh), g[h]);
+        c |= (__float_as_uint(f) & 0xffffu) << (4 * BITS * h);
     }
     code = c;
     coset = half ? 1u : 0u;
-    return true;
+    return ok;
 }
 
 // Block code of a general-path point.
@@ -361,6 +386,29 @@ __device__ __forceinline__ unsigned pack_point(const float (&r)[8], int coset) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) code |= (unsigned)__float2int_rn(__fadd_rn(r[j], off)) << (j * BITS);
     return code;
+}
+
+// Block code -> the 8 unscaled coordinates y_j = (m_j - offset) * sc, exact:
+// 2^22 + m_j is built from its bits (the fp32 spacing at 2^22 is 1/2, so the
+// field goes in shifted left by one), 2^22 + offset is exact for the integer
+// and the half-integer offsets alike, their difference is m_j - offset, and
+// that small half-integer times the fp16 scale is exact too.  Pairs of
+// coordinates share packed f32x2 instructions.
+template <int BITS>
+__device__ __forceinline__ void unscale_block(unsigned code, unsigned coset, float sc, float* y) {
+    using C = Code<BITS>;
+    const float k = coset ? 4194304.0f + C::H : 4194304.0f + C::HI0;
+    const float2 k2 = make_float2(k, k), s2 = make_float2(sc, sc);
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+        const unsigned a = j ? (code >> (j * BITS - 1)) : (code << 1);
+        const unsigned b = code >> ((j + 1) * BITS - 1);
+        const float2 t = make_float2(__uint_as_float((a & (C::MASK << 1)) | 0x4A800000u),
+                                     __uint_as_float((b & (C::MASK << 1)) | 0x4A800000u));
+        const float2 v = __fmul2_rn(fsub2(t, k2), s2);
+        y[j] = v.x;
+        y[j + 1] = v.y;
+    }
 }
 
 // ------------------------------------------------------------ fp16 <-> fp32

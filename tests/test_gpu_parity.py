@@ -123,6 +123,48 @@ def test_e8_nearest_bit_exact(nq, orc, bits, strict):
     assert mism.size == 0, (mism[:5], u[mism[:1]], got[mism[:1]], ref[mism[:1]])
 
 
+def _near_tie_blocks(rng, bits, strict, n):
+    """Blocks whose two coset distances (after the parity fix-ups) differ by at
+    most a few 1e-5: one coordinate's residual is set so that, in exact
+    arithmetic, sum|u - rint(u)| - 2 + fix-up costs lands near zero (exact ties
+    included).  Only the inputs are made here; the expected points are the
+    oracle's."""
+    h = ((1 << bits) - 1) / 2
+    hi0 = (1 << bits) // 2 - 1
+    out = []
+    while len(out) < n:
+        u = rng.uniform(-h * 0.98, h * 0.98, 8)
+        r0 = np.rint(u)
+        e0 = r0 - u
+        e1 = e0 - np.copysign(0.5, e0)
+        s0 = np.minimum(np.abs(e0), hi0 - np.abs(u))
+        odd0 = int(r0.sum()) & 1
+        odd1 = bool(strict) and (int(round((u + e1 - 0.5).sum())) & 1)
+        gap = np.abs(e0).sum() - 2 + (1 - 2 * s0.max()) * odd0 - (1 - 2 * np.abs(e1).max()) * odd1
+        ks = [k for k in range(8) if s0[k] != s0.max() and abs(e1[k]) != np.abs(e1).max()
+              and 0.05 < abs(e0[k]) < 0.45 and abs(u[k]) < hi0]
+        if not ks:
+            continue
+        na = abs(e0[ks[0]]) - gap + rng.choice([0.0, rng.uniform(-3e-5, 3e-5), rng.uniform(-1e-6, 1e-6)])
+        if not 0.01 < na < 0.49:
+            continue
+        u[ks[0]] = r0[ks[0]] - np.sign(e0[ks[0]]) * na
+        out.append(u)
+    return np.asarray(out, dtype=np.float32)
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+@pytest.mark.parametrize("strict", [0, 1])
+def test_e8_nearest_near_ties(nq, orc, bits, strict):
+    """Coset choices decided by less than the fp32 rounding of the distances."""
+    rng = np.random.default_rng(90 + bits + 7 * strict)
+    u = _near_tie_blocks(rng, bits, strict, 20000)
+    got = nq.e8_nearest(torch.from_numpy(u).cuda(), strict, bits).cpu().numpy()
+    ref = orc.e8_nearest(u, strict, bits)
+    mism = np.nonzero(np.any(got != ref, axis=1))[0]
+    assert mism.size == 0, (mism[:5], u[mism[:1]], got[mism[:1]], ref[mism[:1]])
+
+
 # ------------------------------------------------------------- tiny cache
 
 
