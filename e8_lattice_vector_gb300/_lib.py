@@ -47,6 +47,9 @@ SIGNATURES = {
     "nq_decompress_kv": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
                                         ctypes.POINTER(Shape), ctypes.POINTER(Params), ctypes.c_void_p,
                                         ctypes.c_void_p, ctypes.c_void_p]),
+    "nq_roundtrip_kv": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                       ctypes.POINTER(Shape), ctypes.POINTER(Params), ctypes.c_void_p,
+                                       ctypes.c_void_p, ctypes.c_void_p]),
     "nq_e8_nearest": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
                                      ctypes.c_int, ctypes.c_void_p]),
     "nq_strerror": (ctypes.c_char_p, [ctypes.c_int]),

@@ -156,6 +156,32 @@ def decompress_kv(buf, shape, params, rope=None, K_out=None, V_out=None):
     return K_out, V_out
 
 
+def roundtrip_kv(K, V, params, rope=None, K_out=None, V_out=None):
+    """decompress_kv(compress_kv(K, V)) in one pass, without the compressed
+    buffer; returns (K_out, V_out).  Passing K_out=K, V_out=V reconstructs the
+    cache in place."""
+    _check_kv(K, "K")
+    _check_kv(V, "V")
+    shape = shape_of(K)
+    if shape_of(V) != shape:
+        raise ValueError("K and V shapes differ")
+    if K_out is None:
+        K_out = torch.empty_like(K)
+    if V_out is None:
+        V_out = torch.empty_like(V)
+    _check_kv(K_out, "K_out")
+    _check_kv(V_out, "V_out")
+    if shape_of(K_out) != shape or shape_of(V_out) != shape:
+        raise ValueError("output shapes differ from the input's")
+    rp = _rope_ptr(rope, params, shape[3], shape[4])
+    st = _lib.lib().nq_roundtrip_kv(ctypes_void(K.data_ptr()), ctypes_void(V.data_ptr()), rp,
+                                    ctypes_ref(_cshape(shape)), ctypes_ref(params.c()),
+                                    ctypes_void(K_out.data_ptr()), ctypes_void(V_out.data_ptr()),
+                                    _stream_handle(K.device))
+    _lib.check("nq_roundtrip_kv", st)
+    return K_out, V_out
+
+
 def e8_nearest(u, strict, bits):
     """Nearest E8 codebook point of each 8-block of a float32 CUDA tensor [..., 8]."""
     if not (u.is_cuda and u.dtype == torch.float32 and u.is_contiguous() and u.shape[-1] == 8):

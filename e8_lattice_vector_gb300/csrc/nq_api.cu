@@ -247,6 +247,33 @@ int nq_compress_kv(const void* k_f16, const void* v_f16, const float* rope_table
                                       reinterpret_cast<uint16_t*>(base + L.v_scale));
 }
 
+int nq_roundtrip_kv(const void* k_f16, const void* v_f16, const float* rope_table,
+                    const nq_shape* shape, const nq_params* params, void* k_f16_out, void* v_f16_out,
+                    void* stream) {
+    int st = nq::check(shape, params);
+    if (st != NQ_OK) return st;
+    nq_layout L;
+    nq::make_layout(shape, params, &L);
+    if (L.rows == 0) return NQ_OK;
+    const bool rope = params->rope_theta > 0.0f;
+    if (!k_f16 || !v_f16 || !k_f16_out || !v_f16_out || (rope && !rope_table)) return NQ_ERR_ARG;
+    if (!nq::aligned16(k_f16) || !nq::aligned16(v_f16) || !nq::aligned16(k_f16_out) ||
+        !nq::aligned16(v_f16_out) || (rope && !nq::aligned16(rope_table)))
+        return NQ_ERR_ARG;
+    nq::LaunchArgs a;
+    a.slices = int64_t(shape->layers) * shape->batch * shape->kv_heads;
+    a.tokens = shape->tokens;
+    a.tpad = int(L.tokens_padded);
+    a.group = params->group_size;
+    a.delta_chunk = 0;
+    a.stream = static_cast<cudaStream_t>(stream);
+    st = nq::launch_roundtrip_tensor(a, shape->head_dim, params->key_bits, params->strict != 0, k_f16,
+                                     rope ? rope_table : nullptr, k_f16_out);
+    if (st != NQ_OK) return st;
+    return nq::launch_roundtrip_tensor(a, shape->head_dim, params->value_bits, params->strict != 0, v_f16,
+                                       nullptr, v_f16_out);
+}
+
 int nq_decompress_kv(const void* in, size_t in_bytes, const float* rope_table,
                      const nq_shape* shape, const nq_params* params, void* k_f16_out,
                      void* v_f16_out, void* stream) {

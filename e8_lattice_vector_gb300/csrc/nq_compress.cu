@@ -11,49 +11,12 @@
 // The grid is one resident block per SM; warps take work items
 // (slice, chunk of delta_chunk tokens, or 32 tokens without delta)
 // round-robin.
-#include "nq_internal.h"
+#include "nq_encode.cuh"
 
 namespace nq {
 
 constexpr int kStages = 3;
 constexpr int kCompressSmem = kWarpsPerBlock * kStages * kTileBytes;
-
-// Copy the fp16 rows of a tile into a stage; rows past the chunk are zeros.
-// Scaled coordinates u = y * inv of 8-block k of a one-thread row.
-template <int N>
-__device__ __forceinline__ void row_block_u(const float (&y)[N], float inv, int k, float (&u)[8]) {
-#pragma unroll
-    for (int j = 0; j < 8; j += 2) {
-        const float2 p = __fmul2_rn(make_float2(y[8 * k + j], y[8 * k + j + 1]), make_float2(inv, inv));
-        u[j] = p.x;
-        u[j + 1] = p.y;
-    }
-}
-
-// The same for a two-thread row: slots at or above Q hold the odd thread's
-// negated coordinates, so their reciprocal scale carries the thread's sign.
-template <int Q, int N, int NS>
-__device__ __forceinline__ void pair_block_u(const float (&y)[N], const float (&inv)[NS], float sgn, int k,
-                                             float (&u)[8]) {
-    const float ik = (8 * k >= Q) ? __fmul_rn(inv[(8 * k) / 32], sgn) : inv[(8 * k) / 32];
-    row_block_u(y, ik, k, u);
-}
-
-template <int D>
-__device__ __forceinline__ void load_tile(const __half* __restrict__ x, const TileWalk& w, uint32_t stage,
-                                          int lane) {
-    constexpr int CPR = D / 8;  // 16-byte chunks per row
-    const int nvalid = min(kTileRows, w.t_end - w.t0);
-    const __half* base = x + (w.slice * w.tokens + w.t0) * int64_t(D);
-#pragma unroll
-    for (int i = 0; i < CPR; ++i) {
-        const int g = lane + 32 * i;
-        const int r = g / CPR;
-        const int c = g - r * CPR;
-        const bool ok = r < nvalid;
-        cp_async16(stage + swz(r, c), ok ? base + 8 * g : base, ok ? 16 : 0);
-    }
-}
 
 template <int D, int BITS, bool STRICT>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -63,10 +26,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int DP = PaddedDim<D>::value;
     constexpr int NB = DP / 8;
     constexpr int NSUB = DP / 32;
-    using C = Code<BITS>;
     using RP = RowPack<BITS, NB>;
     constexpr int RB = DP * BITS / 8;  // idx bytes per row
-    constexpr float STEP = float(DP) * C::H;
 
     extern __shared__ __align__(1024) uint8_t smem[];
     const int lane = threadIdx.x & 31;
@@ -117,76 +78,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // table layout [D/4][tokens] float4: lanes read consecutive tokens
             const float4* cs = rope + (active ? t : cur.t_begin);
 #pragma unroll
-            for (int q = 0; q < D / 4; ++q) {
-                const float4 v = __ldg(cs + int64_t(q) * tokens);
-#pragma unroll
-                for (int p = 0; p < 2; ++p) {
-                    const int j = 2 * q + p;
-                    const float c = p ? v.z : v.x, s = p ? v.w : v.y;
-                    const float a = y[j], b = y[j + D / 2];
-                    y[j] = __fmaf_rn(a, c, __fmul_rn(b, s));
-                    y[j + D / 2] = __fmaf_rn(b, c, -__fmul_rn(a, s));
-                }
-            }
+            for (int q = 0; q < D / 4; ++q) row_rope_remove<D>(y, q, __ldg(cs + int64_t(q) * tokens));
         }
 
-        // ---- Hadamard rotation (compression stage order)
-        fwht_forward<DP>(y);
-
-        // ---- group absmax -> fp16 scale -> reciprocal (per 32-subgroup)
-        float amax[NSUB];
-#pragma unroll
-        for (int s = 0; s < NSUB; ++s) {
-            float m = 0.0f;
-#pragma unroll
-            for (int j = 32 * s; j < 32 * s + 32; j += 2) m = fmax3(m, fabsf(y[j]), fabsf(y[j + 1]));
-            amax[s] = m;
-        }
-        if (group >= 64) {
-#pragma unroll
-            for (int s = 0; s < NSUB; s += 2) amax[s] = amax[s + 1] = fmaxf(amax[s], amax[s + 1]);
-        }
-        if (group >= 128 && NSUB == 4) {
-            const float m = fmaxf(amax[0], amax[2]);
-#pragma unroll
-            for (int s = 0; s < NSUB; ++s) amax[s] = m;
-        }
         unsigned short sc[NSUB];
-        float inv[NSUB];
-        bool fast = true;
-#pragma unroll
-        for (int s = 0; s < NSUB; ++s) {
-            sc[s] = group_scale(amax[s], STEP);
-            const float scf = __half2float(__ushort_as_half(sc[s]));
-            inv[s] = sc[s] ? __frcp_rn(__fmul_rn(scf, float(DP))) : 0.0f;
-            fast = fast && (__fmul_rn(amax[s], inv[s]) < C::H);
-        }
-
-        // ---- E8 nearest point per 8-block -> block codes
         unsigned blk[NB];
-        unsigned cw = 0, declined = 0;
-#pragma unroll
-        for (int k = 0; k < NB; ++k) {
-            float u[8];
-            row_block_u(y, inv[k / 4], k, u);
-            unsigned c;
-            const bool ok = e8_fast<BITS, STRICT>(u, blk[k], c);
-            cw |= c << k;
-            declined |= unsigned(!ok) << k;
-        }
-        if (!fast) declined = (1u << NB) - 1u;
-        if (declined) {
-#pragma unroll
-            for (int k = 0; k < NB; ++k) {
-                if (!((declined >> k) & 1u)) continue;
-                float u[8];
-                row_block_u(y, inv[k / 4], k, u);
-                const uint2 res = e8_slow<BITS, STRICT>(make_float4(u[0], u[1], u[2], u[3]),
-                                                        make_float4(u[4], u[5], u[6], u[7]));
-                blk[k] = res.x;
-                cw = (cw & ~(1u << k)) | (res.y << k);
-            }
-        }
+        unsigned cw;
+        row_encode_codes<D, BITS, STRICT>(y, group, blk, cw, sc);
 
         // ---- temporal delta against the previous token of the chunk
         if (delta) {
@@ -254,22 +152,6 @@ constexpr int kPairCompressSmem = kWarpsPerBlock * kPairStages * kPairTileBytes;
 // The walk runs over the padded token range (tokens rounded up to 32) so that
 // every record row, padding included, is written; rows at or past `tokens`
 // are zero-filled.
-template <int D>
-__device__ __forceinline__ void load_pair_tile(const __half* __restrict__ x, int64_t slice, int t0, int tokens,
-                                               uint32_t stage, int lane) {
-    constexpr int CPR = D / 8;  // 16-byte chunks per row
-    const int nvalid = min(kPairRows, tokens - t0);
-    const __half* base = x + (slice * tokens + min(t0, tokens - 1)) * int64_t(D);
-#pragma unroll
-    for (int i = 0; i < CPR / 2; ++i) {  // 16 rows * CPR chunks / 32 lanes
-        const int g = lane + 32 * i;
-        const int r = g / CPR;
-        const int c = g - r * CPR;
-        const bool ok = r < nvalid;
-        cp_async16(stage + swz16(r, c), ok ? base + 8 * g : base, ok ? 16 : 0);
-    }
-}
-
 template <int NBYTES>
 __device__ __forceinline__ void store_words(uint8_t* dst, const unsigned* w) {
     if constexpr (NBYTES % 16 == 0) {
@@ -286,8 +168,8 @@ __device__ __forceinline__ void store_words(uint8_t* dst, const unsigned* w) {
 }
 
 // The per-row work after the RoPE removal, shared by both two-thread
-// kernels: Hadamard rotation (compression order), group scale, E8 search,
-// temporal delta, and the store of record row rrow.  y: the thread's
+// kernels: the block codes (rotation, group scale, E8 search), the temporal
+// delta, and the store of record row rrow.  y: the thread's
 // coordinates in PairMap slots.  t: token index of the row; first: the tile
 // starts a delta chunk at t_begin.
 template <int D, int BITS, bool STRICT>
@@ -299,83 +181,23 @@ __device__ __forceinline__ void pair_encode_row(float (&y)[D / 2], int hf, int r
     constexpr int DP = D;
     using PM = PairMap<DP>;
     constexpr int HALF = PM::HALF;
-    constexpr int Q = PM::Q;
     constexpr int NBT = PM::NBT;
     constexpr int NSUB = HALF / 32;  // 32-coordinate subgroups per thread
-    using C = Code<BITS>;
     using RP = RowPack<BITS, NBT>;
     constexpr int RB = DP * BITS / 8;  // idx bytes per row
     constexpr int RBT = RB / 2;        // idx bytes per thread
-    constexpr float STEP = float(DP) * C::H;
     const int nsc = DP / group;
     const int span = group / 32;  // 32-coordinate subgroups per scale group
 
-    // ---- Hadamard rotation, compression order: bits below DP/4 in-thread,
-    //      bit DP/2 in-thread (signed), bit DP/4 by exchange
-#pragma unroll
-    for (int h = 1; h < Q; h *= 2) fwht_stage<HALF>(y, h);
-    stage_signed<HALF>(y, sgn);
-    stage_exchange<HALF>(y);
-
-    // ---- group absmax -> fp16 scale -> reciprocal (per 32-subgroup)
-    float amax[NSUB];
-#pragma unroll
-    for (int s = 0; s < NSUB; ++s) {
-        float m = 0.0f;
-#pragma unroll
-        for (int j = 32 * s; j < 32 * s + 32; j += 2) m = fmax3(m, fabsf(y[j]), fabsf(y[j + 1]));
-        amax[s] = m;
-    }
-    if (NSUB == 2 && span >= 2) amax[0] = amax[1] = fmaxf(amax[0], amax[1]);
-    if (span > NSUB) {
-        const float o = __shfl_xor_sync(kFull, amax[0], 1);
-#pragma unroll
-        for (int s = 0; s < NSUB; ++s) amax[s] = fmaxf(amax[s], o);
-    }
     unsigned short sc[NSUB];
-    float inv[NSUB];
-    bool fast = true;
-#pragma unroll
-    for (int s = 0; s < NSUB; ++s) {
-        sc[s] = group_scale(amax[s], STEP);
-        const float scf = __half2float(__ushort_as_half(sc[s]));
-        inv[s] = sc[s] ? __frcp_rn(__fmul_rn(scf, float(DP))) : 0.0f;
-        fast = fast && (__fmul_rn(amax[s], inv[s]) < C::H);
-    }
-
-    // ---- E8 nearest point per 8-block -> block codes
-    // Fast path for every block without a branch, then the general path for
-    // the blocks it declined (rare), so consecutive blocks can overlap.
     unsigned blk[NBT];
-    unsigned cwl = 0, declined = 0;
-#pragma unroll
-    for (int k = 0; k < NBT; ++k) {
-        float u[8];
-        pair_block_u<Q>(y, inv, sgn, k, u);
-        unsigned c;
-        const bool ok = e8_fast<BITS, STRICT>(u, blk[k], c);
-        cwl |= c << k;
-        declined |= unsigned(!ok) << k;
-    }
-    if (!fast) declined = (1u << NBT) - 1u;
-    if (declined) {
-#pragma unroll
-        for (int k = 0; k < NBT; ++k) {
-            if (!((declined >> k) & 1u)) continue;
-            float u[8];
-            pair_block_u<Q>(y, inv, sgn, k, u);
-            const uint2 res = e8_slow<BITS, STRICT>(make_float4(u[0], u[1], u[2], u[3]),
-                                                    make_float4(u[4], u[5], u[6], u[7]));
-            blk[k] = res.x;
-            cwl = (cwl & ~(1u << k)) | (res.y << k);
-        }
-    }
+    unsigned cwl;
+    pair_encode_codes<D, BITS, STRICT>(y, hf, sgn, group, blk, cwl, sc);
     unsigned cw = cwl << (hf * NBT);
     cw |= __shfl_xor_sync(kFull, cw, 1);
 
     // ---- temporal delta against the previous token (row r - 1: lane - 2)
     if (delta) {
-        
 #pragma unroll
         for (int k = 0; k < NBT; ++k) {
             unsigned prev = __shfl_up_sync(kFull, blk[k], 2);
@@ -399,7 +221,7 @@ __device__ __forceinline__ void pair_encode_row(float (&y)[D / 2], int hf, int r
 #pragma unroll
         for (int s = 0; s < NSUB; ++s) sc[s] = 0;
     }
-            unsigned w[RP::WORDS];
+    unsigned w[RP::WORDS];
     RP::pack(blk, w);
     store_words<RBT>(idx + rrow * RB + hf * RBT, w);
     if (hf == 0) coset[rrow] = uint16_t(cw);
@@ -469,17 +291,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (rope != nullptr) {
             const float4* cs = rope + (active ? t : 0);
 #pragma unroll
-            for (int qq = 0; qq < Q / 2; ++qq) {
-                const float4 v = __ldg(cs + int64_t(hf * (Q / 2) + qq) * tokens);
-#pragma unroll
-                for (int p = 0; p < 2; ++p) {
-                    const int l = 2 * qq + p;
-                    const float c = p ? v.z : v.x, s = p ? v.w : v.y;
-                    const float a = y[l], b = y[l + Q];
-                    y[l] = __fmaf_rn(a, c, __fmul_rn(b, s));
-                    y[l + Q] = __fmaf_rn(b, c, -__fmul_rn(a, s));
-                }
-            }
+            for (int qq = 0; qq < Q / 2; ++qq)
+                pair_rope_remove<D>(y, qq, __ldg(cs + int64_t(hf * (Q / 2) + qq) * tokens));
         }
 
         pair_encode_row<D, BITS, STRICT>(y, hf, r, sgn, t, active, delta, cur.t0 == cur.t_begin, cur.t_begin,
@@ -487,31 +300,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         cur.next();
     }
     cp_async_wait<0>();
-}
-
-// ------------------------------------ keys: the RoPE table shared by a block
-//
-// A block of 16 warps compresses the same 16-token tile of 16 consecutive
-// slices (warp w: slice 16*g + w).  The tile's RoPE table rows (head_dim/4
-// planes x 16 tokens x 16 bytes) are staged once per block, next to the 16
-// warps' fp16 tiles, in a 3-stage ring filled by cp.async; one block barrier
-// per tile orders the refills.  Each key row then reads 512 bytes of table
-// from shared memory instead of L2.
-constexpr int kRopeWarps = 16;
-constexpr int kRopeThreads = kRopeWarps * 32;
-constexpr int kRopeStages = 3;
-template <int D>
-struct RopeStage {
-    static constexpr int TABLE = D * 4 * kPairRows;  // head_dim/4 planes x 16 tokens x 16 B
-    static constexpr int BYTES = TABLE + kRopeWarps * kPairTileBytes;
-    static constexpr int SMEM = kRopeStages * BYTES + 1024;
-};
-
-// table position of (plane q, tile row rr): the odd thread's planes (q >= D/8)
-// are shifted by 4 rows so the two threads of a row hit different banks
-template <int D>
-__device__ __forceinline__ uint32_t rope_slot(int q, int rr) {
-    return uint32_t((q * kPairRows + (rr ^ (q >= D / 8 ? 4 : 0))) * 16);
 }
 
 template <int D, int BITS, bool STRICT>
@@ -584,19 +372,7 @@ __global__ void __launch_bounds__(kRopeThreads, 1)
             for (int c = 0; c < NBT; ++c) h8_to_f(lds128(tile + swz16(r, PM::chunk(hf, c))), &y[8 * c]);
             // RoPE removal with the block's table tile: pairs (i, i + D/2) are slots (l, l + Q)
 #pragma unroll
-            for (int qq = 0; qq < Q / 2; ++qq) {
-                const uint4 raw = lds128(stage + rope_slot<D>(hf * (Q / 2) + qq, r));
-                const float4 v = make_float4(__uint_as_float(raw.x), __uint_as_float(raw.y), __uint_as_float(raw.z),
-                                             __uint_as_float(raw.w));
-#pragma unroll
-                for (int p = 0; p < 2; ++p) {
-                    const int l = 2 * qq + p;
-                    const float c = p ? v.z : v.x, sn = p ? v.w : v.y;
-                    const float a = y[l], b = y[l + Q];
-                    y[l] = __fmaf_rn(a, c, __fmul_rn(b, sn));
-                    y[l + Q] = __fmaf_rn(b, c, -__fmul_rn(a, sn));
-                }
-            }
+            for (int qq = 0; qq < Q / 2; ++qq) pair_rope_remove<D>(y, qq, rope_tile_entry<D>(stage, hf * (Q / 2) + qq, r));
             pair_encode_row<D, BITS, STRICT>(y, hf, r, sgn, t, active, delta, cur.t0 == cur.t_begin, cur.t_begin,
                                              slice * tpad + t, group, carry, carry_c, idx, coset, scales);
         }

@@ -11,7 +11,7 @@
 // earlier tiles.  The reconstructed fp16 rows are written into a swizzled
 // shared-memory tile and leave by one TMA tensor store per 64 columns, which
 // clips the rows past the end of the slice and the columns past head_dim.
-#include "nq_internal.h"
+#include "nq_decode.cuh"
 
 namespace nq {
 
@@ -39,14 +39,6 @@ __device__ __forceinline__ void load_records(const uint8_t* __restrict__ idx, co
     if (lane < nsch) cp_async16(stage + kRecScale + 16 * lane, scales + row0 * nsc + 8 * lane, 16);
 }
 
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
-    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(map),
-                 "r"(src), "r"(x), "r"(y), "r"(z)
-                 : "memory");
-}
-
-// One record row -> unscaled, inverse-transformed coordinates (before the
-// RoPE re-apply).  `stage` holds the 32-row record tile of the lane's warp.
 template <int D, int BITS>
 __device__ __forceinline__ void decode_row(uint32_t stage, const uint8_t* stage_gen, int lane, int nsc, int gshift,
                                            bool delta, bool first, unsigned (&carry)[PaddedDim<D>::value / 8],
@@ -107,45 +99,7 @@ __device__ __forceinline__ void decode_row(uint32_t stage, const uint8_t* stage_
         carry_c = __shfl_sync(kFull, cw, 31);
     }
 
-    // ---- unpack, unscale: y = (code - offset) * scale  (exact)
-#pragma unroll
-    for (int k = 0; k < NB; ++k) unscale_block<BITS>(blk[k], (cw >> k) & 1u, scf[k / 4], &y[8 * k]);
-
-    // ---- inverse Hadamard: x = H (r * sc)
-    fwht<DP>(y);
-}
-
-// Rotate the pairs (2q, 2q + D/2) and (2q + 1, 2q + 1 + D/2) by +angle;
-// cs = (cos, sin) of both pairs.
-template <int D, int N>
-__device__ __forceinline__ void rope_apply_pairs(float (&y)[N], int q, float4 cs) {
-#pragma unroll
-    for (int p = 0; p < 2; ++p) {
-        const int j = 2 * q + p;
-        const float c = p ? cs.z : cs.x, s = p ? cs.w : cs.y;
-        const float a = y[j], b = y[j + D / 2];
-        y[j] = __fmaf_rn(a, c, -__fmul_rn(b, s));
-        y[j + D / 2] = __fmaf_rn(b, c, __fmul_rn(a, s));
-    }
-}
-
-// fp16 rows -> swizzled shared-memory tile -> TMA tensor store of 32 rows
-// (the map clips rows past the slice end and columns past head_dim).  PENDING
-// = stores of the warp's other output tiles that may still be reading.
-template <int D, int PENDING, int N>
-__device__ __forceinline__ void store_rows(const float (&y)[N], uint32_t ob, int lane, const CUtensorMap* map,
-                                           int t0, int slice) {
-    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(PENDING) : "memory");  // ob is free
-    __syncwarp();
-#pragma unroll
-    for (int q = 0; q < D / 8; ++q) sts128(ob + swz(lane, q), f_to_h8(&y[8 * q]));
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    __syncwarp();
-    if (lane == 0) {
-        tma_store_3d(map, ob, 0, t0, slice);
-        if (D > 64) tma_store_3d(map, ob + 4096, 64, t0, slice);
-        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-    }
+    row_decode_codes<D, BITS>(blk, cw, scf, y);
 }
 
 template <int D, int BITS>
@@ -377,7 +331,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     constexpr int Q = PM::Q;
     constexpr int NBT = PM::NBT;
     constexpr int NSUB = HALF / 32;
-    using C = Code<BITS>;
     using RP = RowPack<BITS, NBT>;
     constexpr int RB = DP * BITS / 8;
     constexpr int RBT = RB / 2;
@@ -388,7 +341,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int hf = lane & 1;
     const int r = lane >> 1;
     const float sgn = hf ? -1.0f : 1.0f;
-    const unsigned negbits = hf ? 0x80008000u : 0u;
     const uint32_t base = (smem_u32(smem) + 1023u) & ~1023u;
     const uint8_t* gbase = smem + (base - smem_u32(smem));
     const uint32_t wbase = base + (threadIdx.x >> 5) * kPairWarpSmem;
@@ -463,59 +415,18 @@ __global__ void __launch_bounds__(kThreads, 2)
             carry_c = __shfl_sync(kFull, cw, 30 + hf);
         }
 
-        // ---- unpack, unscale: y = (code - offset) * scale  (exact)
         float y[HALF];
-#pragma unroll
-        for (int k = 0; k < NBT; ++k) unscale_block<BITS>(blk[k], (cw >> k) & 1u, scf[(8 * k) / 32], &y[8 * k]);
-
-        // ---- inverse Hadamard (textbook order): bits below DP/4 in-thread, bit
-        //      DP/4 in-thread (signed), bit DP/2 by exchange
-#pragma unroll
-        for (int h = 1; h < Q; h *= 2) fwht_stage<HALF>(y, h);
-        stage_signed<HALF>(y, sgn);
-        stage_exchange<HALF>(y);
+        pair_decode_codes<D, BITS>(blk, cw, scf, sgn, y);
 
         // ---- RoPE re-apply on keys: pairs (i, i + D/2) are slots (l, l + Q)
         if (rope != nullptr) {
             const float4* cs = rope + (t < cur.t_end ? t : cur.t_begin);
 #pragma unroll
-            for (int qq = 0; qq < Q / 2; ++qq) {
-                const float4 v = __ldg(cs + int64_t(hf * (Q / 2) + qq) * tokens);
-#pragma unroll
-                for (int p = 0; p < 2; ++p) {
-                    const int l = 2 * qq + p;
-                    const float c = p ? v.z : v.x;
-                    const float s = __fmul_rn(p ? v.w : v.y, sgn);  // odd thread: upper slot negated
-                    const float a = y[l], b = y[l + Q];
-                    y[l] = __fmaf_rn(a, c, -__fmul_rn(b, s));
-                    y[l + Q] = __fmaf_rn(b, c, __fmul_rn(a, s));
-                }
-            }
+            for (int qq = 0; qq < Q / 2; ++qq)
+                pair_rope_apply<D>(y, qq, __ldg(cs + int64_t(hf * (Q / 2) + qq) * tokens), sgn);
         }
 
-        // ---- fp16 rows -> swizzled smem tile -> TMA tensor store (16 rows)
-        const uint32_t ob = outbuf + (i & 1) * kPairTileBytes;
-        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-        __syncwarp();
-#pragma unroll
-        for (int c = 0; c < NBT; ++c) {
-            uint4 v = f_to_h8(&y[8 * c]);
-            if (8 * c >= Q) {
-                v.x ^= negbits;
-                v.y ^= negbits;
-                v.z ^= negbits;
-                v.w ^= negbits;
-            }
-            sts128(ob + swz16(r, PM::chunk(hf, c)), v);
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) {
-            const int z = int(cur.slice);
-            tma_store_3d(&out_map, ob, 0, cur.t0, z);
-            if (D > 64) tma_store_3d(&out_map, ob + 2048, 64, cur.t0, z);
-            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-        }
+        pair_store_rows<D, 1>(y, outbuf + (i & 1) * kPairTileBytes, r, hf, lane, &out_map, cur.t0, int(cur.slice));
         cur.next();
     }
     cp_async_wait<0>();

@@ -48,6 +48,8 @@ int launch_compress_tensor(const LaunchArgs& a, int head_dim, int bits, bool str
 int launch_decompress_tensor(const LaunchArgs& a, int head_dim, int bits, const uint8_t* idx,
                              const uint16_t* coset, const uint16_t* scales, const float* rope,
                              void* x_out);
+int launch_roundtrip_tensor(const LaunchArgs& a, int head_dim, int bits, bool strict, const void* x,
+                            const float* rope, void* x_out);
 
 int launch_e8_nearest(const float* u, float* out, int64_t n_blocks, bool strict, int bits,
                       cudaStream_t stream);

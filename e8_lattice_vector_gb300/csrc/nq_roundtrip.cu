@@ -1,0 +1,311 @@
+// nq_roundtrip.cu -- the round trip in one pass: fp16 rows -> RoPE removal
+// (keys) -> Hadamard -> group scale -> E8 codes -> unscale -> inverse
+// Hadamard -> RoPE re-apply -> fp16 rows, with no compressed intermediate in
+// memory.  The reconstruction equals decompress(compress(x)) bit for bit: the
+// codes, cosets and scales are the compressor's (the temporal delta is
+// lossless and has no effect here) and the decode is the decompressor's.
+//
+// The streaming is the compressor's: fp16 tiles arrive in a shared-memory
+// ring by cp.async; each reconstructed tile is written back into the ring
+// slot its input came from (same swizzled layout the TMA tensor store reads)
+// and leaves by TMA.  A slot is refilled only after the store from it has
+// finished reading.  Tiles are read before they are written and never read
+// again, so the output may alias the input (an in-place round trip).
+#include "nq_decode.cuh"
+#include "nq_encode.cuh"
+
+namespace nq {
+
+constexpr int kRtStages = 3;
+constexpr int kRtRowSmem = kWarpsPerBlock * kRtStages * kTileBytes + 1024;
+constexpr int kRtPairSmem = kWarpsPerBlock * kRtStages * kPairTileBytes + 1024;
+
+// ------------------------------------------------ one thread per row (D = 96)
+
+template <int D, int BITS, bool STRICT>
+__global__ void __launch_bounds__(kThreads, 1)
+    roundtrip_row_kernel(const __half* __restrict__ x, const float4* __restrict__ rope,
+                         const __grid_constant__ CUtensorMap out_map, int64_t slices, int tokens, int group) {
+    constexpr int DP = PaddedDim<D>::value;
+    constexpr int NB = DP / 8;
+    constexpr int NSUB = DP / 32;
+
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int lane = threadIdx.x & 31;
+    const uint32_t ring = ((smem_u32(smem) + 1023u) & ~1023u) + (threadIdx.x >> 5) * (kRtStages * kTileBytes);
+    const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+
+    TileWalk cur(warp, nwarps, slices, tokens, kTileRows);
+    TileWalk pre = cur;
+#pragma unroll
+    for (int s = 0; s < kRtStages - 1; ++s) {
+        if (pre.valid()) {
+            load_tile<D>(x, pre, ring + s * kTileBytes, lane);
+            pre.next();
+        }
+        cp_async_commit();
+    }
+
+    for (int i = 0; cur.valid(); ++i) {
+        cp_async_wait<kRtStages - 2>();  // tile i has landed
+        __syncwarp();
+        const uint32_t stage = ring + (i % kRtStages) * kTileBytes;
+        const int t = cur.t0 + lane;
+
+        float y[DP];
+#pragma unroll
+        for (int q = 0; q < D / 8; ++q) h8_to_f(lds128(stage + swz(lane, q)), &y[8 * q]);
+#pragma unroll
+        for (int j = D; j < DP; ++j) y[j] = 0.0f;
+        // the slot of tile i - 1 is refilled next: its store must have read it
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        __syncwarp();
+        if (pre.valid()) {
+            load_tile<D>(x, pre, ring + ((i + kRtStages - 1) % kRtStages) * kTileBytes, lane);
+            pre.next();
+        }
+        cp_async_commit();
+
+        const float4* cs = rope == nullptr ? nullptr : rope + (t < cur.t_end ? t : cur.t_begin);
+        if (cs != nullptr) {
+#pragma unroll
+            for (int q = 0; q < D / 4; ++q) row_rope_remove<D>(y, q, __ldg(cs + int64_t(q) * tokens));
+        }
+        unsigned short sc[NSUB];
+        unsigned blk[NB];
+        unsigned cw;
+        row_encode_codes<D, BITS, STRICT>(y, group, blk, cw, sc);
+        float scf[NSUB];
+#pragma unroll
+        for (int s = 0; s < NSUB; ++s) scf[s] = __half2float(__ushort_as_half(sc[s]));
+        row_decode_codes<D, BITS>(blk, cw, scf, y);
+        if (cs != nullptr) {
+#pragma unroll
+            for (int q = 0; q < D / 4; ++q) rope_apply_pairs<D>(y, q, __ldg(cs + int64_t(q) * tokens));
+        }
+        store_rows<D, 0>(y, stage, lane, &out_map, cur.t0, int(cur.slice));
+        cur.next();
+    }
+    cp_async_wait<0>();
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// ------------------------------------- two threads per row (D = 64, 128)
+
+// Encode + decode of the thread's half of row r (PairMap slots, RoPE removed).
+template <int D, int BITS, bool STRICT>
+__device__ __forceinline__ void pair_round_trip(float (&y)[D / 2], int hf, float sgn, int group) {
+    constexpr int NBT = PairMap<D>::NBT;
+    constexpr int NSUB = D / 64;
+    unsigned short sc[NSUB];
+    unsigned blk[NBT];
+    unsigned cwl;
+    pair_encode_codes<D, BITS, STRICT>(y, hf, sgn, group, blk, cwl, sc);
+    float scf[NSUB];
+#pragma unroll
+    for (int s = 0; s < NSUB; ++s) scf[s] = __half2float(__ushort_as_half(sc[s]));
+    pair_decode_codes<D, BITS>(blk, cwl, scf, sgn, y);
+}
+
+// Values, and keys without RoPE: a warp per 16-token tile.
+template <int D, int BITS, bool STRICT>
+__global__ void __launch_bounds__(kThreads, 2)
+    roundtrip_pair_kernel(const __half* __restrict__ x, const __grid_constant__ CUtensorMap out_map,
+                          int64_t slices, int tokens, int group) {
+    using PM = PairMap<D>;
+    constexpr int HALF = PM::HALF;
+    constexpr int NBT = PM::NBT;
+    using Walk = TileWalkT<kPairRows>;
+
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int lane = threadIdx.x & 31;
+    const int hf = lane & 1;
+    const int r = lane >> 1;
+    const float sgn = hf ? -1.0f : 1.0f;
+    const uint32_t ring =
+        ((smem_u32(smem) + 1023u) & ~1023u) + (threadIdx.x >> 5) * (kRtStages * kPairTileBytes);
+    const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+
+    Walk cur(warp, nwarps, slices, tokens, kPairRows);
+    Walk pre = cur;
+#pragma unroll
+    for (int s = 0; s < kRtStages - 1; ++s) {
+        if (pre.valid()) {
+            load_pair_tile<D>(x, pre.slice, pre.t0, tokens, ring + s * kPairTileBytes, lane);
+            pre.next();
+        }
+        cp_async_commit();
+    }
+
+    for (int i = 0; cur.valid(); ++i) {
+        cp_async_wait<kRtStages - 2>();
+        __syncwarp();
+        const uint32_t stage = ring + (i % kRtStages) * kPairTileBytes;
+        float y[HALF];
+#pragma unroll
+        for (int c = 0; c < NBT; ++c) h8_to_f(lds128(stage + swz16(r, PM::chunk(hf, c))), &y[8 * c]);
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        __syncwarp();
+        if (pre.valid()) {
+            load_pair_tile<D>(x, pre.slice, pre.t0, tokens,
+                              ring + ((i + kRtStages - 1) % kRtStages) * kPairTileBytes, lane);
+            pre.next();
+        }
+        cp_async_commit();
+
+        pair_round_trip<D, BITS, STRICT>(y, hf, sgn, group);
+        pair_store_rows<D, 0>(y, stage, r, hf, lane, &out_map, cur.t0, int(cur.slice));
+        cur.next();
+    }
+    cp_async_wait<0>();
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Keys with RoPE: 16 warps share the tile's table rows (16 slices at the same
+// tokens), as in the compressor; one block barrier per tile.
+template <int D, int BITS, bool STRICT>
+__global__ void __launch_bounds__(kRopeThreads, 1)
+    roundtrip_pair_rope_kernel(const __half* __restrict__ x, const float4* __restrict__ rope,
+                               const __grid_constant__ CUtensorMap out_map, int64_t slices, int tokens,
+                               int group) {
+    using PM = PairMap<D>;
+    constexpr int HALF = PM::HALF;
+    constexpr int Q = PM::Q;
+    constexpr int NBT = PM::NBT;
+    using RS = RopeStage<D>;
+    using Walk = TileWalkT<kPairRows>;
+
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const uint32_t sbase = (smem_u32(smem) + 1023u) & ~1023u;
+    const int wib = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int hf = lane & 1;
+    const int r = lane >> 1;
+    const float sgn = hf ? -1.0f : 1.0f;
+    const int64_t ngroups = (slices + kRopeWarps - 1) / kRopeWarps;
+
+    Walk cur(blockIdx.x, gridDim.x, ngroups, tokens, kPairRows);
+    Walk pre = cur;
+
+    auto load_stage = [&](const Walk& w, uint32_t stage) {
+        for (int g = threadIdx.x; g < (D / 4) * kPairRows; g += kRopeThreads) {
+            const int q = g / kPairRows, rr = g - q * kPairRows;
+            const int tok = w.t0 + rr;
+            const bool ok = tok < tokens;
+            cp_async16(stage + rope_slot<D>(q, rr), rope + int64_t(q) * tokens + (ok ? tok : 0), ok ? 16 : 0);
+        }
+        const int64_t sl = w.slice * kRopeWarps + wib;
+        if (sl < slices) load_pair_tile<D>(x, sl, w.t0, tokens, stage + RS::TABLE + wib * kPairTileBytes, lane);
+    };
+
+#pragma unroll
+    for (int s = 0; s < kRopeStages - 1; ++s) {
+        if (pre.valid()) {
+            load_stage(pre, sbase + s * RS::BYTES);
+            pre.next();
+        }
+        cp_async_commit();
+    }
+
+    for (int i = 0; cur.valid(); ++i) {
+        cp_async_wait<kRopeStages - 2>();  // this thread's copies of tile i are done
+        // the ring slot about to be refilled held tile i - 1: this warp's store
+        // from it must have finished reading before the barrier releases the refill
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        __syncthreads();
+        if (pre.valid()) {
+            load_stage(pre, sbase + ((i + kRopeStages - 1) % kRopeStages) * RS::BYTES);
+            pre.next();
+        }
+        cp_async_commit();
+        const uint32_t stage = sbase + (i % kRopeStages) * RS::BYTES;
+        const int64_t slice = cur.slice * kRopeWarps + wib;
+        if (slice < slices) {  // warp-uniform
+            const uint32_t tile = stage + RS::TABLE + wib * kPairTileBytes;
+            float y[HALF];
+#pragma unroll
+            for (int c = 0; c < NBT; ++c) h8_to_f(lds128(tile + swz16(r, PM::chunk(hf, c))), &y[8 * c]);
+#pragma unroll
+            for (int qq = 0; qq < Q / 2; ++qq) pair_rope_remove<D>(y, qq, rope_tile_entry<D>(stage, hf * (Q / 2) + qq, r));
+            pair_round_trip<D, BITS, STRICT>(y, hf, sgn, group);
+#pragma unroll
+            for (int qq = 0; qq < Q / 2; ++qq)
+                pair_rope_apply<D>(y, qq, rope_tile_entry<D>(stage, hf * (Q / 2) + qq, r), sgn);
+            __syncwarp();  // every lane has read its input from the tile
+            pair_store_rows<D, 0>(y, tile, r, hf, lane, &out_map, cur.t0, int(slice));
+        }
+        cur.next();
+    }
+    cp_async_wait<0>();
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// ----------------------------------------------------------------- launch
+
+template <typename K>
+static int grid_for(K kern, int smem, int threads, int64_t items) {
+    if (!ensure_smem(reinterpret_cast<const void*>(kern), smem)) return -1;
+    const int cap = grid_capacity_threads(reinterpret_cast<const void*>(kern), smem, threads);
+    if (cap <= 0) return -1;
+    return int(std::min<int64_t>(items, cap));
+}
+
+template <int D, int BITS, bool STRICT>
+static int launch_rt(const LaunchArgs& a, const __half* x, const float4* rope, const CUtensorMap& map) {
+    const int64_t tiles16 = (a.tokens + kPairRows - 1) / kPairRows;
+    if constexpr (D == 96) {
+        auto kern = roundtrip_row_kernel<D, BITS, STRICT>;
+        const int64_t items = a.slices * ((a.tokens + kTileRows - 1) / kTileRows);
+        const int grid = grid_for(kern, kRtRowSmem, kThreads, (items + kWarpsPerBlock - 1) / kWarpsPerBlock);
+        if (grid < 0) return NQ_ERR_CUDA;
+        kern<<<grid, kThreads, kRtRowSmem, a.stream>>>(x, rope, map, a.slices, a.tokens, a.group);
+    } else if (rope != nullptr) {
+        auto kern = roundtrip_pair_rope_kernel<D, BITS, STRICT>;
+        constexpr int smem = RopeStage<D>::SMEM;
+        const int64_t items = (a.slices + kRopeWarps - 1) / kRopeWarps * tiles16;
+        const int grid = grid_for(kern, smem, kRopeThreads, items);
+        if (grid < 0) return NQ_ERR_CUDA;
+        kern<<<grid, kRopeThreads, smem, a.stream>>>(x, rope, map, a.slices, a.tokens, a.group);
+    } else {
+        auto kern = roundtrip_pair_kernel<D, BITS, STRICT>;
+        const int64_t items = a.slices * tiles16;
+        const int grid = grid_for(kern, kRtPairSmem, kThreads, (items + kWarpsPerBlock - 1) / kWarpsPerBlock);
+        if (grid < 0) return NQ_ERR_CUDA;
+        kern<<<grid, kThreads, kRtPairSmem, a.stream>>>(x, map, a.slices, a.tokens, a.group);
+    }
+    return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
+}
+
+template <int D>
+static int dispatch_bits(const LaunchArgs& a, int bits, bool strict, const __half* x, const float4* rope,
+                         const CUtensorMap& map) {
+    switch (bits * 2 + (strict ? 1 : 0)) {
+        case 4: return launch_rt<D, 2, false>(a, x, rope, map);
+        case 5: return launch_rt<D, 2, true>(a, x, rope, map);
+        case 6: return launch_rt<D, 3, false>(a, x, rope, map);
+        case 7: return launch_rt<D, 3, true>(a, x, rope, map);
+        case 8: return launch_rt<D, 4, false>(a, x, rope, map);
+        case 9: return launch_rt<D, 4, true>(a, x, rope, map);
+        default: return NQ_ERR_UNSUPPORTED;
+    }
+}
+
+int launch_roundtrip_tensor(const LaunchArgs& a, int head_dim, int bits, bool strict, const void* x,
+                            const float* rope, void* x_out) {
+    if (a.slices == 0 || a.tokens == 0) return NQ_OK;
+    CUtensorMap map;
+    const int box_rows = head_dim == 96 ? kTileRows : kPairRows;
+    if (!make_row_tile_map(&map, x_out, head_dim, a.tokens, a.slices, box_rows)) return NQ_ERR_CUDA;
+    const __half* xh = static_cast<const __half*>(x);
+    const float4* r = reinterpret_cast<const float4*>(rope);
+    switch (head_dim) {
+        case 64: return dispatch_bits<64>(a, bits, strict, xh, r, map);
+        case 96: return dispatch_bits<96>(a, bits, strict, xh, r, map);
+        case 128: return dispatch_bits<128>(a, bits, strict, xh, r, map);
+        default: return NQ_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace nq

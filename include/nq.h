@@ -143,6 +143,20 @@ int nq_decompress_kv(const void* in, size_t in_bytes, const float* rope_table,
                      const nq_shape* shape, const nq_params* params, void* k_f16_out,
                      void* v_f16_out, void* stream);
 
+/* The round trip in one pass: K and V (device fp16) -> the reconstruction
+ * decompress(compress(.)) written to k_f16_out / v_f16_out (device fp16, same
+ * layout), with no compressed buffer in memory.  This is the method's own use
+ * of the codec: compress_kv_cache(mode="quant_only") quantizes the cache and
+ * hands back the dequantized tensors in place ("E8 walkthrough", quantize()
+ * returns the dequantized point; nexusquant README, usage).  The result equals
+ * nq_decompress_kv(nq_compress_kv(.)) bit for bit (delta_chunk has no effect:
+ * the delta is lossless).  The outputs may alias the inputs (in-place); any
+ * other overlap is an error of the caller.  rope_table as for nq_compress_kv.
+ * Errors: as nq_compress_kv (NQ_ERR_ARG for null or misaligned pointers). */
+int nq_roundtrip_kv(const void* k_f16, const void* v_f16, const float* rope_table,
+                    const nq_shape* shape, const nq_params* params, void* k_f16_out, void* v_f16_out,
+                    void* stream);
+
 /* Nearest point of the E8 codebook for n_blocks 8-float blocks ("E8
  * walkthrough", nearest_point()).  u, out: device float [n_blocks][8].
  * bits = 0: the unbounded lattice (|u| < 2^22 required); bits in 2..4: the

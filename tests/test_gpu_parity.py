@@ -99,6 +99,14 @@ def _round_trip_check(nq, orc, K, V, params, expect_exact_recon=True):
         _assert_recon(gb, r)
         if expect_exact_recon:
             assert _same_values(gb, r)
+    # the one-pass round trip reconstructs the same values
+    K3, V3 = nq.roundtrip_kv(K, V, params, rope)
+    torch.cuda.synchronize()
+    for g3, r in ((K3, kd), (V3, vd)):
+        gb = _bits(g3).reshape(r.shape)
+        _assert_recon(gb, r)
+        if expect_exact_recon:
+            assert _same_values(gb, r)
     return buf
 
 
@@ -257,6 +265,25 @@ def test_short_sequences(nq, orc, T):
     _round_trip_check(nq, orc, K, V, CodecParams(3, 2, 64, False, 32, 1e4))
 
 
+@pytest.mark.parametrize("shape,theta", [((2, 1, 3, 77, 128), 1e4), ((1, 2, 5, 45, 64), 5e5),
+                                         ((1, 1, 4, 70, 96), 1e4), ((1, 1, 2, 33, 128), 0.0)])
+def test_roundtrip_in_place(nq, orc, shape, theta):
+    """nq_roundtrip_kv with the outputs aliasing the inputs."""
+    from e8_lattice_vector_gb300 import CodecParams
+
+    params = CodecParams(key_bits=3, value_bits=2, group_size=64, strict=False, delta_chunk=0, rope_theta=theta)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7)
+    K = (torch.randn(shape, generator=g, device="cuda") * 2).to(torch.float16)
+    V = torch.randn(shape, generator=g, device="cuda").to(torch.float16)
+    rope = nq.RopeTable.build(shape[3], shape[4], theta) if theta > 0 else None
+    K2, V2 = nq.decompress_kv(nq.compress_kv(K, V, params, rope), shape, params, rope)
+    Kc, Vc = K.clone(), V.clone()
+    nq.roundtrip_kv(Kc, Vc, params, rope, K_out=Kc, V_out=Vc)
+    torch.cuda.synchronize()
+    assert bool((Kc == K2).all()) and bool((Vc == V2).all())
+
+
 def test_empty_cache_is_noop(nq):
     from e8_lattice_vector_gb300 import CodecParams
 
@@ -264,6 +291,8 @@ def test_empty_cache_is_noop(nq):
     buf = nq.compress_kv(K, K.clone(), CodecParams(), nq.RopeTable.build(0, 128, 1e4))
     K2, V2 = nq.decompress_kv(buf, K.shape, CodecParams(), nq.RopeTable.build(0, 128, 1e4))
     assert K2.numel() == 0
+    K3, V3 = nq.roundtrip_kv(K, K.clone(), CodecParams(), nq.RopeTable.build(0, 128, 1e4))
+    assert K3.numel() == 0
 
 
 # ------------------------------------------- full-size caches, sampled rows
@@ -337,5 +366,8 @@ def test_full_size_sampled_parity(nq, orc, name):
                 ref[n] = orc.decode_row(idx, cw, sc, D, bits, params.group_size, csr)
             _assert_recon(xr2, ref)
             assert _same_values(xr2, ref)
-        del buf, K2, V2
+        # the one-pass round trip equals decompress(compress(.)) everywhere
+        K3, V3 = nq.roundtrip_kv(K, V, params, rope)
+        assert bool((K3 == K2).all()) and bool((V3 == V2).all())
+        del buf, K2, V2, K3, V3
         torch.cuda.empty_cache()

@@ -113,6 +113,13 @@ def test_compress_validates_before_touching_the_gpu(nq):
     empty = nq.Shape(1, 1, 8, 0, 128)
     assert L.nq_compress_kv(None, None, None, ctypes.byref(empty), ctypes.byref(good), None, 0, None) == 0
     assert L.nq_e8_nearest(None, None, 0, 1, 2, None) == 0
+    # the one-pass round trip validates the same way
+    sh = ctypes.byref(shape)
+    assert L.nq_roundtrip_kv(p16, p16, p16, sh, ctypes.byref(good), None, p16, None) == nq.NQ_ERR_ARG
+    assert L.nq_roundtrip_kv(p16, p16, None, sh, ctypes.byref(good), p16, p16, None) == nq.NQ_ERR_ARG
+    assert L.nq_roundtrip_kv(p16, p16, p16, sh, ctypes.byref(good), p16, p17, None) == nq.NQ_ERR_ARG
+    assert L.nq_roundtrip_kv(p16, p16, p16, sh, ctypes.byref(bad), p16, p16, None) == nq.NQ_ERR_UNSUPPORTED
+    assert L.nq_roundtrip_kv(None, None, None, ctypes.byref(empty), ctypes.byref(good), None, None, None) == 0
     assert L.nq_e8_nearest(p16, p16, 5, 1, 5, None) == nq.NQ_ERR_UNSUPPORTED
     assert L.nq_e8_nearest(p16, p16, -1, 1, 2, None) == nq.NQ_ERR_ARG
 
