@@ -4,8 +4,8 @@ The codec runs in libnq (hand-written CUDA, C ABI in include/nq.h); this
 package is its thin Python binding.  Nothing here computes the method on the
 CPU: when the library is missing, calls raise.
 """
-from .codec import (CodecParams, RopeTable, compress_kv, decompress_kv, e8_nearest, plan, roundtrip_kv,
-                    sections, shape_of)
+from .codec import (CodecParams, RopeTable, code_histogram, compress_kv, decompress_kv, e8_nearest, plan,
+                    roundtrip_kv, sections, shape_of)
 
-__all__ = ["CodecParams", "RopeTable", "compress_kv", "decompress_kv", "e8_nearest", "plan", "roundtrip_kv",
-           "sections", "shape_of"]
+__all__ = ["CodecParams", "RopeTable", "code_histogram", "compress_kv", "decompress_kv", "e8_nearest", "plan",
+           "roundtrip_kv", "sections", "shape_of"]

@@ -12,6 +12,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libnq.so")
 
 NQ_OK, NQ_ERR_ARG, NQ_ERR_UNSUPPORTED, NQ_ERR_SIZE, NQ_ERR_CUDA = range(5)
+NQ_HIST_BINS = 274
 FORMAT_VERSION = 1
 
 
@@ -50,6 +51,8 @@ SIGNATURES = {
     "nq_roundtrip_kv": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                        ctypes.POINTER(Shape), ctypes.POINTER(Params), ctypes.c_void_p,
                                        ctypes.c_void_p, ctypes.c_void_p]),
+    "nq_code_histogram": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(Shape),
+                                         ctypes.POINTER(Params), ctypes.c_void_p, ctypes.c_void_p]),
     "nq_e8_nearest": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
                                      ctypes.c_int, ctypes.c_void_p]),
     "nq_strerror": (ctypes.c_char_p, [ctypes.c_int]),

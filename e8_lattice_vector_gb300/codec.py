@@ -182,6 +182,22 @@ def roundtrip_kv(K, V, params, rope=None, K_out=None, V_out=None):
     return K_out, V_out
 
 
+def code_histogram(buf, shape, params, counts=None):
+    """Symbol counts of a compressed buffer: int64 device tensor [2, 274] (K, V)
+    of field values [0, 16), idx bytes [16, 272) and coset bits [272, 274)."""
+    shape = tuple(int(v) for v in shape)
+    if counts is None:
+        counts = torch.empty((2, _lib.NQ_HIST_BINS), dtype=torch.int64, device=buf.device)
+    if not (counts.is_cuda and counts.dtype == torch.int64 and counts.is_contiguous()
+            and counts.numel() == 2 * _lib.NQ_HIST_BINS):
+        raise ValueError("counts must be a contiguous int64 CUDA tensor of 2 * 274 entries")
+    st = _lib.lib().nq_code_histogram(ctypes_void(buf.data_ptr()), int(buf.numel()), ctypes_ref(_cshape(shape)),
+                                      ctypes_ref(params.c()), ctypes_void(counts.data_ptr()),
+                                      _stream_handle(buf.device))
+    _lib.check("nq_code_histogram", st)
+    return counts
+
+
 def e8_nearest(u, strict, bits):
     """Nearest E8 codebook point of each 8-block of a float32 CUDA tensor [..., 8]."""
     if not (u.is_cuda and u.dtype == torch.float32 and u.is_contiguous() and u.shape[-1] == 8):

@@ -274,6 +274,33 @@ int nq_roundtrip_kv(const void* k_f16, const void* v_f16, const float* rope_tabl
                                        nullptr, v_f16_out);
 }
 
+int nq_code_histogram(const void* in, size_t in_bytes, const nq_shape* shape, const nq_params* params,
+                      uint64_t* counts, void* stream) {
+    int st = nq::check(shape, params);
+    if (st != NQ_OK) return st;
+    nq_layout L;
+    nq::make_layout(shape, params, &L);
+    if (!counts || (reinterpret_cast<uintptr_t>(counts) & 7u) != 0) return NQ_ERR_ARG;
+    if (L.rows > 0 && (!in || !nq::aligned16(in))) return NQ_ERR_ARG;
+    if (in_bytes < L.total_bytes) return NQ_ERR_SIZE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(counts, 0, 2 * NQ_HIST_BINS * sizeof(uint64_t), s) != cudaSuccess) return NQ_ERR_CUDA;
+    if (L.rows == 0) return NQ_OK;
+    nq::LaunchArgs a;
+    a.slices = int64_t(shape->layers) * shape->batch * shape->kv_heads;
+    a.tokens = shape->tokens;
+    a.tpad = int(L.tokens_padded);
+    a.group = params->group_size;
+    a.delta_chunk = params->delta_chunk;
+    a.stream = s;
+    const uint8_t* base = static_cast<const uint8_t*>(in);
+    st = nq::launch_code_histogram(a, int(L.padded_dim), params->key_bits, base + L.k_idx,
+                                   reinterpret_cast<const uint16_t*>(base + L.k_coset), counts);
+    if (st != NQ_OK) return st;
+    return nq::launch_code_histogram(a, int(L.padded_dim), params->value_bits, base + L.v_idx,
+                                     reinterpret_cast<const uint16_t*>(base + L.v_coset), counts + NQ_HIST_BINS);
+}
+
 int nq_decompress_kv(const void* in, size_t in_bytes, const float* rope_table,
                      const nq_shape* shape, const nq_params* params, void* k_f16_out,
                      void* v_f16_out, void* stream) {

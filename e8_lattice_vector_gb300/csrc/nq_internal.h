@@ -50,6 +50,8 @@ int launch_decompress_tensor(const LaunchArgs& a, int head_dim, int bits, const 
                              void* x_out);
 int launch_roundtrip_tensor(const LaunchArgs& a, int head_dim, int bits, bool strict, const void* x,
                             const float* rope, void* x_out);
+int launch_code_histogram(const LaunchArgs& a, int padded_dim, int bits, const uint8_t* idx,
+                          const uint16_t* coset, uint64_t* counts);
 
 int launch_e8_nearest(const float* u, float* out, int64_t n_blocks, bool strict, int bits,
                       cudaStream_t stream);

@@ -157,6 +157,25 @@ int nq_roundtrip_kv(const void* k_f16, const void* v_f16, const float* rope_tabl
                     const nq_shape* shape, const nq_params* params, void* k_f16_out, void* v_f16_out,
                     void* stream);
 
+/* Symbol statistics of a compressed buffer, for judging how much an entropy
+ * coder could still take off (the pages pack the indices, delta-code them
+ * along tokens and hand them to zstd: "E8 walkthrough", "Bit Rate
+ * Accounting"; "Negative results", delta coding entry).  Per tensor
+ * (K first, then V) NQ_HIST_BINS 64-bit counters:
+ *   [0, 16)    occurrences of each b-bit field value in the idx section (the
+ *              temporal-delta symbols when delta_chunk > 0; values >= 2^b
+ *              stay zero)
+ *   [16, 272)  occurrences of each byte value in the idx section
+ *   [272]      blocks in the integer coset (coset bit 0), [273] in the
+ *              half-integer coset (coset bit 1)
+ * Only the record rows of real tokens count, not the padding rows.
+ * in: device buffer from nq_compress_kv with this shape and params (in_bytes
+ * >= nq_plan().total_bytes).  counts: device uint64[2 * NQ_HIST_BINS],
+ * overwritten (zeroed on the stream, then accumulated); 8-byte aligned. */
+#define NQ_HIST_BINS 274
+int nq_code_histogram(const void* in, size_t in_bytes, const nq_shape* shape, const nq_params* params,
+                      uint64_t* counts, void* stream);
+
 /* Nearest point of the E8 codebook for n_blocks 8-float blocks ("E8
  * walkthrough", nearest_point()).  u, out: device float [n_blocks][8].
  * bits = 0: the unbounded lattice (|u| < 2^22 required); bits in 2..4: the

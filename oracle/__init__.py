@@ -44,6 +44,7 @@ def lib():
             "orc_undelta_row": (None, [_P, _P, _P, ctypes.c_uint16, _I, _I]),
             "orc_compress_tensor": (None, [_P, _I64, _I, _I, _P, _I, _I, _I, _I, _P, _P, _P]),
             "orc_decompress_tensor": (None, [_P, _P, _P, _I64, _I, _I, _P, _I, _I, _I, _P]),
+            "orc_code_histogram": (None, [_P, _P, _I64, _I, _I, _P]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(L, name)
@@ -191,3 +192,14 @@ def undelta_row(idx, coset, prev_idx, prev_coset, dp, bits):
     c = np.array([coset], dtype=np.uint16)
     lib().orc_undelta_row(_ptr(idx), _ptr(c), _ptr(_c(prev_idx, np.uint8)), int(prev_coset), int(dp), int(bits))
     return idx, int(c[0])
+
+
+def code_histogram(idx, coset, head_dim, bits):
+    """Counts (274 uint64) of field values, idx bytes and coset bits over the
+    record rows idx [rows, Dp*b/8], coset [rows]."""
+    idx = _c(idx, np.uint8)
+    coset = _c(coset, np.uint16)
+    counts = np.zeros(274, dtype=np.uint64)
+    rows = idx.shape[0] if idx.ndim == 2 else 0
+    lib().orc_code_histogram(_ptr(idx), _ptr(coset), int(rows), padded_dim(head_dim), int(bits), _ptr(counts))
+    return counts

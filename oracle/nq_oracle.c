@@ -380,3 +380,21 @@ void orc_decompress_tensor(const uint8_t* idx, const uint16_t* coset, const uint
         }
     }
 }
+
+/* Symbol statistics of compressed rows, for the entropy report (the pages
+ * delta-code the packed indices and hand them to an entropy coder: "E8
+ * walkthrough", "Bit Rate Accounting").  counts[274]: [0, 16) field values,
+ * [16, 272) idx bytes, [272] integer-coset blocks, [273] half-coset blocks.
+ * Plain counting over every field, byte and block of `rows` record rows. */
+void orc_code_histogram(const uint8_t* idx, const uint16_t* coset, int64_t rows, int dp, int bits,
+                        uint64_t* counts) {
+    size_t rb = (size_t)dp * bits / 8;
+    int nb = dp / 8;
+    for (int i = 0; i < 274; ++i) counts[i] = 0;
+    for (int64_t r = 0; r < rows; ++r) {
+        const uint8_t* row = idx + (size_t)r * rb;
+        for (int i = 0; i < dp; ++i) counts[get_field(row, i, bits)] += 1;
+        for (size_t b = 0; b < rb; ++b) counts[16 + row[b]] += 1;
+        for (int k = 0; k < nb; ++k) counts[272 + ((coset[r] >> k) & 1u)] += 1;
+    }
+}

@@ -95,6 +95,11 @@ void orc_decompress_tensor(const uint8_t* idx, const uint16_t* coset, const uint
                            int64_t slices, int tokens, int head_dim, const float* cs, int bits,
                            int group, int delta_chunk, uint16_t* x_out);
 
+/* Counts of field values [0, 16), idx bytes [16, 272) and coset bits
+ * [272], [273] over `rows` record rows; counts: 274 entries, overwritten. */
+void orc_code_histogram(const uint8_t* idx, const uint16_t* coset, int64_t rows, int dp, int bits,
+                        uint64_t* counts);
+
 #ifdef __cplusplus
 }
 #endif

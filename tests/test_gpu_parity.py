@@ -99,6 +99,10 @@ def _round_trip_check(nq, orc, K, V, params, expect_exact_recon=True):
         _assert_recon(gb, r)
         if expect_exact_recon:
             assert _same_values(gb, r)
+    # symbol statistics of the buffer equal the oracle's counts over its records
+    counts = nq.code_histogram(buf, shape, params).cpu().numpy().astype(np.uint64)
+    for n, (ref, bits) in enumerate(((k_ref, params.key_bits), (v_ref, params.value_bits))):
+        assert np.array_equal(counts[n], orc.code_histogram(ref[0], ref[1], D, bits)), ("histogram", n)
     # the one-pass round trip reconstructs the same values
     K3, V3 = nq.roundtrip_kv(K, V, params, rope)
     torch.cuda.synchronize()

@@ -113,6 +113,12 @@ def test_compress_validates_before_touching_the_gpu(nq):
     empty = nq.Shape(1, 1, 8, 0, 128)
     assert L.nq_compress_kv(None, None, None, ctypes.byref(empty), ctypes.byref(good), None, 0, None) == 0
     assert L.nq_e8_nearest(None, None, 0, 1, 2, None) == 0
+    # the histogram validates before its first CUDA call
+    cnt = ctypes.c_void_p(64)
+    assert L.nq_code_histogram(p16, 1 << 30, sh := ctypes.byref(shape), ctypes.byref(good), None, None) == nq.NQ_ERR_ARG
+    assert L.nq_code_histogram(p16, 1 << 30, sh, ctypes.byref(good), ctypes.c_void_p(12), None) == nq.NQ_ERR_ARG
+    assert L.nq_code_histogram(p17, 1 << 30, sh, ctypes.byref(good), cnt, None) == nq.NQ_ERR_ARG
+    assert L.nq_code_histogram(p16, 100, sh, ctypes.byref(good), cnt, None) == nq.NQ_ERR_SIZE
     # the one-pass round trip validates the same way
     sh = ctypes.byref(shape)
     assert L.nq_roundtrip_kv(p16, p16, p16, sh, ctypes.byref(good), None, p16, None) == nq.NQ_ERR_ARG

@@ -464,3 +464,58 @@ def test_decode_saturates_at_fp16_max(orc):
         idx, cw, sc = orc.encode_row(x, 128, bits, 64, 1)
         xh = orc.decode_row(idx, cw, sc, 128, bits, 64).view(np.float16)
         assert np.all(np.isfinite(xh)) and np.max(np.abs(xh.astype(np.float64))) <= 65504.0
+
+
+# ------------------------------------------------ symbol statistics (report)
+
+
+def _pack_fields(fields, bits):
+    """LSB-first packing of b-bit fields (field i at bit i*b), written out here
+    independently of the oracle."""
+    nbits = len(fields) * bits
+    out = np.zeros((nbits + 7) // 8, dtype=np.uint8)
+    for i, f in enumerate(fields):
+        for q in range(bits):
+            if (int(f) >> q) & 1:
+                b = i * bits + q
+                out[b >> 3] |= np.uint8(1 << (b & 7))
+    return out
+
+
+def test_code_histogram_hand_built_rows(orc):
+    """Rows whose field, byte and coset-bit counts are known by construction."""
+    # b = 2, Dp = 64: fields 0,1,2,3 repeating -> every byte is 0b11100100
+    idx = np.full((3, 16), 0xE4, np.uint8)
+    coset = np.array([0x00FF, 0x0000, 0x000F], np.uint16)
+    c = orc.code_histogram(idx, coset, 64, 2)
+    assert list(c[:4]) == [48, 48, 48, 48] and not c[4:16].any()
+    assert c[16 + 0xE4] == 48 and c[16:272].sum() == 48
+    assert list(c[272:274]) == [12, 12]  # 8 + 0 + 4 half-coset blocks of 24
+    # b = 3, Dp = 128: field i = i mod 8, fields straddle byte boundaries
+    row = _pack_fields([i % 8 for i in range(128)], 3)
+    c = orc.code_histogram(row[None, :], np.array([0xAAAA], np.uint16), 128, 3)
+    assert list(c[:8]) == [16] * 8 and not c[8:16].any()
+    assert c[16:272].sum() == 48
+    # the byte pattern of 8 fields 0..7 (24 bits) repeats every 3 bytes
+    assert all(c[16 + int(row[j])] == 16 for j in range(3))
+    assert list(c[272:274]) == [8, 8]
+
+
+def test_code_histogram_totals_on_compressed_rows(orc):
+    rng = np.random.default_rng(21)
+    for D, bits in ((128, 2), (96, 3), (64, 4)):
+        x = rng.normal(size=(2, 40, D)).astype(np.float16).view(np.uint16)
+        idx, coset, _ = orc.compress_tensor(x, 40, D, bits, 32, 1, 32)
+        c = orc.code_histogram(idx, coset, D, bits)
+        dp = orc.padded_dim(D)
+        assert c[:16].sum() == 80 * dp and c[16:272].sum() == 80 * dp * bits // 8
+        assert c[272:274].sum() == 80 * dp // 8
+        assert not c[1 << bits:16].any()
+
+
+def test_entropy_bits_closed_forms():
+    from e8_lattice_vector_gb300.entropy import entropy_bits
+
+    assert entropy_bits([5, 5, 5, 5]) == 2.0
+    assert entropy_bits([7, 0, 0]) == 0.0
+    assert abs(entropy_bits([1, 3]) - (2 - 0.75 * np.log2(3))) < 1e-12
