@@ -4,8 +4,10 @@ The codec runs in libnq (hand-written CUDA, C ABI in include/nq.h); this
 package is its thin Python binding.  Nothing here computes the method on the
 CPU: when the library is missing, calls raise.
 """
-from .codec import (CodecParams, RopeTable, code_histogram, compress_kv, decompress_kv, e8_nearest, plan,
-                    roundtrip_kv, sections, shape_of)
+from .codec import (CodecParams, RopeTable, code_histogram, compress_kv, compress_kv_layers, decompress_kv,
+                    decompress_kv_layers, e8_nearest, layer_profile, plan, plan_layers, roundtrip_kv,
+                    roundtrip_kv_layers, sections, shape_of)
 
-__all__ = ["CodecParams", "RopeTable", "code_histogram", "compress_kv", "decompress_kv", "e8_nearest", "plan",
-           "roundtrip_kv", "sections", "shape_of"]
+__all__ = ["CodecParams", "RopeTable", "code_histogram", "compress_kv", "compress_kv_layers", "decompress_kv",
+           "decompress_kv_layers", "e8_nearest", "layer_profile", "plan", "plan_layers", "roundtrip_kv",
+           "roundtrip_kv_layers", "sections", "shape_of"]

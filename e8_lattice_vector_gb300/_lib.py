@@ -38,6 +38,13 @@ class Layout(ctypes.Structure):
 
 
 # name -> (restype, argtypes); the exported C ABI, in header order
+class LayerBits(ctypes.Structure):
+    _fields_ = [("key_bits", ctypes.c_int32), ("value_bits", ctypes.c_int32)]
+
+
+_LB = ctypes.POINTER(LayerBits)
+_U64P = ctypes.POINTER(ctypes.c_uint64)
+
 SIGNATURES = {
     "nq_plan": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Params), ctypes.POINTER(Layout)]),
     "nq_rope_table": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
@@ -51,6 +58,16 @@ SIGNATURES = {
     "nq_roundtrip_kv": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                        ctypes.POINTER(Shape), ctypes.POINTER(Params), ctypes.c_void_p,
                                        ctypes.c_void_p, ctypes.c_void_p]),
+    "nq_plan_layers": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Params), _LB, _U64P, _U64P]),
+    "nq_compress_kv_layers": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                             ctypes.POINTER(Shape), ctypes.POINTER(Params), _LB, ctypes.c_void_p,
+                                             ctypes.c_size_t, ctypes.c_void_p]),
+    "nq_decompress_kv_layers": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                                               ctypes.POINTER(Shape), ctypes.POINTER(Params), _LB, ctypes.c_void_p,
+                                               ctypes.c_void_p, ctypes.c_void_p]),
+    "nq_roundtrip_kv_layers": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                              ctypes.POINTER(Shape), ctypes.POINTER(Params), _LB, ctypes.c_void_p,
+                                              ctypes.c_void_p, ctypes.c_void_p]),
     "nq_code_histogram": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(Shape),
                                          ctypes.POINTER(Params), ctypes.c_void_p, ctypes.c_void_p]),
     "nq_e8_nearest": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,

@@ -15,7 +15,7 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libnq.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["nq_api.cu", "nq_compress.cu", "nq_decompress.cu", "nq_roundtrip.cu", "nq_stats.cu"]
+SOURCES = ["nq_api.cu", "nq_compress.cu", "nq_decompress.cu", "nq_roundtrip.cu", "nq_stats.cu", "nq_layers.cu"]
 HEADERS = ["nq_device.cuh", "nq_internal.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -182,6 +182,89 @@ def roundtrip_kv(K, V, params, rope=None, K_out=None, V_out=None):
     return K_out, V_out
 
 
+def _layer_table(layer_bits, layers):
+    lb = list(layer_bits)
+    if len(lb) != layers:
+        raise ValueError("layer_bits needs one (key_bits, value_bits) entry per layer")
+    arr = (_lib.LayerBits * max(layers, 1))()
+    for i, (kb, vb) in enumerate(lb):
+        arr[i].key_bits, arr[i].value_bits = int(kb), int(vb)
+    return arr
+
+
+def layer_profile(layers, key_bits=3, value_bits=2, protect_boundary=0):
+    """A per-layer table: the first and last `protect_boundary` layers kept in
+    fp16 ((0, 0)), the others at (key_bits, value_bits)."""
+    keep = set(range(min(protect_boundary, layers))) | set(range(max(layers - protect_boundary, 0), layers))
+    return [(0, 0) if l in keep else (key_bits, value_bits) for l in range(layers)]
+
+
+def plan_layers(shape, params, layer_bits):
+    """(offsets per layer, total bytes) of the per-layer buffer."""
+    shape = tuple(int(v) for v in shape)
+    table = _layer_table(layer_bits, shape[0])
+    offs = (ctypes.c_uint64 * max(shape[0], 1))()
+    total = ctypes.c_uint64(0)
+    st = _lib.lib().nq_plan_layers(ctypes_ref(_cshape(shape)), ctypes_ref(params.c()), table, offs,
+                                   ctypes.byref(total))
+    _lib.check("nq_plan_layers", st)
+    return [int(offs[i]) for i in range(shape[0])], int(total.value)
+
+
+def compress_kv_layers(K, V, params, layer_bits, rope=None, out=None):
+    """Compress with a per-layer table of (key_bits, value_bits); (0, 0) keeps
+    a layer in fp16.  Returns (or fills) the uint8 device buffer."""
+    _check_kv(K, "K")
+    _check_kv(V, "V")
+    shape = shape_of(K)
+    if shape_of(V) != shape:
+        raise ValueError("K and V shapes differ")
+    _, total = plan_layers(shape, params, layer_bits)
+    if out is None:
+        out = torch.empty(max(total, 16), dtype=torch.uint8, device=K.device)
+    rp = _rope_ptr(rope, params, shape[3], shape[4])
+    st = _lib.lib().nq_compress_kv_layers(ctypes_void(K.data_ptr()), ctypes_void(V.data_ptr()), rp,
+                                          ctypes_ref(_cshape(shape)), ctypes_ref(params.c()),
+                                          _layer_table(layer_bits, shape[0]), ctypes_void(out.data_ptr()),
+                                          int(out.numel()), _stream_handle(K.device))
+    _lib.check("nq_compress_kv_layers", st)
+    return out
+
+
+def decompress_kv_layers(buf, shape, params, layer_bits, rope=None, K_out=None, V_out=None):
+    shape = tuple(int(v) for v in shape)
+    if K_out is None:
+        K_out = torch.empty(shape, dtype=torch.float16, device=buf.device)
+    if V_out is None:
+        V_out = torch.empty(shape, dtype=torch.float16, device=buf.device)
+    _check_kv(K_out, "K_out")
+    _check_kv(V_out, "V_out")
+    rp = _rope_ptr(rope, params, shape[3], shape[4])
+    st = _lib.lib().nq_decompress_kv_layers(ctypes_void(buf.data_ptr()), int(buf.numel()), rp,
+                                            ctypes_ref(_cshape(shape)), ctypes_ref(params.c()),
+                                            _layer_table(layer_bits, shape[0]), ctypes_void(K_out.data_ptr()),
+                                            ctypes_void(V_out.data_ptr()), _stream_handle(buf.device))
+    _lib.check("nq_decompress_kv_layers", st)
+    return K_out, V_out
+
+
+def roundtrip_kv_layers(K, V, params, layer_bits, rope=None, K_out=None, V_out=None):
+    _check_kv(K, "K")
+    _check_kv(V, "V")
+    shape = shape_of(K)
+    K_out = torch.empty_like(K) if K_out is None else K_out
+    V_out = torch.empty_like(V) if V_out is None else V_out
+    _check_kv(K_out, "K_out")
+    _check_kv(V_out, "V_out")
+    rp = _rope_ptr(rope, params, shape[3], shape[4])
+    st = _lib.lib().nq_roundtrip_kv_layers(ctypes_void(K.data_ptr()), ctypes_void(V.data_ptr()), rp,
+                                           ctypes_ref(_cshape(shape)), ctypes_ref(params.c()),
+                                           _layer_table(layer_bits, shape[0]), ctypes_void(K_out.data_ptr()),
+                                           ctypes_void(V_out.data_ptr()), _stream_handle(K.device))
+    _lib.check("nq_roundtrip_kv_layers", st)
+    return K_out, V_out
+
+
 def code_histogram(buf, shape, params, counts=None):
     """Symbol counts of a compressed buffer: int64 device tensor [2, 274] (K, V)
     of field values [0, 16), idx bytes [16, 272) and coset bits [272, 274)."""

@@ -157,6 +157,42 @@ int nq_roundtrip_kv(const void* k_f16, const void* v_f16, const float* rope_tabl
                     const nq_shape* shape, const nq_params* params, void* k_f16_out, void* v_f16_out,
                     void* stream);
 
+/* Per-layer bit widths ("graduated" profiles that spend more bits on some
+ * layers) and layers kept in fp16 (boundary-layer protection): nexusquant
+ * README, configuration table, per-layer settings.  One entry per layer:
+ * key_bits, value_bits in 2..4, or both 0 to keep that layer's K and V as
+ * they are.  The shared nq_params supply group_size, strict, delta_chunk and
+ * rope_theta (its key_bits / value_bits must be valid and are otherwise
+ * unused).  The buffer holds one part per layer at offsets[l] (256-byte
+ * aligned): the nq_compress_kv buffer of that layer alone (shape with
+ * layers = 1 and the layer's bit widths), or the layer's fp16 K followed by its
+ * fp16 V.  Host-side loops over the single-layer entry points, asynchronous on
+ * the stream; errors as those (a layer with one of its bit widths 0 is
+ * NQ_ERR_UNSUPPORTED). */
+typedef struct {
+    int32_t key_bits, value_bits;
+} nq_layer_bits;
+
+/* offsets: caller-owned host array of shape->layers entries; *total_bytes:
+ * the buffer size.  Host only. */
+int nq_plan_layers(const nq_shape* shape, const nq_params* params, const nq_layer_bits* per_layer,
+                   uint64_t* offsets, uint64_t* total_bytes);
+/* K, V (device fp16, layout above) -> `out` (device, out_bytes >= total).
+ * per_layer: host array of shape->layers entries. */
+int nq_compress_kv_layers(const void* k_f16, const void* v_f16, const float* rope_table,
+                          const nq_shape* shape, const nq_params* params, const nq_layer_bits* per_layer,
+                          void* out, size_t out_bytes, void* stream);
+/* The inverse of nq_compress_kv_layers (same shape, params and table). */
+int nq_decompress_kv_layers(const void* in, size_t in_bytes, const float* rope_table,
+                            const nq_shape* shape, const nq_params* params,
+                            const nq_layer_bits* per_layer, void* k_f16_out, void* v_f16_out,
+                            void* stream);
+/* nq_roundtrip_kv per layer; kept layers are copied (nothing to do in place). */
+int nq_roundtrip_kv_layers(const void* k_f16, const void* v_f16, const float* rope_table,
+                           const nq_shape* shape, const nq_params* params,
+                           const nq_layer_bits* per_layer, void* k_f16_out, void* v_f16_out,
+                           void* stream);
+
 /* Symbol statistics of a compressed buffer, for judging how much an entropy
  * coder could still take off (the pages pack the indices, delta-code them
  * along tokens and hand them to zstd: "E8 walkthrough", "Bit Rate

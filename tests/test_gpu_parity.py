@@ -288,6 +288,47 @@ def test_roundtrip_in_place(nq, orc, shape, theta):
     assert bool((Kc == K2).all()) and bool((Vc == V2).all())
 
 
+def test_per_layer_bits_and_kept_layers(nq, orc):
+    """A per-layer table with kept (fp16) layers and mixed bit widths: every
+    compressed part equals the oracle's compression of that layer alone, kept
+    parts are the layer's bytes, and both directions reproduce the oracle."""
+    from e8_lattice_vector_gb300 import CodecParams
+
+    shape = (5, 1, 3, 77, 128)
+    table = [(0, 0), (3, 2), (2, 2), (4, 3), (0, 0)]
+    params = CodecParams(3, 2, 64, True, 64, 1e4)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(11)
+    K = (torch.randn(shape, generator=g, device="cuda") * 3).to(torch.float16)
+    V = torch.randn(shape, generator=g, device="cuda").to(torch.float16)
+    rope = nq.RopeTable.build(shape[3], shape[4], params.rope_theta)
+    buf = nq.compress_kv_layers(K, V, params, table, rope)
+    offs, total = nq.plan_layers(shape, params, table)
+    K2, V2 = nq.decompress_kv_layers(buf, shape, params, table, rope)
+    K3, V3 = nq.roundtrip_kv_layers(K, V, params, table, rope)
+    torch.cuda.synchronize()
+    one = (1,) + shape[1:]
+    raw = K[0].numel() * 2
+    for l, (kb, vb) in enumerate(table):
+        part = buf[offs[l]:]
+        if kb == 0:
+            assert torch.equal(part[:raw], K[l].contiguous().view(-1).view(torch.uint8))
+            assert torch.equal(part[raw:2 * raw], V[l].contiguous().view(-1).view(torch.uint8))
+            assert torch.equal(K2[l], K[l]) and torch.equal(V2[l], V[l]) and torch.equal(K3[l], K[l])
+            continue
+        p = CodecParams(kb, vb, params.group_size, params.strict, params.delta_chunk, params.rope_theta)
+        got = _gpu_sections(nq, part, one, p)
+        k_ref, v_ref, cs = _oracle_compress(orc, K[l:l + 1], V[l:l + 1], p)
+        for name, ref in (("k", k_ref), ("v", v_ref)):
+            for a, b in zip(got[name], ref):
+                assert np.array_equal(a, b), (l, name)
+        kd = orc.decompress_tensor(*k_ref, 3, 77, 128, kb, 64, params.delta_chunk, cs)
+        vd = orc.decompress_tensor(*v_ref, 3, 77, 128, vb, 64, params.delta_chunk, None)
+        for out2, out3, ref in ((K2[l], K3[l], kd), (V2[l], V3[l], vd)):
+            assert _same_values(_bits(out2).reshape(ref.shape), ref)
+            assert _same_values(_bits(out3).reshape(ref.shape), ref)
+
+
 def test_empty_cache_is_noop(nq):
     from e8_lattice_vector_gb300 import CodecParams
 

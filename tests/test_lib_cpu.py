@@ -160,3 +160,45 @@ def test_package_has_no_cpu_path():
                 with open(os.path.join(dirpath, f)) as fh:
                     src = fh.read()
                 assert "import oracle" not in src and "from oracle" not in src and "nq_oracle" not in src, f
+
+
+def test_plan_layers_parts(nq):
+    """One 256-aligned part per layer: the single-layer buffer of the layer's bit
+    widths, or the layer's K and V in fp16."""
+    import e8_lattice_vector_gb300 as pkg
+    from e8_lattice_vector_gb300 import CodecParams
+
+    shape = (5, 2, 3, 77, 96)
+    p = CodecParams(3, 2, 64, False, 64, 1e4)
+    table = [(0, 0), (3, 2), (2, 2), (4, 3), (0, 0)]
+    offs, total = pkg.plan_layers(shape, p, table)
+    one = (1,) + shape[1:]
+    raw = 2 * 2 * 3 * 77 * 96 * 2
+    expect, off = [], 0
+    for kb, vb in table:
+        expect.append(off)
+        size = raw if kb == 0 else int(pkg.plan(one, CodecParams(kb, vb, 64, False, 64, 1e4)).total_bytes)
+        off = (off + size + 255) // 256 * 256
+    assert offs == expect and total == off
+    assert pkg.layer_profile(6, 3, 2, protect_boundary=2) == [(0, 0), (0, 0), (3, 2), (3, 2), (0, 0), (0, 0)]
+
+
+def test_layers_validate_before_touching_the_gpu(nq):
+    L = nq.lib()
+    shape = nq.Shape(2, 1, 8, 64, 128)
+    good = nq.Params(2, 2, 64, 0, 0, 1e4)
+    offs = (ctypes.c_uint64 * 2)()
+    total = ctypes.c_uint64()
+    ok = (nq.LayerBits * 2)(nq.LayerBits(3, 2), nq.LayerBits(0, 0))
+    half = (nq.LayerBits * 2)(nq.LayerBits(3, 0), nq.LayerBits(2, 2))
+    sh, pr = ctypes.byref(shape), ctypes.byref(good)
+    assert L.nq_plan_layers(sh, pr, ok, offs, ctypes.byref(total)) == 0 and total.value > 0
+    assert L.nq_plan_layers(sh, pr, half, offs, ctypes.byref(total)) == nq.NQ_ERR_UNSUPPORTED
+    assert L.nq_plan_layers(sh, pr, None, offs, ctypes.byref(total)) == nq.NQ_ERR_ARG
+    p16 = ctypes.c_void_p(16)
+    assert L.nq_compress_kv_layers(None, p16, p16, sh, pr, ok, p16, 1 << 30, None) == nq.NQ_ERR_ARG
+    assert L.nq_compress_kv_layers(p16, p16, p16, sh, pr, ok, p16, 100, None) == nq.NQ_ERR_SIZE
+    assert L.nq_decompress_kv_layers(p16, 100, p16, sh, pr, ok, p16, p16, None) == nq.NQ_ERR_SIZE
+    assert L.nq_roundtrip_kv_layers(p16, p16, p16, sh, pr, half, p16, p16, None) == nq.NQ_ERR_UNSUPPORTED
+    empty = nq.Shape(0, 1, 8, 64, 128)
+    assert L.nq_compress_kv_layers(None, None, None, ctypes.byref(empty), pr, None, None, 0, None) == 0
