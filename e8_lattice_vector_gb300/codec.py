@@ -25,12 +25,12 @@ class CodecParams:
     key_bits: int = 2
     value_bits: int = 2
     group_size: int = 64
-    strict: bool = False
+    strict: int = 0  # 0 relaxed, 1 strict, 2 strict in the joint 8b-bit format (no coset words)
     delta_chunk: int = 0
     rope_theta: float = 1e4
 
     def c(self):
-        return _lib.Params(self.key_bits, self.value_bits, self.group_size, int(bool(self.strict)),
+        return _lib.Params(self.key_bits, self.value_bits, self.group_size, int(self.strict),
                            self.delta_chunk, float(self.rope_theta))
 
 
@@ -311,7 +311,11 @@ def sections(buf, lay, tokens=None):
     out = {}
     for t, rb in (("k", int(lay.k_idx_row_bytes)), ("v", int(lay.v_idx_row_bytes))):
         out[t + "_idx"] = shape(view(getattr(lay, t + "_idx"), rows * rb).view(rows, rb))
-        out[t + "_coset"] = shape(view(getattr(lay, t + "_coset"), rows * 2).view(torch.int16))
+        # the joint format (strict = 2) has an empty coset section
+        has_coset = int(getattr(lay, t + "_scale")) - int(getattr(lay, t + "_coset")) >= rows * 2
+        nc = rows if has_coset else 0
+        cos = view(getattr(lay, t + "_coset"), nc * 2).view(torch.int16)
+        out[t + "_coset"] = shape(cos) if has_coset else cos
         spr = int(lay.scales_per_row)
         out[t + "_scale"] = shape(view(getattr(lay, t + "_scale"), rows * spr * 2).view(torch.float16).view(rows, spr))
     return out

@@ -28,13 +28,22 @@ int check(const nq_shape* s, const nq_params* p) {
     const int dp = padded_dim(s->head_dim);
     if (p->group_size != 32 && p->group_size != 64 && p->group_size != 128) return NQ_ERR_UNSUPPORTED;
     if (p->group_size > dp) return NQ_ERR_UNSUPPORTED;
-    if (p->strict != 0 && p->strict != 1) return NQ_ERR_ARG;
+    if (p->strict < 0 || p->strict > 2) return NQ_ERR_ARG;
     if (p->delta_chunk < 0 || (p->delta_chunk % 32) != 0) return NQ_ERR_ARG;
     if (!std::isfinite(p->rope_theta)) return NQ_ERR_ARG;
     return NQ_OK;
 }
 
 int pad_tokens(int tokens) { return (tokens + 31) / 32 * 32; }
+
+// The coset words of a tensor, or null in the strict joint format (strict = 2),
+// whose block codes carry the coset bit themselves.
+uint16_t* coset_section(uint8_t* base, uint64_t off, const nq_params* p) {
+    return p->strict == 2 ? nullptr : reinterpret_cast<uint16_t*>(base + off);
+}
+const uint16_t* coset_section(const uint8_t* base, uint64_t off, const nq_params* p) {
+    return p->strict == 2 ? nullptr : reinterpret_cast<const uint16_t*>(base + off);
+}
 
 void make_layout(const nq_shape* s, const nq_params* p, nq_layout* L) {
     const int dp = padded_dim(s->head_dim);
@@ -51,14 +60,15 @@ void make_layout(const nq_shape* s, const nq_params* p, nq_layout* L) {
     uint64_t off = 0;
     L->k_idx = off;
     off = align256(off + rows * L->k_idx_row_bytes);
+    const uint64_t coset_bytes = p->strict == 2 ? 0 : 2;  // the joint format has no coset words
     L->k_coset = off;
-    off = align256(off + rows * 2);
+    off = align256(off + rows * coset_bytes);
     L->k_scale = off;
     off = align256(off + rows * L->scales_per_row * 2);
     L->v_idx = off;
     off = align256(off + rows * L->v_idx_row_bytes);
     L->v_coset = off;
-    off = align256(off + rows * 2);
+    off = align256(off + rows * coset_bytes);
     L->v_scale = off;
     off = align256(off + rows * L->scales_per_row * 2);
     L->total_bytes = off;
@@ -236,14 +246,14 @@ int nq_compress_kv(const void* k_f16, const void* v_f16, const float* rope_table
     a.delta_chunk = params->delta_chunk;
     a.stream = static_cast<cudaStream_t>(stream);
     uint8_t* base = static_cast<uint8_t*>(out);
-    st = nq::launch_compress_tensor(a, shape->head_dim, params->key_bits, params->strict != 0, k_f16,
+    st = nq::launch_compress_tensor(a, shape->head_dim, params->key_bits, params->strict, k_f16,
                                     rope ? rope_table : nullptr, base + L.k_idx,
-                                    reinterpret_cast<uint16_t*>(base + L.k_coset),
+                                    nq::coset_section(base, L.k_coset, params),
                                     reinterpret_cast<uint16_t*>(base + L.k_scale));
     if (st != NQ_OK) return st;
-    return nq::launch_compress_tensor(a, shape->head_dim, params->value_bits, params->strict != 0,
+    return nq::launch_compress_tensor(a, shape->head_dim, params->value_bits, params->strict,
                                       v_f16, nullptr, base + L.v_idx,
-                                      reinterpret_cast<uint16_t*>(base + L.v_coset),
+                                      nq::coset_section(base, L.v_coset, params),
                                       reinterpret_cast<uint16_t*>(base + L.v_scale));
 }
 
@@ -295,10 +305,10 @@ int nq_code_histogram(const void* in, size_t in_bytes, const nq_shape* shape, co
     a.stream = s;
     const uint8_t* base = static_cast<const uint8_t*>(in);
     st = nq::launch_code_histogram(a, int(L.padded_dim), params->key_bits, base + L.k_idx,
-                                   reinterpret_cast<const uint16_t*>(base + L.k_coset), counts);
+                                   nq::coset_section(base, L.k_coset, params), counts);
     if (st != NQ_OK) return st;
     return nq::launch_code_histogram(a, int(L.padded_dim), params->value_bits, base + L.v_idx,
-                                     reinterpret_cast<const uint16_t*>(base + L.v_coset), counts + NQ_HIST_BINS);
+                                     nq::coset_section(base, L.v_coset, params), counts + NQ_HIST_BINS);
 }
 
 int nq_decompress_kv(const void* in, size_t in_bytes, const float* rope_table,
@@ -324,12 +334,12 @@ int nq_decompress_kv(const void* in, size_t in_bytes, const float* rope_table,
     a.stream = static_cast<cudaStream_t>(stream);
     const uint8_t* base = static_cast<const uint8_t*>(in);
     st = nq::launch_decompress_tensor(a, shape->head_dim, params->key_bits, base + L.k_idx,
-                                      reinterpret_cast<const uint16_t*>(base + L.k_coset),
+                                      nq::coset_section(base, L.k_coset, params),
                                       reinterpret_cast<const uint16_t*>(base + L.k_scale),
                                       rope ? rope_table : nullptr, k_f16_out);
     if (st != NQ_OK) return st;
     return nq::launch_decompress_tensor(a, shape->head_dim, params->value_bits, base + L.v_idx,
-                                        reinterpret_cast<const uint16_t*>(base + L.v_coset),
+                                        nq::coset_section(base, L.v_coset, params),
                                         reinterpret_cast<const uint16_t*>(base + L.v_scale), nullptr,
                                         v_f16_out);
 }

@@ -18,7 +18,7 @@ namespace nq {
 constexpr int kStages = 3;
 constexpr int kCompressSmem = kWarpsPerBlock * kStages * kTileBytes;
 
-template <int D, int BITS, bool STRICT>
+template <int D, int BITS, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     compress_kernel(const __half* __restrict__ x, const float4* __restrict__ rope, int64_t slices,
                     int tokens, int tpad, int group, int chunk, bool delta, uint8_t* __restrict__ idx,
@@ -84,7 +84,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         unsigned short sc[NSUB];
         unsigned blk[NB];
         unsigned cw;
-        row_encode_codes<D, BITS, STRICT>(y, group, blk, cw, sc);
+        row_encode_codes<D, BITS, MODE != 0>(y, group, blk, cw, sc);
+        if constexpr (MODE == 2) {  // strict joint format: the coset bit goes into the block code
+#pragma unroll
+            for (int k = 0; k < NB; ++k) blk[k] = joint_pack<BITS>(blk[k], (cw >> k) & 1u);
+        }
 
         // ---- temporal delta against the previous token of the chunk
         if (delta) {
@@ -125,7 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int q = 0; q < RB / 8; ++q) reinterpret_cast<uint2*>(dst)[q] = make_uint2(w[2 * q], w[2 * q + 1]);
         }
-        coset[rrow] = uint16_t(cw);
+        if constexpr (MODE != 2) coset[rrow] = uint16_t(cw);
         __half* sdst = scales + rrow * nsc;
         const int stride = group / 32;
         for (int s = 0, g = 0; s < NSUB; s += stride, ++g) sdst[g] = __ushort_as_half(sc[s]);
@@ -172,7 +176,7 @@ __device__ __forceinline__ void store_words(uint8_t* dst, const unsigned* w) {
 // delta, and the store of record row rrow.  y: the thread's
 // coordinates in PairMap slots.  t: token index of the row; first: the tile
 // starts a delta chunk at t_begin.
-template <int D, int BITS, bool STRICT>
+template <int D, int BITS, int MODE>
 __device__ __forceinline__ void pair_encode_row(float (&y)[D / 2], int hf, int r, float sgn, int t, bool active,
                                                 bool delta, bool first, int t_begin, int64_t rrow, int group,
                                                 unsigned (&carry)[D / 16], unsigned& carry_c,
@@ -192,7 +196,11 @@ __device__ __forceinline__ void pair_encode_row(float (&y)[D / 2], int hf, int r
     unsigned short sc[NSUB];
     unsigned blk[NBT];
     unsigned cwl;
-    pair_encode_codes<D, BITS, STRICT>(y, hf, sgn, group, blk, cwl, sc);
+    pair_encode_codes<D, BITS, MODE != 0>(y, hf, sgn, group, blk, cwl, sc);
+    if constexpr (MODE == 2) {  // strict joint format: the coset bit goes into the block code
+#pragma unroll
+        for (int k = 0; k < NBT; ++k) blk[k] = joint_pack<BITS>(blk[k], (cwl >> k) & 1u);
+    }
     unsigned cw = cwl << (hf * NBT);
     cw |= __shfl_xor_sync(kFull, cw, 1);
 
@@ -224,7 +232,7 @@ __device__ __forceinline__ void pair_encode_row(float (&y)[D / 2], int hf, int r
     unsigned w[RP::WORDS];
     RP::pack(blk, w);
     store_words<RBT>(idx + rrow * RB + hf * RBT, w);
-    if (hf == 0) coset[rrow] = uint16_t(cw);
+    if (MODE != 2 && hf == 0) coset[rrow] = uint16_t(cw);
 #pragma unroll
     for (int s = 0; s < NSUB; ++s) {
         const int gs = hf * NSUB + s;  // global 32-subgroup
@@ -232,7 +240,7 @@ __device__ __forceinline__ void pair_encode_row(float (&y)[D / 2], int hf, int r
     }
 }
 
-template <int D, int BITS, bool STRICT>
+template <int D, int BITS, int MODE>
 __global__ void __launch_bounds__(kThreads, 2)
     compress_pair_kernel(const __half* __restrict__ x, const float4* __restrict__ rope, int64_t slices,
                          int tokens, int tpad, int group, int chunk, bool delta, uint8_t* __restrict__ idx,
@@ -295,14 +303,14 @@ __global__ void __launch_bounds__(kThreads, 2)
                 pair_rope_remove<D>(y, qq, __ldg(cs + int64_t(hf * (Q / 2) + qq) * tokens));
         }
 
-        pair_encode_row<D, BITS, STRICT>(y, hf, r, sgn, t, active, delta, cur.t0 == cur.t_begin, cur.t_begin,
+        pair_encode_row<D, BITS, MODE>(y, hf, r, sgn, t, active, delta, cur.t0 == cur.t_begin, cur.t_begin,
                                          cur.slice * tpad + t, group, carry, carry_c, idx, coset, scales);
         cur.next();
     }
     cp_async_wait<0>();
 }
 
-template <int D, int BITS, bool STRICT>
+template <int D, int BITS, int MODE>
 __global__ void __launch_bounds__(kRopeThreads, 1)
     compress_pair_rope_kernel(const __half* __restrict__ x, const float4* __restrict__ rope, int64_t slices,
                               int tokens, int tpad, int group, int chunk, bool delta, uint8_t* __restrict__ idx,
@@ -373,7 +381,7 @@ __global__ void __launch_bounds__(kRopeThreads, 1)
             // RoPE removal with the block's table tile: pairs (i, i + D/2) are slots (l, l + Q)
 #pragma unroll
             for (int qq = 0; qq < Q / 2; ++qq) pair_rope_remove<D>(y, qq, rope_tile_entry<D>(stage, hf * (Q / 2) + qq, r));
-            pair_encode_row<D, BITS, STRICT>(y, hf, r, sgn, t, active, delta, cur.t0 == cur.t_begin, cur.t_begin,
+            pair_encode_row<D, BITS, MODE>(y, hf, r, sgn, t, active, delta, cur.t0 == cur.t_begin, cur.t_begin,
                                              slice * tpad + t, group, carry, carry_c, idx, coset, scales);
         }
         cur.next();
@@ -381,10 +389,10 @@ __global__ void __launch_bounds__(kRopeThreads, 1)
     cp_async_wait<0>();
 }
 
-template <int D, int BITS, bool STRICT>
+template <int D, int BITS, int MODE>
 static int launch(const LaunchArgs& a, const __half* x, const float4* rope, uint8_t* idx,
                   uint16_t* coset, __half* scales) {
-    auto kern = compress_kernel<D, BITS, STRICT>;
+    auto kern = compress_kernel<D, BITS, MODE>;
     if (!ensure_smem(reinterpret_cast<const void*>(kern), kCompressSmem)) return NQ_ERR_CUDA;
     const int chunk = a.delta_chunk > 0 ? a.delta_chunk : kTileRows;
     const int64_t items = a.slices * ((a.tokens + chunk - 1) / chunk);
@@ -398,10 +406,10 @@ static int launch(const LaunchArgs& a, const __half* x, const float4* rope, uint
     return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
 }
 
-template <int D, int BITS, bool STRICT>
+template <int D, int BITS, int MODE>
 static int launch_pair(const LaunchArgs& a, const __half* x, const float4* rope, uint8_t* idx,
                        uint16_t* coset, __half* scales) {
-    auto kern = compress_pair_kernel<D, BITS, STRICT>;
+    auto kern = compress_pair_kernel<D, BITS, MODE>;
     if (!ensure_smem(reinterpret_cast<const void*>(kern), kPairCompressSmem)) return NQ_ERR_CUDA;
     const int chunk = a.delta_chunk > 0 ? a.delta_chunk : kPairRows;
     const int64_t items = a.slices * ((a.tpad + chunk - 1) / chunk);
@@ -415,10 +423,10 @@ static int launch_pair(const LaunchArgs& a, const __half* x, const float4* rope,
     return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
 }
 
-template <int D, int BITS, bool STRICT>
+template <int D, int BITS, int MODE>
 static int launch_pair_rope(const LaunchArgs& a, const __half* x, const float4* rope, uint8_t* idx,
                             uint16_t* coset, __half* scales) {
-    auto kern = compress_pair_rope_kernel<D, BITS, STRICT>;
+    auto kern = compress_pair_rope_kernel<D, BITS, MODE>;
     constexpr int smem = RopeStage<D>::SMEM;
     if (!ensure_smem(reinterpret_cast<const void*>(kern), smem)) return NQ_ERR_CUDA;
     const int chunk = a.delta_chunk > 0 ? a.delta_chunk : kPairRows;
@@ -433,24 +441,30 @@ static int launch_pair_rope(const LaunchArgs& a, const __half* x, const float4* 
     return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
 }
 
-template <int D, int BITS, bool STRICT>
+template <int D, int BITS, int MODE>
 static int launch_pair_any(const LaunchArgs& a, const __half* x, const float4* rope, uint8_t* idx,
                            uint16_t* coset, __half* scales) {
-    return rope ? launch_pair_rope<D, BITS, STRICT>(a, x, rope, idx, coset, scales)
-                : launch_pair<D, BITS, STRICT>(a, x, rope, idx, coset, scales);
+    return rope ? launch_pair_rope<D, BITS, MODE>(a, x, rope, idx, coset, scales)
+                : launch_pair<D, BITS, MODE>(a, x, rope, idx, coset, scales);
 }
 
 template <int D>
-static int dispatch_bits(const LaunchArgs& a, int bits, bool strict, const __half* x,
+static int dispatch_bits(const LaunchArgs& a, int bits, int mode, const __half* x,
                          const float4* rope, uint8_t* idx, uint16_t* coset, __half* scales) {
+#define NQ_MODE(B, M)                                                                           \
+    if constexpr (D == 96)                                                                      \
+        return launch<D, B, M>(a, x, rope, idx, coset, scales);                                \
+    else                                                                                        \
+        return launch_pair_any<D, B, M>(a, x, rope, idx, coset, scales);
 #define NQ_CASE(B)                                                                              \
     case B:                                                                                     \
-        if constexpr (D == 96)                                                                  \
-            return strict ? launch<D, B, true>(a, x, rope, idx, coset, scales)                  \
-                          : launch<D, B, false>(a, x, rope, idx, coset, scales);                \
-        else                                                                                    \
-            return strict ? launch_pair_any<D, B, true>(a, x, rope, idx, coset, scales)         \
-                          : launch_pair_any<D, B, false>(a, x, rope, idx, coset, scales);
+        if (mode == 2) {                                                                        \
+            NQ_MODE(B, 2)                                                                       \
+        } else if (mode == 1) {                                                                 \
+            NQ_MODE(B, 1)                                                                       \
+        } else {                                                                                \
+            NQ_MODE(B, 0)                                                                       \
+        }
     switch (bits) {
         NQ_CASE(2)
         NQ_CASE(3)
@@ -459,9 +473,10 @@ static int dispatch_bits(const LaunchArgs& a, int bits, bool strict, const __hal
             return NQ_ERR_UNSUPPORTED;
     }
 #undef NQ_CASE
+#undef NQ_MODE
 }
 
-int launch_compress_tensor(const LaunchArgs& a, int head_dim, int bits, bool strict,
+int launch_compress_tensor(const LaunchArgs& a, int head_dim, int bits, int mode,
                            const void* x, const float* rope, uint8_t* idx, uint16_t* coset,
                            uint16_t* scales) {
     const __half* xh = static_cast<const __half*>(x);
@@ -469,11 +484,11 @@ int launch_compress_tensor(const LaunchArgs& a, int head_dim, int bits, bool str
     __half* sh = reinterpret_cast<__half*>(scales);
     switch (head_dim) {
         case 64:
-            return dispatch_bits<64>(a, bits, strict, xh, r, idx, coset, sh);
+            return dispatch_bits<64>(a, bits, mode, xh, r, idx, coset, sh);
         case 96:
-            return dispatch_bits<96>(a, bits, strict, xh, r, idx, coset, sh);
+            return dispatch_bits<96>(a, bits, mode, xh, r, idx, coset, sh);
         case 128:
-            return dispatch_bits<128>(a, bits, strict, xh, r, idx, coset, sh);
+            return dispatch_bits<128>(a, bits, mode, xh, r, idx, coset, sh);
         default:
             return NQ_ERR_UNSUPPORTED;
     }

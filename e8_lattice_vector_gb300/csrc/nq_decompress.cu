@@ -34,15 +34,16 @@ __device__ __forceinline__ void load_records(const uint8_t* __restrict__ idx, co
     const uint8_t* ib = idx + row0 * RB;
 #pragma unroll
     for (int g = lane; g < 2 * RB; g += 32) cp_async16(stage + kRecIdx + 16 * g, ib + 16 * g, 16);
-    if (lane < 4) cp_async16(stage + kRecCoset + 16 * lane, coset + row0 + 8 * lane, 16);
+    if (lane < 4 && coset != nullptr) cp_async16(stage + kRecCoset + 16 * lane, coset + row0 + 8 * lane, 16);
     const int nsch = 4 * nsc;  // 32 * nsc * 2 / 16
     if (lane < nsch) cp_async16(stage + kRecScale + 16 * lane, scales + row0 * nsc + 8 * lane, 16);
 }
 
-template <int D, int BITS>
+template <int D, int BITS, bool JOINT>
 __device__ __forceinline__ void decode_row(uint32_t stage, const uint8_t* stage_gen, int lane, int nsc, int gshift,
-                                           bool delta, bool first, unsigned (&carry)[PaddedDim<D>::value / 8],
-                                           unsigned& carry_c, float (&y)[PaddedDim<D>::value]) {
+                                           bool delta, bool first,
+                                           unsigned (&carry)[PaddedDim<D>::value / 8], unsigned& carry_c,
+                                           float (&y)[PaddedDim<D>::value]) {
     constexpr int DP = PaddedDim<D>::value;
     constexpr int NB = DP / 8;
     using C = Code<BITS>;
@@ -69,7 +70,7 @@ __device__ __forceinline__ void decode_row(uint32_t stage, const uint8_t* stage_
         }
     }
     const uint16_t* stage_h = reinterpret_cast<const uint16_t*>(stage_gen);
-    unsigned cw = stage_h[kRecCoset / 2 + lane];
+    unsigned cw = JOINT ? 0u : unsigned(stage_h[kRecCoset / 2 + lane]);
     float scf[DP / 32];
 #pragma unroll
     for (int s = 0; s < DP / 32; ++s)
@@ -99,10 +100,18 @@ __device__ __forceinline__ void decode_row(uint32_t stage, const uint8_t* stage_
         carry_c = __shfl_sync(kFull, cw, 31);
     }
 
+    if constexpr (JOINT) {  // strict joint format: the coset bits come out of the block codes
+#pragma unroll
+        for (int k = 0; k < NB; ++k) {
+            unsigned c;
+            blk[k] = joint_split<BITS>(blk[k], c);
+            cw |= c << k;
+        }
+    }
     row_decode_codes<D, BITS>(blk, cw, scf, y);
 }
 
-template <int D, int BITS>
+template <int D, int BITS, bool JOINT>
 __global__ void __launch_bounds__(kThreads, 1)
     decompress_kernel(const uint8_t* __restrict__ idx, const uint16_t* __restrict__ coset,
                       const __half* __restrict__ scales, const float4* __restrict__ rope,
@@ -152,7 +161,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         const uint8_t* stage_gen = smem + (stage - smem_u32(smem));
         float y[DP];
-        decode_row<D, BITS>(stage, stage_gen, lane, nsc, gshift, delta, cur.t0 == cur.t_begin, carry, carry_c, y);
+        decode_row<D, BITS, JOINT>(stage, stage_gen, lane, nsc, gshift, delta, cur.t0 == cur.t_begin, carry, carry_c,
+                                   y);
 
         // ---- RoPE re-apply on keys: rotate each (i, i + D/2) pair by +angle
         if (rope != nullptr) {
@@ -187,7 +197,7 @@ struct KeyStage {
     static constexpr int SMEM = OUT + kKeyStages * BYTES + 1024;
 };
 
-template <int D, int BITS>
+template <int D, int BITS, bool JOINT>
 __global__ void __launch_bounds__(kKeyThreads, 1)
     decompress_key_kernel(const uint8_t* __restrict__ idx, const uint16_t* __restrict__ coset,
                           const __half* __restrict__ scales, const float4* __restrict__ rope,
@@ -250,8 +260,8 @@ __global__ void __launch_bounds__(kKeyThreads, 1)
         if (slice < slices) {  // warp-uniform
             const uint32_t rec = stage + KS::TABLE + wib * kRecStage;
             float y[DP];
-            decode_row<D, BITS>(rec, gbase + (rec - base), lane, nsc, gshift, delta, cur.t0 == cur.t_begin, carry,
-                                carry_c, y);
+            decode_row<D, BITS, JOINT>(rec, gbase + (rec - base), lane, nsc, gshift, delta,
+                                       cur.t0 == cur.t_begin, carry, carry_c, y);
 #pragma unroll
             for (int q = 0; q < D / 4; ++q) {
                 const uint4 raw = lds128(stage + 16 * (q * kTileRows + lane));
@@ -290,7 +300,7 @@ __device__ __forceinline__ void load_pair_records(const uint8_t* __restrict__ id
     const uint8_t* ib = idx + row0 * RB;  // 16 * RB bytes = RB chunks
 #pragma unroll
     for (int g = lane; g < RB; g += 32) cp_async16(stage + kPairRecIdx + 16 * g, ib + 16 * g, 16);
-    if (lane < 2) cp_async16(stage + kPairRecCoset + 16 * lane, coset + row0 + 8 * lane, 16);
+    if (lane < 2 && coset != nullptr) cp_async16(stage + kPairRecCoset + 16 * lane, coset + row0 + 8 * lane, 16);
     const int nsch = 2 * nsc;  // 16 * nsc * 2 / 16
     if (lane < nsch) cp_async16(stage + kPairRecScale + 16 * lane, scales + row0 * nsc + 8 * lane, 16);
 }
@@ -319,7 +329,7 @@ __device__ __forceinline__ void lds_words(uint32_t a, unsigned* w) {
     }
 }
 
-template <int D, int BITS>
+template <int D, int BITS, bool JOINT>
 __global__ void __launch_bounds__(kThreads, 2)
     decompress_pair_kernel(const uint8_t* __restrict__ idx, const uint16_t* __restrict__ coset,
                            const __half* __restrict__ scales, const float4* __restrict__ rope,
@@ -383,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         // ---- the thread's half of the record
         unsigned w[RP::WORDS];
         lds_words<RBT>(stage + kPairRecIdx + r * RB + hf * RBT, w);
-        const unsigned cw_full = reinterpret_cast<const uint16_t*>(gstage + kPairRecCoset)[r];
+        const unsigned cw_full = JOINT ? 0u : unsigned(reinterpret_cast<const uint16_t*>(gstage + kPairRecCoset)[r]);
         unsigned cw = (cw_full >> (hf * NBT)) & ((1u << NBT) - 1u);
         float scf[NSUB];
 #pragma unroll
@@ -415,6 +425,15 @@ __global__ void __launch_bounds__(kThreads, 2)
             carry_c = __shfl_sync(kFull, cw, 30 + hf);
         }
 
+        if constexpr (JOINT) {  // strict joint format: the coset bits come out of the block codes
+#pragma unroll
+            for (int k = 0; k < NBT; ++k) {
+                unsigned c;
+                blk[k] = joint_split<BITS>(blk[k], c);
+                cw |= c << k;
+            }
+        }
+
         float y[HALF];
         pair_decode_codes<D, BITS>(blk, cw, scf, sgn, y);
 
@@ -433,10 +452,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
-template <int D, int BITS>
+template <int D, int BITS, bool JOINT>
 static int launch_pair(const LaunchArgs& a, const uint8_t* idx, const uint16_t* coset, const __half* scales,
                        const float4* rope, const CUtensorMap& map) {
-    auto kern = decompress_pair_kernel<D, BITS>;
+    auto kern = decompress_pair_kernel<D, BITS, JOINT>;
     if (!ensure_smem(reinterpret_cast<const void*>(kern), kPairDecompressSmem)) return NQ_ERR_CUDA;
     const int chunk = a.delta_chunk > 0 ? a.delta_chunk : kPairRows;
     const int64_t items = a.slices * ((a.tokens + chunk - 1) / chunk);
@@ -450,10 +469,10 @@ static int launch_pair(const LaunchArgs& a, const uint8_t* idx, const uint16_t* 
     return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
 }
 
-template <int D, int BITS>
+template <int D, int BITS, bool JOINT>
 static int launch(const LaunchArgs& a, const uint8_t* idx, const uint16_t* coset, const __half* scales,
                   const float4* rope, const CUtensorMap& map) {
-    auto kern = decompress_kernel<D, BITS>;
+    auto kern = decompress_kernel<D, BITS, JOINT>;
     if (!ensure_smem(reinterpret_cast<const void*>(kern), kDecompressSmem)) return NQ_ERR_CUDA;
     const int chunk = a.delta_chunk > 0 ? a.delta_chunk : kTileRows;
     const int64_t items = a.slices * ((a.tokens + chunk - 1) / chunk);
@@ -467,10 +486,10 @@ static int launch(const LaunchArgs& a, const uint8_t* idx, const uint16_t* coset
     return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
 }
 
-template <int D, int BITS>
+template <int D, int BITS, bool JOINT>
 static int launch_keys(const LaunchArgs& a, const uint8_t* idx, const uint16_t* coset, const __half* scales,
                        const float4* rope, const CUtensorMap& map) {
-    auto kern = decompress_key_kernel<D, BITS>;
+    auto kern = decompress_key_kernel<D, BITS, JOINT>;
     constexpr int smem = KeyStage<D>::SMEM;
     if (!ensure_smem(reinterpret_cast<const void*>(kern), smem)) return NQ_ERR_CUDA;
     const int chunk = a.delta_chunk > 0 ? a.delta_chunk : kTileRows;
@@ -485,27 +504,32 @@ static int launch_keys(const LaunchArgs& a, const uint8_t* idx, const uint16_t* 
     return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
 }
 
-template <int D, int BITS>
+template <int D, int BITS, bool JOINT>
 static int launch_any(const LaunchArgs& a, const uint8_t* idx, const uint16_t* coset, const __half* scales,
                       const float4* rope, const CUtensorMap& map) {
     if constexpr (D != 64) {
-        if (rope != nullptr) return launch_keys<D, BITS>(a, idx, coset, scales, rope, map);
-        return launch<D, BITS>(a, idx, coset, scales, rope, map);
+        if (rope != nullptr) return launch_keys<D, BITS, JOINT>(a, idx, coset, scales, rope, map);
+        return launch<D, BITS, JOINT>(a, idx, coset, scales, rope, map);
     } else {
-        return launch_pair<D, BITS>(a, idx, coset, scales, rope, map);
+        return launch_pair<D, BITS, JOINT>(a, idx, coset, scales, rope, map);
     }
 }
 
 template <int D>
 static int dispatch_bits(const LaunchArgs& a, int bits, const uint8_t* idx, const uint16_t* coset,
                          const __half* scales, const float4* rope, const CUtensorMap& map) {
+    // no coset words: the strict joint format, whose block codes carry the coset bits
+    const bool joint = coset == nullptr;
     switch (bits) {
         case 2:
-            return launch_any<D, 2>(a, idx, coset, scales, rope, map);
+            return joint ? launch_any<D, 2, true>(a, idx, coset, scales, rope, map)
+                         : launch_any<D, 2, false>(a, idx, coset, scales, rope, map);
         case 3:
-            return launch_any<D, 3>(a, idx, coset, scales, rope, map);
+            return joint ? launch_any<D, 3, true>(a, idx, coset, scales, rope, map)
+                         : launch_any<D, 3, false>(a, idx, coset, scales, rope, map);
         case 4:
-            return launch_any<D, 4>(a, idx, coset, scales, rope, map);
+            return joint ? launch_any<D, 4, true>(a, idx, coset, scales, rope, map)
+                         : launch_any<D, 4, false>(a, idx, coset, scales, rope, map);
         default:
             return NQ_ERR_UNSUPPORTED;
     }

@@ -49,6 +49,28 @@ __device__ __forceinline__ unsigned swar_add(unsigned a, unsigned b) {
     return ((a & ~H) + (b & ~H)) ^ ((a ^ b) & H);
 }
 
+// Strict-E8 joint enumeration of a block in exactly 8b bits.  In both cosets
+// of strict E8 the field sum m_0 + ... + m_7 is even (the coordinate sum is
+// even and the offsets add a multiple of 8 * (L - 1) / 2 that is even), so the
+// low bit of m_7 follows from the other fields and its place holds the coset
+// bit: fields 0..6 as they are, m_7 >> 1 in the next b - 1 bits, the coset in
+// the top bit.
+template <int BITS>
+__device__ __forceinline__ unsigned joint_pack(unsigned code, unsigned coset) {
+    constexpr int SH = 7 * BITS;
+    const unsigned m7 = (code >> SH) & Code<BITS>::MASK;
+    return (code & ((1u << SH) - 1u)) | ((m7 >> 1) << SH) | (coset << (8 * BITS - 1));
+}
+template <int BITS>
+__device__ __forceinline__ unsigned joint_split(unsigned joint, unsigned& coset) {
+    constexpr int SH = 7 * BITS;
+    constexpr unsigned LOW7 = (Code<BITS>::FIELD_HI >> (BITS - 1)) & ((1u << SH) - 1u);  // bit j*b, j < 7
+    coset = (joint >> (8 * BITS - 1)) & 1u;
+    const unsigned parity = __popc(joint & LOW7) & 1u;
+    const unsigned hi = (joint >> SH) & ((1u << (BITS - 1)) - 1u);
+    return (joint & ((1u << SH) - 1u)) | (((hi << 1) | parity) << SH);
+}
+
 // ------------------------------------------------------------------ Hadamard
 
 __device__ __forceinline__ float2 fsub2(float2 a, float2 b) {

@@ -42,7 +42,7 @@ bool ensure_smem(const void* kernel, int smem);
 // 64 columns x box_rows tokens x 1 slice, 128-byte swizzle.  false on failure.
 bool make_row_tile_map(CUtensorMap* map, void* base, int head_dim, int tokens, int64_t slices, int box_rows);
 
-int launch_compress_tensor(const LaunchArgs& a, int head_dim, int bits, bool strict, const void* x,
+int launch_compress_tensor(const LaunchArgs& a, int head_dim, int bits, int mode, const void* x,
                            const float* rope, uint8_t* idx, uint16_t* coset, uint16_t* scales);
 
 int launch_decompress_tensor(const LaunchArgs& a, int head_dim, int bits, const uint8_t* idx,

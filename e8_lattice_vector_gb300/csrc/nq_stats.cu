@@ -2,8 +2,10 @@
 // report: per tensor, how often each b-bit field value occurs in the idx
 // section (these are the temporal-delta symbols when the delta is on), how
 // often each byte value occurs there (the order-0 statistics a byte-level
-// entropy coder would see), and how many blocks sit in each coset.  Only the
-// record rows of real tokens are counted, not the padding rows.
+// entropy coder would see), and how many blocks sit in each coset (in the
+// strict joint format, where the coset bit is the top bit of the block code,
+// that top bit as stored).  Only the record rows of real tokens are counted,
+// not the padding rows.
 //
 // A thread takes whole record rows.  Field values are counted in registers by
 // SWAR equality tests on the 8-field block codes (one popcount per symbol and
@@ -62,7 +64,12 @@ __global__ void __launch_bounds__(kHistThreads)
 #pragma unroll
             for (int s = 0; s < L - 1; ++s) fc[s] += count_symbol<BITS>(blk[k], unsigned(s));
         }
-        ones += __popc(unsigned(__ldg(coset + rec)) & ((1u << NB) - 1u));
+        if (coset != nullptr) {
+            ones += __popc(unsigned(__ldg(coset + rec)) & ((1u << NB) - 1u));
+        } else {  // joint format: the top bit of each block code
+#pragma unroll
+            for (int k = 0; k < NB; ++k) ones += (blk[k] >> (8 * BITS - 1)) & 1u;
+        }
         blocks += NB;
     }
     unsigned rest = 8 * blocks;  // fields of the last symbol: all the others

@@ -33,6 +33,7 @@
  * order below, each starting at a 256-byte aligned offset given by nq_plan:
  *   K idx   [rows][Dp * key_bits / 8]   bytes   (rows = slices * tokens_padded)
  *   K coset [rows]                       uint16, bit k = coset of block k
+ *                                         (empty when strict = 2, the joint format)
  *   K scale [rows][Dp / group_size]      fp16
  *   V idx / V coset / V scale            the same with value_bits.
  * Dp = padded head_dim (64 for head_dim 64, 128 for 96 and 128).  Within an
@@ -42,7 +43,8 @@
  * delta coding on, every row whose token index is not a multiple of
  * delta_chunk holds its codes minus the previous token's codes (per field,
  * modulo 2^b) and its coset word XOR the previous one; scales are never
- * delta-coded.
+ * delta-coded.  In the joint format the delta applies to the stored fields
+ * (the coset bit included) the same way.
  */
 #ifndef NQ_H
 #define NQ_H
@@ -74,7 +76,13 @@ typedef struct {
  *  key_bits, value_bits: 2, 3 or 4 bits per coordinate ("K3V2", "K2V2").
  *  group_size: 32, 64 or 128 coordinates per fp16 scale; must divide Dp.
  *  strict: 1 = strict E8 (both cosets even-sum), 0 = relaxed parity (the
- *          half-integer coset drops its even-sum rule).
+ *          half-integer coset drops its even-sum rule), 2 = strict E8 in the
+ *          joint format: every block is exactly 8b bits and there are no
+ *          coset words (the field sum of a strict point is even, so the low
+ *          bit of the last field is implied and its place holds the coset
+ *          bit: fields 0..6, then m_7 >> 1 in b - 1 bits, then the coset bit).
+ *          Relaxed codes need the extra bit per block that the coset words
+ *          carry ("What Makes E8 Special", "The Relaxed Parity Discovery").
  *  delta_chunk: 0 = no temporal delta; otherwise a positive multiple of 32:
  *          codes are delta-coded along tokens and the chain restarts at every
  *          token index that is a multiple of delta_chunk (one chain per

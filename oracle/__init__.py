@@ -43,7 +43,9 @@ def lib():
             "orc_delta_row": (None, [_P, _P, _P, ctypes.c_uint16, _I, _I]),
             "orc_undelta_row": (None, [_P, _P, _P, ctypes.c_uint16, _I, _I]),
             "orc_compress_tensor": (None, [_P, _I64, _I, _I, _P, _I, _I, _I, _I, _P, _P, _P]),
-            "orc_decompress_tensor": (None, [_P, _P, _P, _I64, _I, _I, _P, _I, _I, _I, _P]),
+            "orc_decompress_tensor": (None, [_P, _P, _P, _I64, _I, _I, _P, _I, _I, _I, _I, _P]),
+            "orc_joint_pack_row": (None, [_P, ctypes.c_uint16, _I, _I]),
+            "orc_joint_split_row": (ctypes.c_uint16, [_P, _I, _I]),
             "orc_code_histogram": (None, [_P, _P, _I64, _I, _I, _P]),
         }
         for name, (res, args) in sigs.items():
@@ -148,7 +150,8 @@ def compress_tensor(x_bits, tokens, head_dim, bits, group, strict, delta_chunk, 
     return idx, coset, scales
 
 
-def decompress_tensor(idx, coset, scales, slices, tokens, head_dim, bits, group, delta_chunk, cs=None):
+def decompress_tensor(idx, coset, scales, slices, tokens, head_dim, bits, group, delta_chunk, cs=None,
+                      joint=False):
     idx = _c(idx, np.uint8)
     coset = _c(coset, np.uint16)
     scales = _c(scales, np.uint16)
@@ -156,8 +159,20 @@ def decompress_tensor(idx, coset, scales, slices, tokens, head_dim, bits, group,
     csa = None if cs is None else _c(cs, np.float32)
     lib().orc_decompress_tensor(_ptr(idx), _ptr(coset), _ptr(scales), int(slices), int(tokens),
                                 int(head_dim), _ptr(csa), int(bits), int(group), int(delta_chunk),
-                                _ptr(out))
+                                int(bool(joint)), _ptr(out))
     return out
+
+
+def joint_pack_row(idx, coset, dp, bits):
+    idx = _c(idx, np.uint8).copy()
+    lib().orc_joint_pack_row(_ptr(idx), int(coset), int(dp), int(bits))
+    return idx
+
+
+def joint_split_row(idx, dp, bits):
+    idx = _c(idx, np.uint8).copy()
+    c = lib().orc_joint_split_row(_ptr(idx), int(dp), int(bits))
+    return idx, int(c)
 
 
 def encode_row(x_bits, head_dim, bits, group, strict, cs_row=None):
@@ -198,7 +213,7 @@ def code_histogram(idx, coset, head_dim, bits):
     """Counts (274 uint64) of field values, idx bytes and coset bits over the
     record rows idx [rows, Dp*b/8], coset [rows]."""
     idx = _c(idx, np.uint8)
-    coset = _c(coset, np.uint16)
+    coset = None if coset is None else _c(coset, np.uint16)
     counts = np.zeros(274, dtype=np.uint64)
     rows = idx.shape[0] if idx.ndim == 2 else 0
     lib().orc_code_histogram(_ptr(idx), _ptr(coset), int(rows), padded_dim(head_dim), int(bits), _ptr(counts))

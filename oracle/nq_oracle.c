@@ -325,6 +325,34 @@ void orc_undelta_row(uint8_t* idx, uint16_t* coset, const uint8_t* prev_idx, uin
 
 /* ----------------------------------------------------------------- tensors */
 
+/* The strict joint format (strict = 2).  Reading: the pages print no format
+ * for it; in strict E8 the field sum of a block is even in both cosets (the
+ * coordinate sum is even and the offsets add 8 times (2^b - 2)/2 or 8 times
+ * (2^b - 1)/2, both even), so the low bit of m_7 follows from m_0..m_6 and its
+ * place holds the block's coset bit: field 7 stores (m_7 >> 1) with the coset
+ * bit above it, and a block is exactly 8b bits. */
+void orc_joint_pack_row(uint8_t* idx, uint16_t coset, int dp, int bits) {
+    for (int k = 0; k < dp / 8; ++k) {
+        unsigned m7 = get_field(idx, 8 * k + 7, bits);
+        unsigned c = (coset >> k) & 1u;
+        put_field(idx, 8 * k + 7, bits, (m7 >> 1) | (c << (bits - 1)));
+    }
+}
+
+uint16_t orc_joint_split_row(uint8_t* idx, int dp, int bits) {
+    unsigned coset = 0;
+    for (int k = 0; k < dp / 8; ++k) {
+        unsigned f = get_field(idx, 8 * k + 7, bits);
+        unsigned c = f >> (bits - 1);
+        unsigned half7 = f & ((1u << (bits - 1)) - 1u);
+        unsigned sum = 0;
+        for (int j = 0; j < 7; ++j) sum += get_field(idx, 8 * k + j, bits);
+        put_field(idx, 8 * k + 7, bits, (half7 << 1) | (sum & 1u));
+        coset |= c << k;
+    }
+    return (uint16_t)coset;
+}
+
 void orc_compress_tensor(const uint16_t* x, int64_t slices, int tokens, int head_dim,
                          const float* cs, int bits, int group, int strict, int delta_chunk,
                          uint8_t* idx, uint16_t* coset, uint16_t* scales) {
@@ -337,8 +365,12 @@ void orc_compress_tensor(const uint16_t* x, int64_t slices, int tokens, int head
         for (int t = 0; t < tokens; ++t) {
             int64_t row = s * tokens + t;
             const float* cs_row = cs ? cs + (size_t)t * head_dim : 0; /* D/2 pairs of 2 */
-            orc_encode_row(x + row * head_dim, cs_row, head_dim, bits, group, strict,
+            orc_encode_row(x + row * head_dim, cs_row, head_dim, bits, group, strict ? 1 : 0,
                            idx + row * rb, coset + row, scales + row * ng);
+            if (strict == 2) { /* joint format: the coset bits move into the codes */
+                orc_joint_pack_row(idx + row * rb, coset[row], dp, bits);
+                coset[row] = 0;
+            }
             if (delta_chunk > 0) {
                 uint8_t raw_idx[64];
                 uint16_t raw_coset = coset[row];
@@ -354,7 +386,7 @@ void orc_compress_tensor(const uint16_t* x, int64_t slices, int tokens, int head
 
 void orc_decompress_tensor(const uint8_t* idx, const uint16_t* coset, const uint16_t* scales,
                            int64_t slices, int tokens, int head_dim, const float* cs, int bits,
-                           int group, int delta_chunk, uint16_t* x_out) {
+                           int group, int delta_chunk, int joint, uint16_t* x_out) {
     int dp = orc_padded_dim(head_dim);
     size_t rb = (size_t)dp * bits / 8;
     int ng = dp / group;
@@ -375,8 +407,15 @@ void orc_decompress_tensor(const uint8_t* idx, const uint16_t* coset, const uint
                 memcpy(cur_idx, idx + row * rb, rb);
                 cur_coset = coset[row];
             }
-            orc_decode_row(cur_idx, cur_coset, scales + row * ng, cs_row, head_dim, bits, group,
-                           x_out + row * head_dim);
+            if (joint) {
+                uint8_t split[64];
+                memcpy(split, cur_idx, rb);
+                uint16_t c = orc_joint_split_row(split, dp, bits);
+                orc_decode_row(split, c, scales + row * ng, cs_row, head_dim, bits, group, x_out + row * head_dim);
+            } else {
+                orc_decode_row(cur_idx, cur_coset, scales + row * ng, cs_row, head_dim, bits, group,
+                               x_out + row * head_dim);
+            }
         }
     }
 }
@@ -385,7 +424,8 @@ void orc_decompress_tensor(const uint8_t* idx, const uint16_t* coset, const uint
  * delta-code the packed indices and hand them to an entropy coder: "E8
  * walkthrough", "Bit Rate Accounting").  counts[274]: [0, 16) field values,
  * [16, 272) idx bytes, [272] integer-coset blocks, [273] half-coset blocks.
- * Plain counting over every field, byte and block of `rows` record rows. */
+ * Plain counting over every field, byte and block of `rows` record rows;
+ * coset NULL (the joint format) takes each block's top stored bit. */
 void orc_code_histogram(const uint8_t* idx, const uint16_t* coset, int64_t rows, int dp, int bits,
                         uint64_t* counts) {
     size_t rb = (size_t)dp * bits / 8;
@@ -395,6 +435,10 @@ void orc_code_histogram(const uint8_t* idx, const uint16_t* coset, int64_t rows,
         const uint8_t* row = idx + (size_t)r * rb;
         for (int i = 0; i < dp; ++i) counts[get_field(row, i, bits)] += 1;
         for (size_t b = 0; b < rb; ++b) counts[16 + row[b]] += 1;
-        for (int k = 0; k < nb; ++k) counts[272 + ((coset[r] >> k) & 1u)] += 1;
+        for (int k = 0; k < nb; ++k) {
+            /* joint format (no coset words): the top bit of field 7 */
+            unsigned c = coset ? ((coset[r] >> k) & 1u) : (get_field(row, 8 * k + 7, bits) >> (bits - 1));
+            counts[272 + c] += 1;
+        }
     }
 }

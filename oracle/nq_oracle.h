@@ -87,13 +87,22 @@ void orc_undelta_row(uint8_t* idx, uint16_t* coset, const uint8_t* prev_idx, uin
 
 /* Whole tensor [slices][tokens][head_dim] fp16 -> sections idx / coset /
  * scales (rows in the same order).  cs: RoPE table or NULL.  delta_chunk: 0
- * off, else the delta restarts at every multiple of delta_chunk tokens. */
+ * off, else the delta restarts at every multiple of delta_chunk tokens.
+ * strict: 0 relaxed, 1 strict, 2 strict in the joint format (coset words 0). */
 void orc_compress_tensor(const uint16_t* x, int64_t slices, int tokens, int head_dim,
                          const float* cs, int bits, int group, int strict, int delta_chunk,
                          uint8_t* idx, uint16_t* coset, uint16_t* scales);
 void orc_decompress_tensor(const uint8_t* idx, const uint16_t* coset, const uint16_t* scales,
                            int64_t slices, int tokens, int head_dim, const float* cs, int bits,
-                           int group, int delta_chunk, uint16_t* x_out);
+                           int group, int delta_chunk, int joint, uint16_t* x_out);
+
+/* Strict joint format (strict = 2 in orc_compress_tensor, joint = 1 in
+ * orc_decompress_tensor): per block, field 7 holds (m_7 >> 1) and the coset
+ * bit above it; the low bit of m_7 is the parity of m_0 + ... + m_6.  Pack
+ * writes the coset bits of `coset` into the row; split restores m_7 in place
+ * and returns the coset word. */
+void orc_joint_pack_row(uint8_t* idx, uint16_t coset, int dp, int bits);
+uint16_t orc_joint_split_row(uint8_t* idx, int dp, int bits);
 
 /* Counts of field values [0, 16), idx bytes [16, 272) and coset bits
  * [272], [273] over `rows` record rows; counts: 274 entries, overwritten. */

@@ -82,18 +82,22 @@ def _round_trip_check(nq, orc, K, V, params, expect_exact_recon=True):
     buf = nq.compress_kv(K, V, params, rope)
     (k_ref, v_ref, cs) = _oracle_compress(orc, K, V, params)
     got = _gpu_sections(nq, buf, shape, params)
+    joint = int(params.strict) == 2  # no coset words: the block codes carry the coset bits
     for name, ref in (("k", k_ref), ("v", v_ref)):
         gi, gc, gs = got[name]
         ri, rc, rs = ref
         assert np.array_equal(gs, rs), name + " scales"
-        assert np.array_equal(gc, rc), name + " coset words"
+        if joint:
+            assert gc.size == 0 and not rc.any(), name + " coset section"
+        else:
+            assert np.array_equal(gc, rc), name + " coset words"
         assert np.array_equal(gi, ri), name + " idx"
     K2, V2 = nq.decompress_kv(buf, shape, params, rope)
     torch.cuda.synchronize()
     kd = orc.decompress_tensor(*k_ref, L * B * H, T, D, params.key_bits, params.group_size,
-                               params.delta_chunk, cs)
+                               params.delta_chunk, cs, joint=joint)
     vd = orc.decompress_tensor(*v_ref, L * B * H, T, D, params.value_bits, params.group_size,
-                               params.delta_chunk, None)
+                               params.delta_chunk, None, joint=joint)
     for g, r in ((K2, kd), (V2, vd)):
         gb = _bits(g).reshape(r.shape)
         _assert_recon(gb, r)
@@ -102,7 +106,8 @@ def _round_trip_check(nq, orc, K, V, params, expect_exact_recon=True):
     # symbol statistics of the buffer equal the oracle's counts over its records
     counts = nq.code_histogram(buf, shape, params).cpu().numpy().astype(np.uint64)
     for n, (ref, bits) in enumerate(((k_ref, params.key_bits), (v_ref, params.value_bits))):
-        assert np.array_equal(counts[n], orc.code_histogram(ref[0], ref[1], D, bits)), ("histogram", n)
+        ref_counts = orc.code_histogram(ref[0], None if joint else ref[1], D, bits)
+        assert np.array_equal(counts[n], ref_counts), ("histogram", n)
     # the one-pass round trip reconstructs the same values
     K3, V3 = nq.roundtrip_kv(K, V, params, rope)
     torch.cuda.synchronize()
@@ -204,6 +209,11 @@ COMBOS = [
     ((1, 1, 3, 40, 64), 4, 2, 32, 0, 0, 0.0),
     ((1, 1, 2, 300, 128), 3, 2, 64, 1, 256, 1e4),
     ((1, 1, 2, 33, 128), 2, 2, 64, 0, 512, 1e4),
+    # strict joint format (no coset words)
+    ((2, 1, 3, 77, 128), 2, 2, 64, 2, 0, 1e4),
+    ((1, 2, 2, 130, 128), 3, 4, 32, 2, 32, 5e5),
+    ((2, 2, 2, 100, 96), 3, 2, 64, 2, 32, 1e4),
+    ((1, 1, 4, 65, 64), 4, 3, 64, 2, 0, 1e4),
 ]
 
 
@@ -214,7 +224,7 @@ def test_combinations_parity(nq, orc, shape, kb, vb, g, strict, delta, theta):
     torch.manual_seed(hash((shape, kb, vb, g, strict, delta)) % (1 << 31))
     K = (torch.randn(shape, device="cuda") * torch.exp(torch.randn(shape[-1], device="cuda") * 0.7)).half()
     V = torch.randn(shape, device="cuda").half()
-    params = CodecParams(kb, vb, g, bool(strict), delta, theta)
+    params = CodecParams(kb, vb, g, int(strict), delta, theta)
     _round_trip_check(nq, orc, K, V, params)
 
 
@@ -248,14 +258,14 @@ def _edge_inputs(kind, shape):
 
 
 @pytest.mark.parametrize("kind", ["zeros", "neg_zeros", "constant", "fp16_max", "tiny", "sparse", "quantized"])
-@pytest.mark.parametrize("strict", [1, 0])
+@pytest.mark.parametrize("strict", [1, 0, 2])
 def test_edge_cases_parity(nq, orc, kind, strict):
     from e8_lattice_vector_gb300 import CodecParams
 
     shape = (1, 1, 2, 45, 128)
     K, V = _edge_inputs(kind, shape)
     for kb, vb in ((3, 2), (2, 2), (4, 4)):
-        params = CodecParams(kb, vb, 64, bool(strict), 32, 1e4)
+        params = CodecParams(kb, vb, 64, int(strict), 32, 1e4)
         _round_trip_check(nq, orc, K, V, params)
 
 

@@ -84,7 +84,8 @@ def test_plan_rejects_bad_arguments(nq):
     assert _plan(nq, (1, 1, 8, 64, 64), group_size=128)[0] == nq.NQ_ERR_UNSUPPORTED
     assert _plan(nq, ok, delta_chunk=40)[0] == nq.NQ_ERR_ARG
     assert _plan(nq, ok, delta_chunk=-32)[0] == nq.NQ_ERR_ARG
-    assert _plan(nq, ok, strict=2)[0] == nq.NQ_ERR_ARG
+    assert _plan(nq, ok, strict=3)[0] == nq.NQ_ERR_ARG
+    assert _plan(nq, ok, strict=-1)[0] == nq.NQ_ERR_ARG
     assert _plan(nq, (1, -1, 8, 64, 128))[0] == nq.NQ_ERR_ARG
     assert _plan(nq, ok, rope_theta=float("inf"))[0] == nq.NQ_ERR_ARG
     st, lay = _plan(nq, (0, 1, 8, 64, 128))
@@ -202,3 +203,14 @@ def test_layers_validate_before_touching_the_gpu(nq):
     assert L.nq_roundtrip_kv_layers(p16, p16, p16, sh, pr, half, p16, p16, None) == nq.NQ_ERR_UNSUPPORTED
     empty = nq.Shape(0, 1, 8, 64, 128)
     assert L.nq_compress_kv_layers(None, None, None, ctypes.byref(empty), pr, None, None, 0, None) == 0
+
+
+def test_plan_joint_format_has_no_coset_words(nq):
+    shape = (2, 1, 4, 100, 128)
+    st1, l1 = _plan(nq, shape, strict=1)
+    st2, l2 = _plan(nq, shape, strict=2)
+    assert st1 == 0 and st2 == 0
+    assert l2.k_scale == l2.k_coset and l2.v_scale == l2.v_coset
+    assert l2.k_idx_row_bytes == l1.k_idx_row_bytes  # 8b bits per block either way
+    rows = l1.rows
+    assert l1.total_bytes - l2.total_bytes >= 2 * (rows * 2 // 256 * 256)

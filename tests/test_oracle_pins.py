@@ -519,3 +519,77 @@ def test_entropy_bits_closed_forms():
     assert entropy_bits([5, 5, 5, 5]) == 2.0
     assert entropy_bits([7, 0, 0]) == 0.0
     assert abs(entropy_bits([1, 3]) - (2 - 0.75 * np.log2(3))) < 1e-12
+
+
+# ------------------------------------------------ strict joint format (8b bits)
+
+
+def _strict_box_points(bits):
+    """Every point of strict E8 inside the b-bit box, as (fields, coset)."""
+    import itertools
+
+    L = 1 << bits
+    hi0 = L // 2 - 1
+    pts = []
+    for r in itertools.product(range(-hi0, hi0 + 1), repeat=8):
+        if sum(r) % 2 == 0:
+            pts.append(([v + hi0 for v in r], 0))
+    for m in itertools.product(range(L), repeat=8):
+        # half-integer coordinates m - (L-1)/2: their sum is sum(m) - 4(L-1), even iff sum(m) is
+        if sum(m) % 2 == 0:
+            pts.append((list(m), 1))
+    return pts
+
+
+def test_joint_format_is_a_bijection_b2(orc):
+    """All 3281 + 32768 strict box points at b = 2 get distinct 16-bit codes and
+    split back to themselves."""
+    pts = _strict_box_points(2)
+    assert len(pts) == 3281 + 32768
+    codes = set()
+    for fields, c in pts:
+        row = _pack_fields(fields, 2)
+        j = orc.joint_pack_row(row, c, 8, 2)
+        code = int(j[0]) | (int(j[1]) << 8)
+        codes.add(code)
+        back, c2 = orc.joint_split_row(j, 8, 2)
+        assert c2 == c and np.array_equal(back, row)
+    assert len(codes) == len(pts) and max(codes) < 1 << 16
+
+
+def test_joint_format_round_trips_strict_decodes(orc):
+    """Strict decodes at b = 3, 4 survive pack -> split; relaxed parity would
+    not always (its half coset has odd sums)."""
+    rng = np.random.default_rng(23)
+    for bits in (3, 4):
+        h = ((1 << bits) - 1) / 2
+        u = rng.uniform(-h, h, size=(4000, 8)).astype(np.float32)
+        for strict in (1, 0):
+            r = orc.e8_nearest(u, strict, bits)
+            bad = 0
+            for blk in r:
+                half = blk[0] != np.floor(blk[0])
+                off = h if half else (1 << bits) // 2 - 1
+                fields = [int(v + off) for v in blk]
+                row = _pack_fields(fields, bits)
+                back, c = orc.joint_split_row(orc.joint_pack_row(row, int(half), 8, bits), 8, bits)
+                bad += (not np.array_equal(back, row)) or c != int(half)
+            if strict:
+                assert bad == 0
+            else:
+                assert bad > 0
+
+
+def test_joint_tensor_equals_strict_tensor(orc):
+    """compress(strict = 2) then decompress(joint) reconstructs exactly what
+    strict = 1 does, with and without the delta; the scales are the same."""
+    rng = np.random.default_rng(24)
+    for D, bits, delta in ((128, 2, 0), (96, 3, 32), (64, 4, 64)):
+        x = (rng.normal(size=(2, 70, D)) * 2).astype(np.float16).view(np.uint16)
+        i1, c1, s1 = orc.compress_tensor(x, 70, D, bits, 64 if D > 64 else 32, 1, delta)
+        i2, c2, s2 = orc.compress_tensor(x, 70, D, bits, 64 if D > 64 else 32, 2, delta)
+        assert np.array_equal(s1, s2) and not c2.any()
+        g = 64 if D > 64 else 32
+        a = orc.decompress_tensor(i1, c1, s1, 2, 70, D, bits, g, delta)
+        b = orc.decompress_tensor(i2, c2, s2, 2, 70, D, bits, g, delta, joint=True)
+        assert np.array_equal(a, b)
