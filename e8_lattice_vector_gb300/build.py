@@ -16,7 +16,7 @@ LIB = os.path.join(OUT_DIR, "libnq.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 SOURCES = ["nq_api.cu", "nq_compress.cu", "nq_decompress.cu", "nq_roundtrip.cu", "nq_stats.cu", "nq_layers.cu"]
-HEADERS = ["nq_device.cuh", "nq_internal.h"]
+HEADERS = sorted(f for f in os.listdir(CSRC) if f.endswith((".cuh", ".h")))
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + [

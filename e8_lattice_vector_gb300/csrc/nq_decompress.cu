@@ -180,12 +180,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------ keys with a shared table
 //
-// Keys of head_dim 96 / 128: the 8 warps of a block decode the same 32-token
-// tile of 8 consecutive slices (slice = 8 * group + warp), so the tile's RoPE
+// Keys of head_dim 96 / 128: the 4 warps of a block decode the same 32-token
+// tile of 4 consecutive slices (slice = 4 * group + warp), so the tile's RoPE
 // table rows are staged in shared memory once per block instead of being read
 // from L2 by every warp.  Three stages (table tile + the warps' record
-// tiles), one output tile per warp; one block barrier per tile.
-constexpr int kKeyWarps = 8;
+// tiles), one output tile per warp; one block barrier per tile.  Two blocks
+// per SM: a barrier holds 4 warps, not all 8.
+constexpr int kKeyWarps = 4;
 constexpr int kKeyThreads = 32 * kKeyWarps;
 constexpr int kKeyStages = 3;
 
