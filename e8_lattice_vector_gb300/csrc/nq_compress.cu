@@ -310,8 +310,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     cp_async_wait<0>();
 }
 
+// Keys: blocks of 8 warps sharing the RoPE table tile, a 2-deep ring, two
+// blocks per SM (16 warps; a barrier waits for 8 of them).
+constexpr int kCompressRopeWarps = 8;
+constexpr int kCompressRopeThreads = kCompressRopeWarps * 32;
+constexpr int kCompressRopeStages = 2;
+
 template <int D, int BITS, int MODE>
-__global__ void __launch_bounds__(kRopeThreads, 1)
+__global__ void __launch_bounds__(kCompressRopeThreads, 2)
     compress_pair_rope_kernel(const __half* __restrict__ x, const float4* __restrict__ rope, int64_t slices,
                               int tokens, int tpad, int group, int chunk, bool delta, uint8_t* __restrict__ idx,
                               uint16_t* __restrict__ coset, __half* __restrict__ scales) {
@@ -320,7 +326,7 @@ __global__ void __launch_bounds__(kRopeThreads, 1)
     constexpr int HALF = PM::HALF;
     constexpr int Q = PM::Q;
     constexpr int NBT = PM::NBT;
-    using RS = RopeStage<D>;
+    using RS = RopeRing<D, kCompressRopeWarps, kCompressRopeStages>;
     using Walk = TileWalkT<kPairRows>;
 
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -330,25 +336,25 @@ __global__ void __launch_bounds__(kRopeThreads, 1)
     const int hf = lane & 1;
     const int r = lane >> 1;
     const float sgn = hf ? -1.0f : 1.0f;
-    const int64_t ngroups = (slices + kRopeWarps - 1) / kRopeWarps;
+    const int64_t ngroups = (slices + kCompressRopeWarps - 1) / kCompressRopeWarps;
 
     // the walk runs over slice groups; the warp's slice is 16 * group + wib
     Walk cur(blockIdx.x, gridDim.x, ngroups, tpad, chunk);
     Walk pre = cur;
 
     auto load_stage = [&](const Walk& w, uint32_t stage) {
-        for (int g = threadIdx.x; g < (D / 4) * kPairRows; g += kRopeThreads) {
+        for (int g = threadIdx.x; g < (D / 4) * kPairRows; g += kCompressRopeThreads) {
             const int q = g / kPairRows, rr = g - q * kPairRows;
             const int tok = w.t0 + rr;
             const bool ok = tok < tokens;
             cp_async16(stage + rope_slot<D>(q, rr), rope + int64_t(q) * tokens + (ok ? tok : 0), ok ? 16 : 0);
         }
-        const int64_t sl = w.slice * kRopeWarps + wib;
+        const int64_t sl = w.slice * kCompressRopeWarps + wib;
         if (sl < slices) load_pair_tile<D>(x, sl, w.t0, tokens, stage + RS::TABLE + wib * kPairTileBytes, lane);
     };
 
 #pragma unroll
-    for (int s = 0; s < kRopeStages - 1; ++s) {
+    for (int s = 0; s < kCompressRopeStages - 1; ++s) {
         if (pre.valid()) {
             load_stage(pre, sbase + s * RS::BYTES);
             pre.next();
@@ -362,15 +368,15 @@ __global__ void __launch_bounds__(kRopeThreads, 1)
     for (int k = 0; k < NBT; ++k) carry[k] = 0;
 
     for (int i = 0; cur.valid(); ++i) {
-        cp_async_wait<kRopeStages - 2>();  // this thread's copies of tile i are done
+        cp_async_wait<kCompressRopeStages - 2>();  // this thread's copies of tile i are done
         __syncthreads();                    // everyone's are; everyone is done with tile i - 1
         if (pre.valid()) {
-            load_stage(pre, sbase + ((i + kRopeStages - 1) % kRopeStages) * RS::BYTES);
+            load_stage(pre, sbase + ((i + kCompressRopeStages - 1) % kCompressRopeStages) * RS::BYTES);
             pre.next();
         }
         cp_async_commit();
-        const uint32_t stage = sbase + (i % kRopeStages) * RS::BYTES;
-        const int64_t slice = cur.slice * kRopeWarps + wib;
+        const uint32_t stage = sbase + (i % kCompressRopeStages) * RS::BYTES;
+        const int64_t slice = cur.slice * kCompressRopeWarps + wib;
         if (slice < slices) {  // warp-uniform
             const int t = cur.t0 + r;
             const bool active = t < tokens;
@@ -427,16 +433,16 @@ template <int D, int BITS, int MODE>
 static int launch_pair_rope(const LaunchArgs& a, const __half* x, const float4* rope, uint8_t* idx,
                             uint16_t* coset, __half* scales) {
     auto kern = compress_pair_rope_kernel<D, BITS, MODE>;
-    constexpr int smem = RopeStage<D>::SMEM;
+    constexpr int smem = RopeRing<D, kCompressRopeWarps, kCompressRopeStages>::SMEM;
     if (!ensure_smem(reinterpret_cast<const void*>(kern), smem)) return NQ_ERR_CUDA;
     const int chunk = a.delta_chunk > 0 ? a.delta_chunk : kPairRows;
-    const int64_t groups = (a.slices + kRopeWarps - 1) / kRopeWarps;
+    const int64_t groups = (a.slices + kCompressRopeWarps - 1) / kCompressRopeWarps;
     const int64_t items = groups * ((a.tpad + chunk - 1) / chunk);
     if (items == 0) return NQ_OK;
-    const int cap = grid_capacity_threads(reinterpret_cast<const void*>(kern), smem, kRopeThreads);
+    const int cap = grid_capacity_threads(reinterpret_cast<const void*>(kern), smem, kCompressRopeThreads);
     if (cap <= 0) return NQ_ERR_CUDA;
     const int grid = int(std::min<int64_t>(items, cap));
-    kern<<<grid, kRopeThreads, smem, a.stream>>>(x, rope, a.slices, a.tokens, a.tpad, a.group, chunk,
+    kern<<<grid, kCompressRopeThreads, smem, a.stream>>>(x, rope, a.slices, a.tokens, a.tpad, a.group, chunk,
                                                  a.delta_chunk > 0, idx, coset, scales);
     return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
 }

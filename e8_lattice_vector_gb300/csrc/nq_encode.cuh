@@ -215,20 +215,18 @@ __device__ __forceinline__ void pair_encode_codes(float (&y)[D / 2], int hf, flo
 
 // ------------------------------------ keys: the RoPE table shared by a block
 //
-// A block of 16 warps compresses the same 16-token tile of 16 consecutive
-// slices (warp w: slice 16*g + w).  The tile's RoPE table rows (head_dim/4
-// planes x 16 tokens x 16 bytes) are staged once per block, next to the 16
-// warps' fp16 tiles, in a 3-stage ring filled by cp.async; one block barrier
-// per tile orders the refills.  Each key row then reads 512 bytes of table
-// from shared memory instead of L2.
-constexpr int kRopeWarps = 16;
-constexpr int kRopeThreads = kRopeWarps * 32;
-constexpr int kRopeStages = 3;
-template <int D>
-struct RopeStage {
+// A block of WARPS warps processes the same 16-token tile of WARPS consecutive
+// slices (warp w: slice WARPS*g + w).  The tile's RoPE table rows (head_dim/4
+// planes x 16 tokens x 16 bytes) are staged once per block, next to the
+// warps' fp16 tiles, in a STAGES-deep ring filled by cp.async; one block
+// barrier per tile orders the refills.  Each key row then reads 512 bytes of
+// table from shared memory instead of L2.
+template <int D, int WARPS, int STAGES>
+struct RopeRing {
+    static constexpr int THREADS = WARPS * 32;
     static constexpr int TABLE = D * 4 * kPairRows;  // head_dim/4 planes x 16 tokens x 16 B
-    static constexpr int BYTES = TABLE + kRopeWarps * kPairTileBytes;
-    static constexpr int SMEM = kRopeStages * BYTES + 1024;
+    static constexpr int BYTES = TABLE + WARPS * kPairTileBytes;
+    static constexpr int SMEM = STAGES * BYTES + 1024;
 };
 
 // table position of (plane q, tile row rr): the odd thread's planes (q >= D/8)

@@ -17,6 +17,11 @@
 namespace nq {
 
 constexpr int kRtStages = 3;
+// keys: 16 warps share the table tile; a 3-deep ring, so the slot a store
+// reads from is refilled only two tiles later
+constexpr int kRtRopeWarps = 16;
+constexpr int kRtRopeThreads = kRtRopeWarps * 32;
+constexpr int kRtRopeStages = 3;
 constexpr int kRtRowSmem = kWarpsPerBlock * kRtStages * kTileBytes + 1024;
 constexpr int kRtPairSmem = kWarpsPerBlock * kRtStages * kPairTileBytes + 1024;
 
@@ -166,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 // Keys with RoPE: 16 warps share the tile's table rows (16 slices at the same
 // tokens), as in the compressor; one block barrier per tile.
 template <int D, int BITS, bool STRICT>
-__global__ void __launch_bounds__(kRopeThreads, 1)
+__global__ void __launch_bounds__(kRtRopeThreads, 1)
     roundtrip_pair_rope_kernel(const __half* __restrict__ x, const float4* __restrict__ rope,
                                const __grid_constant__ CUtensorMap out_map, int64_t slices, int tokens,
                                int group) {
@@ -174,7 +179,7 @@ __global__ void __launch_bounds__(kRopeThreads, 1)
     constexpr int HALF = PM::HALF;
     constexpr int Q = PM::Q;
     constexpr int NBT = PM::NBT;
-    using RS = RopeStage<D>;
+    using RS = RopeRing<D, kRtRopeWarps, kRtRopeStages>;
     using Walk = TileWalkT<kPairRows>;
 
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -184,24 +189,24 @@ __global__ void __launch_bounds__(kRopeThreads, 1)
     const int hf = lane & 1;
     const int r = lane >> 1;
     const float sgn = hf ? -1.0f : 1.0f;
-    const int64_t ngroups = (slices + kRopeWarps - 1) / kRopeWarps;
+    const int64_t ngroups = (slices + kRtRopeWarps - 1) / kRtRopeWarps;
 
     Walk cur(blockIdx.x, gridDim.x, ngroups, tokens, kPairRows);
     Walk pre = cur;
 
     auto load_stage = [&](const Walk& w, uint32_t stage) {
-        for (int g = threadIdx.x; g < (D / 4) * kPairRows; g += kRopeThreads) {
+        for (int g = threadIdx.x; g < (D / 4) * kPairRows; g += kRtRopeThreads) {
             const int q = g / kPairRows, rr = g - q * kPairRows;
             const int tok = w.t0 + rr;
             const bool ok = tok < tokens;
             cp_async16(stage + rope_slot<D>(q, rr), rope + int64_t(q) * tokens + (ok ? tok : 0), ok ? 16 : 0);
         }
-        const int64_t sl = w.slice * kRopeWarps + wib;
+        const int64_t sl = w.slice * kRtRopeWarps + wib;
         if (sl < slices) load_pair_tile<D>(x, sl, w.t0, tokens, stage + RS::TABLE + wib * kPairTileBytes, lane);
     };
 
 #pragma unroll
-    for (int s = 0; s < kRopeStages - 1; ++s) {
+    for (int s = 0; s < kRtRopeStages - 1; ++s) {
         if (pre.valid()) {
             load_stage(pre, sbase + s * RS::BYTES);
             pre.next();
@@ -210,18 +215,18 @@ __global__ void __launch_bounds__(kRopeThreads, 1)
     }
 
     for (int i = 0; cur.valid(); ++i) {
-        cp_async_wait<kRopeStages - 2>();  // this thread's copies of tile i are done
+        cp_async_wait<kRtRopeStages - 2>();  // this thread's copies of tile i are done
         // the ring slot about to be refilled held tile i - 1: this warp's store
         // from it must have finished reading before the barrier releases the refill
         if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
         __syncthreads();
         if (pre.valid()) {
-            load_stage(pre, sbase + ((i + kRopeStages - 1) % kRopeStages) * RS::BYTES);
+            load_stage(pre, sbase + ((i + kRtRopeStages - 1) % kRtRopeStages) * RS::BYTES);
             pre.next();
         }
         cp_async_commit();
-        const uint32_t stage = sbase + (i % kRopeStages) * RS::BYTES;
-        const int64_t slice = cur.slice * kRopeWarps + wib;
+        const uint32_t stage = sbase + (i % kRtRopeStages) * RS::BYTES;
+        const int64_t slice = cur.slice * kRtRopeWarps + wib;
         if (slice < slices) {  // warp-uniform
             const uint32_t tile = stage + RS::TABLE + wib * kPairTileBytes;
             float y[HALF];
@@ -263,11 +268,11 @@ static int launch_rt(const LaunchArgs& a, const __half* x, const float4* rope, c
         kern<<<grid, kThreads, kRtRowSmem, a.stream>>>(x, rope, map, a.slices, a.tokens, a.group);
     } else if (rope != nullptr) {
         auto kern = roundtrip_pair_rope_kernel<D, BITS, STRICT>;
-        constexpr int smem = RopeStage<D>::SMEM;
-        const int64_t items = (a.slices + kRopeWarps - 1) / kRopeWarps * tiles16;
-        const int grid = grid_for(kern, smem, kRopeThreads, items);
+        constexpr int smem = RopeRing<D, kRtRopeWarps, kRtRopeStages>::SMEM;
+        const int64_t items = (a.slices + kRtRopeWarps - 1) / kRtRopeWarps * tiles16;
+        const int grid = grid_for(kern, smem, kRtRopeThreads, items);
         if (grid < 0) return NQ_ERR_CUDA;
-        kern<<<grid, kRopeThreads, smem, a.stream>>>(x, rope, map, a.slices, a.tokens, a.group);
+        kern<<<grid, kRtRopeThreads, smem, a.stream>>>(x, rope, map, a.slices, a.tokens, a.group);
     } else {
         auto kern = roundtrip_pair_kernel<D, BITS, STRICT>;
         const int64_t items = a.slices * tiles16;
