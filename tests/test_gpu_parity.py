@@ -426,3 +426,43 @@ def test_full_size_sampled_parity(nq, orc, name):
         assert bool((K3 == K2).all()) and bool((V3 == V2).all())
         del buf, K2, V2, K3, V3
         torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name,kb,vb", [("mistral7b", 2, 2), ("phi3mini", 3, 2)])
+def test_full_size_joint_format(nq, orc, name, kb, vb):
+    """The strict joint format on a full-size cache: sampled rows re-encoded by
+    the oracle (strict decode, then the joint packing), no coset section, and
+    the sampled reconstructions equal the oracle's."""
+    from e8_lattice_vector_gb300 import CodecParams
+    from e8_lattice_vector_gb300.synth import CONFIGS, make_cache
+
+    cfg = CONFIGS[name]
+    K, V = make_cache(cfg, device="cuda")
+    T, D = cfg.tokens, cfg.head_dim
+    params = CodecParams(kb, vb, 64, 2, 0, cfg.theta)
+    rope = nq.RopeTable.build(T, D, params.rope_theta)
+    cs = rope.pairs()
+    buf = nq.compress_kv(K, V, params, rope)
+    lay = nq.plan(cfg.shape, params)
+    assert lay.k_coset == lay.k_scale and lay.v_coset == lay.v_scale
+    tp = int(lay.tokens_padded)
+    full = nq.sections(buf, lay)
+    rows = _sample_rows(np.random.default_rng(99), cfg, 400)
+    rec = torch.from_numpy((rows // T) * tp + rows % T).cuda()
+    K2, V2 = nq.decompress_kv(buf, cfg.shape, params, rope)
+    dp = orc.padded_dim(D)
+    for t_name, X, X2, bits, rope_on in (("k", K, K2, kb, True), ("v", V, V2, vb, False)):
+        gi = full[t_name + "_idx"][rec].cpu().numpy()
+        gs = full[t_name + "_scale"][rec].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+        sel = torch.from_numpy(rows).cuda()
+        xr = _bits(X.view(-1, D)[sel])
+        xr2 = _bits(X2.view(-1, D)[sel])
+        for n, r in enumerate(rows):
+            csr = cs[int(r % T)] if rope_on else None
+            idx, cw, sc = orc.encode_row(xr[n], D, bits, 64, 1, csr)
+            assert np.array_equal(gs[n], sc), (t_name, r)
+            assert np.array_equal(gi[n], orc.joint_pack_row(idx, cw, dp, bits)), (t_name, r)
+            ref = orc.decode_row(idx, cw, sc, D, bits, 64, csr)
+            assert _same_values(xr2[n], ref), (t_name, r)
+    del buf, K2, V2
+    torch.cuda.empty_cache()
