@@ -188,11 +188,13 @@ __device__ __forceinline__ float fmin3(float a, float b, float c) {
 // ------------------------------------------------------------------- scale
 
 // Smallest binary16 v with v * step >= amax (step = Dp * (2^b - 1) / 2), as
-// bits.  Candidate: amax / step rounded to fp16; it is at most one fp16 step
-// away from the answer, and the products v * step are exact in fp32.
-__device__ __forceinline__ unsigned short group_scale(float amax, float step) {
+// bits.  Candidate: amax * (1 / step) rounded to fp16 -- within two fp32 ulps
+// of amax / step, so at most one fp16 step away from the answer -- then one
+// step up or down decided by the exact products v * step (fp16 times a small
+// integer or half-integer is exact in fp32).
+__device__ __forceinline__ unsigned short group_scale(float amax, float step, float inv_step) {
     if (!(amax > 0.0f)) return 0;
-    float q = __fdiv_rn(amax, step);
+    float q = __fmul_rn(amax, inv_step);
     unsigned short v = __half_as_ushort(__float2half_rn(q));
     if (__fmul_rn(__half2float(__ushort_as_half(v)), step) < amax) {
         ++v;

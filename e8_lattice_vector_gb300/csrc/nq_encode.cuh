@@ -102,7 +102,7 @@ __device__ __forceinline__ void row_encode_codes(float (&y)[PaddedDim<D>::value]
     bool fast = true;
 #pragma unroll
     for (int s = 0; s < NSUB; ++s) {
-        sc[s] = group_scale(amax[s], STEP);
+        sc[s] = group_scale(amax[s], STEP, 1.0f / STEP);
         const float scf = __half2float(__ushort_as_half(sc[s]));
         inv[s] = sc[s] ? __frcp_rn(__fmul_rn(scf, float(DP))) : 0.0f;
         fast = fast && (__fmul_rn(amax[s], inv[s]) < C::H);
@@ -178,7 +178,7 @@ __device__ __forceinline__ void pair_encode_codes(float (&y)[D / 2], int hf, flo
     bool fast = true;
 #pragma unroll
     for (int s = 0; s < NSUB; ++s) {
-        sc[s] = group_scale(amax[s], STEP);
+        sc[s] = group_scale(amax[s], STEP, 1.0f / STEP);
         const float scf = __half2float(__ushort_as_half(sc[s]));
         inv[s] = sc[s] ? __frcp_rn(__fmul_rn(scf, float(DP))) : 0.0f;
         fast = fast && (__fmul_rn(amax[s], inv[s]) < C::H);
