@@ -76,29 +76,35 @@ __device__ __forceinline__ void decode_row(uint32_t stage, const uint8_t* stage_
     for (int s = 0; s < DP / 32; ++s)
         scf[s] = __half2float(__ushort_as_half(stage_h[kRecScale / 2 + lane * nsc + ((32 * s) >> gshift)]));
     __syncwarp();  // the stage may be refilled
-    unsigned blk[NB];
-    RP::unpack(w, blk);
 
-    // ---- undo the temporal delta: inclusive scan over the tile + carry
+    // ---- undo the temporal delta: inclusive scan over the tile + carry.  At
+    // 2 bits the fields never straddle a word, so the scan runs on the packed
+    // words (16 fields each, half the shuffles); otherwise on the block codes.
+    constexpr bool BY_WORD = BITS == 2;
+    constexpr int NS = BY_WORD ? RP::WORDS : NB;
+    unsigned blk[NB];
+    if constexpr (!BY_WORD) RP::unpack(w, blk);
+    unsigned* sv = BY_WORD ? w : blk;
     if (delta) {
 #pragma unroll
         for (int off = 1; off < 32; off *= 2) {
 #pragma unroll
-            for (int k = 0; k < NB; ++k) {
-                const unsigned v = __shfl_up_sync(kFull, blk[k], off);
-                if (lane >= off) blk[k] = swar_add<BITS>(blk[k], v);
+            for (int k = 0; k < NS; ++k) {
+                const unsigned v = __shfl_up_sync(kFull, sv[k], off);
+                if (lane >= off) sv[k] = BY_WORD ? swar_add_word2(sv[k], v) : swar_add<BITS>(sv[k], v);
             }
             const unsigned vc = __shfl_up_sync(kFull, cw, off);
             if (lane >= off) cw ^= vc;
         }
 #pragma unroll
-        for (int k = 0; k < NB; ++k) {
-            if (!first) blk[k] = swar_add<BITS>(blk[k], carry[k]);
-            carry[k] = __shfl_sync(kFull, blk[k], 31);
+        for (int k = 0; k < NS; ++k) {
+            if (!first) sv[k] = BY_WORD ? swar_add_word2(sv[k], carry[k]) : swar_add<BITS>(sv[k], carry[k]);
+            carry[k] = __shfl_sync(kFull, sv[k], 31);
         }
         if (!first) cw ^= carry_c;
         carry_c = __shfl_sync(kFull, cw, 31);
     }
+    if constexpr (BY_WORD) RP::unpack(w, blk);
 
     if constexpr (JOINT) {  // strict joint format: the coset bits come out of the block codes
 #pragma unroll

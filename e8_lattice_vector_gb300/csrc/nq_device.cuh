@@ -71,6 +71,12 @@ __device__ __forceinline__ unsigned joint_split(unsigned joint, unsigned& coset)
     return (joint & ((1u << SH) - 1u)) | (((hi << 1) | parity) << SH);
 }
 
+// Field-wise (a + b) mod 4 of the 16 two-bit fields of a packed word.
+__device__ __forceinline__ unsigned swar_add_word2(unsigned a, unsigned b) {
+    constexpr unsigned H = 0xAAAAAAAAu;  // high bit of every field
+    return ((a & ~H) + (b & ~H)) ^ ((a ^ b) & H);
+}
+
 // ------------------------------------------------------------------ Hadamard
 
 __device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
