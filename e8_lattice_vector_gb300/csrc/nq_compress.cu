@@ -1,150 +1,25 @@
-// nq_compress.cu -- fused compression kernel: fp16 row -> RoPE removal (keys)
+// nq_compress.cu -- fused compression kernels: fp16 row -> RoPE removal (keys)
 // -> zero-padded Hadamard -> group scale -> E8 nearest point -> b-bit codes ->
 // temporal delta -> idx / coset / scale sections.
 //
-// Layout of the work: a warp owns 32 consecutive tokens of one (layer, batch,
-// head) slice (a tile) and lane r owns token row r, in registers, so the
-// Hadamard transform, the group scale and the E8 search need no shuffles; the
-// previous token's codes for the delta come from the neighbouring lane.  The
-// tiles are streamed through a 3-stage shared-memory ring per warp, filled by
-// coalesced 16-byte cp.async copies two tiles ahead of the one being computed.
-// The grid is one resident block per SM; warps take work items
-// (slice, chunk of delta_chunk tokens, or 32 tokens without delta)
-// round-robin.
+// Layout of the work: two threads per token row (lanes 2r and 2r+1 of a warp
+// share row r of a 16-token tile of one (layer, batch, head) slice), so a
+// thread holds 64 of the padded row's 128 coordinates (32 of 64) and the
+// kernels fit 128 registers.  Tiles stream through a 3-stage shared-memory
+// ring per warp, filled by coalesced 16-byte cp.async copies two tiles ahead;
+// keys of head_dim 64 / 128 instead run in blocks of warps that share the
+// tile's RoPE table rows in shared memory.  The previous token's codes for
+// the delta come from the lanes two below.  Warps take work items (slice,
+// chunk of delta_chunk tokens, or 16 tokens without delta) round-robin.
 #include "nq_encode.cuh"
 
 namespace nq {
 
-constexpr int kStages = 3;
-constexpr int kCompressSmem = kWarpsPerBlock * kStages * kTileBytes;
-
-template <int D, int BITS, int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
-    compress_kernel(const __half* __restrict__ x, const float4* __restrict__ rope, int64_t slices,
-                    int tokens, int tpad, int group, int chunk, bool delta, uint8_t* __restrict__ idx,
-                    uint16_t* __restrict__ coset, __half* __restrict__ scales) {
-    constexpr int DP = PaddedDim<D>::value;
-    constexpr int NB = DP / 8;
-    constexpr int NSUB = DP / 32;
-    using RP = RowPack<BITS, NB>;
-    constexpr int RB = DP * BITS / 8;  // idx bytes per row
-
-    extern __shared__ __align__(1024) uint8_t smem[];
-    const int lane = threadIdx.x & 31;
-    const uint32_t ring = smem_u32(smem) + (threadIdx.x >> 5) * (kStages * kTileBytes);
-    const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
-    const int nsc = DP / group;
-
-    TileWalk cur(warp, nwarps, slices, tokens, chunk);
-    TileWalk pre = cur;
-#pragma unroll
-    for (int s = 0; s < kStages - 1; ++s) {
-        if (pre.valid()) {
-            load_tile<D>(x, pre, ring + s * kTileBytes, lane);
-            pre.next();
-        }
-        cp_async_commit();
-    }
-
-    unsigned carry[NB];
-    unsigned carry_c = 0;
-#pragma unroll
-    for (int k = 0; k < NB; ++k) carry[k] = 0;
-
-    for (int i = 0; cur.valid(); ++i) {
-        if (pre.valid()) {
-            load_tile<D>(x, pre, ring + ((i + kStages - 1) % kStages) * kTileBytes, lane);
-            pre.next();
-        }
-        cp_async_commit();
-        cp_async_wait<kStages - 1>();
-        __syncwarp();
-        const uint32_t stage = ring + (i % kStages) * kTileBytes;
-
-        const int t = cur.t0 + lane;
-        const bool active = t < cur.t_end;
-
-        // ---- the lane's row from the stage (fp16 -> fp32), zero padding to DP
-        float y[DP];
-#pragma unroll
-        for (int q = 0; q < D / 8; ++q) h8_to_f(lds128(stage + swz(lane, q)), &y[8 * q]);
-#pragma unroll
-        for (int j = D; j < DP; ++j) y[j] = 0.0f;
-        __syncwarp();  // every lane has its row: the stage may be refilled
-
-        // ---- RoPE removal on keys: rotate each (i, i + D/2) pair by -angle
-        if (rope != nullptr) {
-            // table layout [D/4][tokens] float4: lanes read consecutive tokens
-            const float4* cs = rope + (active ? t : cur.t_begin);
-#pragma unroll
-            for (int q = 0; q < D / 4; ++q) row_rope_remove<D>(y, q, __ldg(cs + int64_t(q) * tokens));
-        }
-
-        unsigned short sc[NSUB];
-        unsigned blk[NB];
-        unsigned cw;
-        row_encode_codes<D, BITS, MODE != 0>(y, group, blk, cw, sc);
-        if constexpr (MODE == 2) {  // strict joint format: the coset bit goes into the block code
-#pragma unroll
-            for (int k = 0; k < NB; ++k) blk[k] = joint_pack<BITS>(blk[k], (cw >> k) & 1u);
-        }
-
-        // ---- temporal delta against the previous token of the chunk
-        if (delta) {
-            const bool first = cur.t0 == cur.t_begin;
-#pragma unroll
-            for (int k = 0; k < NB; ++k) {
-                unsigned prev = __shfl_up_sync(kFull, blk[k], 1);
-                const unsigned last = __shfl_sync(kFull, blk[k], 31);
-                if (lane == 0) prev = first ? 0u : carry[k];
-                if (t != cur.t_begin) blk[k] = swar_sub<BITS>(blk[k], prev);
-                carry[k] = last;  // raw codes of the tile's last token
-            }
-            unsigned pc = __shfl_up_sync(kFull, cw, 1);
-            const unsigned lastc = __shfl_sync(kFull, cw, 31);
-            if (lane == 0) pc = first ? 0u : carry_c;
-            if (t != cur.t_begin) cw ^= pc;
-            carry_c = lastc;
-        }
-
-        // ---- store the row's record (padding rows past the slice get zeros)
-        if (!active) {
-#pragma unroll
-            for (int k = 0; k < NB; ++k) blk[k] = 0;
-            cw = 0;
-#pragma unroll
-            for (int s = 0; s < NSUB; ++s) sc[s] = 0;
-        }
-        const int64_t rrow = cur.slice * tpad + t;
-        unsigned w[RP::WORDS];
-        RP::pack(blk, w);
-        uint8_t* dst = idx + rrow * RB;
-        if constexpr (RB % 16 == 0) {
-#pragma unroll
-            for (int q = 0; q < RB / 16; ++q)
-                st_stream(reinterpret_cast<uint4*>(dst) + q,
-                          make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]));
-        } else {
-#pragma unroll
-            for (int q = 0; q < RB / 8; ++q) reinterpret_cast<uint2*>(dst)[q] = make_uint2(w[2 * q], w[2 * q + 1]);
-        }
-        if constexpr (MODE != 2) coset[rrow] = uint16_t(cw);
-        __half* sdst = scales + rrow * nsc;
-        const int stride = group / 32;
-        for (int s = 0, g = 0; s < NSUB; s += stride, ++g) sdst[g] = __ushort_as_half(sc[s]);
-
-        cur.next();
-    }
-    cp_async_wait<0>();
-}
-
-
 // ------------------------------------------------------- two threads per row
 //
-// head_dim 64 and 128: lanes 2r and 2r+1 share token row r of a 16-row tile
-// (PairMap): each thread holds 64 (or 32) coordinates, so the kernel fits 128
-// registers and two blocks per SM.  The Hadamard transform runs in the
+// Lanes 2r and 2r+1 share token row r of a 16-row tile (PairMap of the padded
+// dimension; head_dim 96 adds zero chunks 12..15): each thread holds 64 (or
+// 32) coordinates, so the kernel fits 128 registers and two blocks per SM.  The Hadamard transform runs in the
 // compression stage order; its stage on bit DP/2 is in-thread with a sign
 // that leaves the odd thread's slot halves exchanged, so the last stage
 // (bit DP/4) is one symmetric shuffle exchange.  Afterwards thread hf holds
@@ -245,7 +120,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     compress_pair_kernel(const __half* __restrict__ x, const float4* __restrict__ rope, int64_t slices,
                          int tokens, int tpad, int group, int chunk, bool delta, uint8_t* __restrict__ idx,
                          uint16_t* __restrict__ coset, __half* __restrict__ scales) {
-    constexpr int DP = D;
+    constexpr int DP = PaddedDim<D>::value;  // head_dim 96 runs zero-padded to 128
     using PM = PairMap<DP>;
     constexpr int HALF = PM::HALF;
     constexpr int Q = PM::Q;
@@ -289,21 +164,46 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int t = cur.t0 + r;
         const bool active = t < tokens;
 
-        // ---- the thread's 64 (32) coordinates of row r
+        // ---- the thread's 64 (32) coordinates of row r (zeros past head_dim)
         float y[HALF];
 #pragma unroll
-        for (int c = 0; c < NBT; ++c) h8_to_f(lds128(stage + swz16(r, PM::chunk(hf, c))), &y[8 * c]);
-        __syncwarp();  // every lane has its coordinates: the stage may be refilled
-
-        // ---- RoPE removal on keys: pairs (i, i + D/2) are slots (l, l + Q)
-        if (rope != nullptr) {
-            const float4* cs = rope + (active ? t : 0);
+        for (int c = 0; c < NBT; ++c) {
+            const int gc = PM::chunk(hf, c);
+            if (D == DP || gc < D / 8) {
+                h8_to_f(lds128(stage + swz16(r, gc)), &y[8 * c]);
+            } else {
 #pragma unroll
-            for (int qq = 0; qq < Q / 2; ++qq)
-                pair_rope_remove<D>(y, qq, __ldg(cs + int64_t(hf * (Q / 2) + qq) * tokens));
+                for (int j = 0; j < 8; ++j) y[8 * c + j] = 0.0f;
+            }
         }
 
-        pair_encode_row<D, BITS, MODE>(y, hf, r, sgn, t, active, delta, cur.t0 == cur.t_begin, cur.t_begin,
+        // ---- RoPE removal on keys
+        if (rope != nullptr) {
+            const float4* cs = rope + (active ? t : 0);
+            if constexpr (D == DP) {  // pairs (i, i + D/2) are slots (l, l + Q)
+#pragma unroll
+                for (int qq = 0; qq < Q / 2; ++qq)
+                    pair_rope_remove<D>(y, qq, __ldg(cs + int64_t(hf * (Q / 2) + qq) * tokens));
+            } else {  // pairs (i, i + D/2) are not slot pairs: partners come from the tile
+#pragma unroll
+                for (int c = 0; c < NBT; ++c) {
+                    const int gc = PM::chunk(hf, c);
+                    if (gc < D / 8) {
+                        const bool lower = gc < D / 16;  // member i of the pair (else i + D/2)
+                        float xp[8];
+                        h8_to_f(lds128(stage + swz16(r, lower ? gc + D / 16 : gc - D / 16)), xp);
+                        const int q0 = 4 * (lower ? gc : gc - D / 16);  // table plane of the chunk's first pair
+#pragma unroll
+                        for (int qq = 0; qq < 4; ++qq)
+                            rope_remove_member(&y[8 * c + 2 * qq], &xp[2 * qq],
+                                               __ldg(cs + int64_t(q0 + qq) * tokens), lower);
+                    }
+                }
+            }
+        }
+        __syncwarp();  // every lane has read its coordinates: the stage may be refilled
+
+        pair_encode_row<DP, BITS, MODE>(y, hf, r, sgn, t, active, delta, cur.t0 == cur.t_begin, cur.t_begin,
                                          cur.slice * tpad + t, group, carry, carry_c, idx, coset, scales);
         cur.next();
     }
@@ -396,23 +296,6 @@ __global__ void __launch_bounds__(kCompressRopeThreads, 2)
 }
 
 template <int D, int BITS, int MODE>
-static int launch(const LaunchArgs& a, const __half* x, const float4* rope, uint8_t* idx,
-                  uint16_t* coset, __half* scales) {
-    auto kern = compress_kernel<D, BITS, MODE>;
-    if (!ensure_smem(reinterpret_cast<const void*>(kern), kCompressSmem)) return NQ_ERR_CUDA;
-    const int chunk = a.delta_chunk > 0 ? a.delta_chunk : kTileRows;
-    const int64_t items = a.slices * ((a.tokens + chunk - 1) / chunk);
-    const int64_t want = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    if (want == 0) return NQ_OK;
-    const int cap = grid_capacity(reinterpret_cast<const void*>(kern), kCompressSmem);
-    if (cap <= 0) return NQ_ERR_CUDA;
-    const int grid = int(std::min<int64_t>(want, cap));
-    kern<<<grid, kThreads, kCompressSmem, a.stream>>>(x, rope, a.slices, a.tokens, a.tpad, a.group, chunk,
-                                                      a.delta_chunk > 0, idx, coset, scales);
-    return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
-}
-
-template <int D, int BITS, int MODE>
 static int launch_pair(const LaunchArgs& a, const __half* x, const float4* rope, uint8_t* idx,
                        uint16_t* coset, __half* scales) {
     auto kern = compress_pair_kernel<D, BITS, MODE>;
@@ -459,7 +342,7 @@ static int dispatch_bits(const LaunchArgs& a, int bits, int mode, const __half* 
                          const float4* rope, uint8_t* idx, uint16_t* coset, __half* scales) {
 #define NQ_MODE(B, M)                                                                           \
     if constexpr (D == 96)                                                                      \
-        return launch<D, B, M>(a, x, rope, idx, coset, scales);                                \
+        return launch_pair<D, B, M>(a, x, rope, idx, coset, scales);                           \
     else                                                                                        \
         return launch_pair_any<D, B, M>(a, x, rope, idx, coset, scales);
 #define NQ_CASE(B)                                                                              \

@@ -258,6 +258,18 @@ __device__ __forceinline__ void row_rope_remove(float (&y)[N], int q, float4 cs)
     }
 }
 
+// RoPE removal of one member of two consecutive pairs given the raw partner
+// values: own = (x_i, x_i+1) of the lower members (lower) or (x_j, x_j+1) of
+// the upper ones, partner = the other members; cs = (cos, sin) of both pairs.
+__device__ __forceinline__ void rope_remove_member(float* own, const float* partner, float4 cs, bool lower) {
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+        const float c = p ? cs.z : cs.x, sn = p ? cs.w : cs.y;
+        const float ps = __fmul_rn(partner[p], sn);
+        own[p] = __fmaf_rn(own[p], c, lower ? ps : -ps);
+    }
+}
+
 // The same on a two-thread row before the rotation: the pairs (i, i + D/2)
 // are slots (l, l + Q), l = 2qq and 2qq + 1.
 template <int D>
