@@ -185,20 +185,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int qq = 0; qq < Q / 2; ++qq)
                     pair_rope_remove<D>(y, qq, __ldg(cs + int64_t(hf * (Q / 2) + qq) * tokens));
             } else {  // pairs (i, i + D/2) are not slot pairs: partners come from the tile
-#pragma unroll
-                for (int c = 0; c < NBT; ++c) {
-                    const int gc = PM::chunk(hf, c);
-                    if (gc < D / 8) {
-                        const bool lower = gc < D / 16;  // member i of the pair (else i + D/2)
-                        float xp[8];
-                        h8_to_f(lds128(stage + swz16(r, lower ? gc + D / 16 : gc - D / 16)), xp);
-                        const int q0 = 4 * (lower ? gc : gc - D / 16);  // table plane of the chunk's first pair
-#pragma unroll
-                        for (int qq = 0; qq < 4; ++qq)
-                            rope_remove_member(&y[8 * c + 2 * qq], &xp[2 * qq],
-                                               __ldg(cs + int64_t(q0 + qq) * tokens), lower);
-                    }
-                }
+                pair_rope_remove_from_tile<D>(y, hf, stage, r, cs, tokens);
             }
         }
         __syncwarp();  // every lane has read its coordinates: the stage may be refilled

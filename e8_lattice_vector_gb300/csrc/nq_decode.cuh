@@ -104,6 +104,69 @@ __device__ __forceinline__ void pair_rope_apply(float (&y)[D / 2], int qq, float
     }
 }
 
+// RoPE re-apply on a two-thread row of head_dim 96 (padded to 128), whose
+// pairs (i, i + 48) are not slot pairs.  In PairMap<128> thread 0 holds
+// global chunks 0-3 and 8-11, thread 1 chunks 4-7 and the zero padding 12-15;
+// chunk g pairs with g + 6 (g < 6).  Thread 0's pairs (2, 8) and (3, 9) are
+// local; the others cross threads, so four symmetric exchanges of one
+// 8-coordinate chunk bring every partner: (0|6), (1|7), (10|4), (11|5) as
+// (thread 0 sends | thread 1 sends).  cs: the token's table column.
+__device__ __forceinline__ void pair96_rope_apply(float (&y)[64], int hf, const float4* cs, int tokens) {
+    // slot chunk sent in exchange e by thread 0 / thread 1, and the own slot chunk it completes
+    constexpr int SEND0[4] = {0, 1, 6, 7}, SEND1[4] = {2, 3, 0, 1};
+    float part[4][8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float v = hf ? y[8 * SEND1[e] + j] : y[8 * SEND0[e] + j];
+            part[e][j] = __shfl_xor_sync(kFull, v, 1);
+        }
+    }
+    // thread 0's local pairs use the values before rotation
+    float loc[2][8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        loc[0][j] = y[8 * 2 + j];  // chunk 2 (partner of chunk 8, slot 4)
+        loc[1][j] = y[8 * 3 + j];  // chunk 3 (partner of chunk 9, slot 5)
+    }
+    // rotate member `own` (lower: a of (a, b), else b) of the 8 pairs starting at pair index p0
+    auto rot = [&](float* own, const float* other, int p0, bool lower) {
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+            const float4 v = __ldg(cs + int64_t(p0 / 2 + qq) * tokens);
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+                const float c = p ? v.z : v.x, sn = p ? v.w : v.y;
+                const int j = 2 * qq + p;
+                const float o = own[j], x = other[j];
+                own[j] = lower ? __fmaf_rn(o, c, -__fmul_rn(x, sn)) : __fmaf_rn(o, c, __fmul_rn(x, sn));
+            }
+        }
+    };
+    if (hf == 0) {
+        float c4[8], c5[8];  // chunks 8 and 9 before rotation
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            c4[j] = y[8 * 4 + j];
+            c5[j] = y[8 * 5 + j];
+        }
+        rot(&y[0], part[0], 0, true);        // chunk 0 with chunk 6
+        rot(&y[8], part[1], 8, true);        // chunk 1 with chunk 7
+        rot(&y[16], c4, 16, true);           // chunk 2 with chunk 8
+        rot(&y[24], c5, 24, true);           // chunk 3 with chunk 9
+        rot(&y[32], loc[0], 16, false);      // chunk 8 with chunk 2
+        rot(&y[40], loc[1], 24, false);      // chunk 9 with chunk 3
+        rot(&y[48], part[2], 32, false);     // chunk 10 with chunk 4
+        rot(&y[56], part[3], 40, false);     // chunk 11 with chunk 5
+    } else {
+        rot(&y[0], part[2], 32, true);       // chunk 4 with chunk 10
+        rot(&y[8], part[3], 40, true);       // chunk 5 with chunk 11
+        rot(&y[16], part[0], 0, false);      // chunk 6 with chunk 0
+        rot(&y[24], part[1], 8, false);      // chunk 7 with chunk 1
+    }
+}
+
 // fp16 rows of a 16-row tile -> swizzled shared-memory tile -> TMA tensor
 // store (the odd thread's negated slots get their sign bits flipped back).
 // PENDING = stores of the warp's other output tiles that may still be reading.

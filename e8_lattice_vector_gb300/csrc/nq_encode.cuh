@@ -270,6 +270,29 @@ __device__ __forceinline__ void rope_remove_member(float* own, const float* part
     }
 }
 
+// RoPE removal on a two-thread row whose pairs (i, i + D/2) are not slot
+// pairs (head_dim 96 in PairMap<128>): every own coordinate below D is
+// rotated against its partner's raw value, read from the fp16 tile in shared
+// memory (chunk g pairs with g + D/16).  cs: the token's table column.
+template <int D, int N>
+__device__ __forceinline__ void pair_rope_remove_from_tile(float (&y)[N], int hf, uint32_t stage, int r,
+                                                           const float4* cs, int tokens) {
+    using PM = PairMap<2 * N>;
+#pragma unroll
+    for (int c = 0; c < N / 8; ++c) {
+        const int gc = PM::chunk(hf, c);
+        if (gc < D / 8) {
+            const bool lower = gc < D / 16;  // member i of the pair (else i + D/2)
+            float xp[8];
+            h8_to_f(lds128(stage + swz16(r, lower ? gc + D / 16 : gc - D / 16)), xp);
+            const int q0 = 4 * (lower ? gc : gc - D / 16);  // table plane of the chunk's first pair
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq)
+                rope_remove_member(&y[8 * c + 2 * qq], &xp[2 * qq], __ldg(cs + int64_t(q0 + qq) * tokens), lower);
+        }
+    }
+}
+
 // The same on a two-thread row before the rotation: the pairs (i, i + D/2)
 // are slots (l, l + Q), l = 2qq and 2qq + 1.
 template <int D>

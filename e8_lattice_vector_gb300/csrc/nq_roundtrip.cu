@@ -22,81 +22,9 @@ constexpr int kRtStages = 3;
 constexpr int kRtRopeWarps = 16;
 constexpr int kRtRopeThreads = kRtRopeWarps * 32;
 constexpr int kRtRopeStages = 3;
-constexpr int kRtRowSmem = kWarpsPerBlock * kRtStages * kTileBytes + 1024;
 constexpr int kRtPairSmem = kWarpsPerBlock * kRtStages * kPairTileBytes + 1024;
 
-// ------------------------------------------------ one thread per row (D = 96)
-
-template <int D, int BITS, bool STRICT>
-__global__ void __launch_bounds__(kThreads, 1)
-    roundtrip_row_kernel(const __half* __restrict__ x, const float4* __restrict__ rope,
-                         const __grid_constant__ CUtensorMap out_map, int64_t slices, int tokens, int group) {
-    constexpr int DP = PaddedDim<D>::value;
-    constexpr int NB = DP / 8;
-    constexpr int NSUB = DP / 32;
-
-    extern __shared__ __align__(1024) uint8_t smem[];
-    const int lane = threadIdx.x & 31;
-    const uint32_t ring = ((smem_u32(smem) + 1023u) & ~1023u) + (threadIdx.x >> 5) * (kRtStages * kTileBytes);
-    const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
-
-    TileWalk cur(warp, nwarps, slices, tokens, kTileRows);
-    TileWalk pre = cur;
-#pragma unroll
-    for (int s = 0; s < kRtStages - 1; ++s) {
-        if (pre.valid()) {
-            load_tile<D>(x, pre, ring + s * kTileBytes, lane);
-            pre.next();
-        }
-        cp_async_commit();
-    }
-
-    for (int i = 0; cur.valid(); ++i) {
-        cp_async_wait<kRtStages - 2>();  // tile i has landed
-        __syncwarp();
-        const uint32_t stage = ring + (i % kRtStages) * kTileBytes;
-        const int t = cur.t0 + lane;
-
-        float y[DP];
-#pragma unroll
-        for (int q = 0; q < D / 8; ++q) h8_to_f(lds128(stage + swz(lane, q)), &y[8 * q]);
-#pragma unroll
-        for (int j = D; j < DP; ++j) y[j] = 0.0f;
-        // the slot of tile i - 1 is refilled next: its store must have read it
-        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-        __syncwarp();
-        if (pre.valid()) {
-            load_tile<D>(x, pre, ring + ((i + kRtStages - 1) % kRtStages) * kTileBytes, lane);
-            pre.next();
-        }
-        cp_async_commit();
-
-        const float4* cs = rope == nullptr ? nullptr : rope + (t < cur.t_end ? t : cur.t_begin);
-        if (cs != nullptr) {
-#pragma unroll
-            for (int q = 0; q < D / 4; ++q) row_rope_remove<D>(y, q, __ldg(cs + int64_t(q) * tokens));
-        }
-        unsigned short sc[NSUB];
-        unsigned blk[NB];
-        unsigned cw;
-        row_encode_codes<D, BITS, STRICT>(y, group, blk, cw, sc);
-        float scf[NSUB];
-#pragma unroll
-        for (int s = 0; s < NSUB; ++s) scf[s] = __half2float(__ushort_as_half(sc[s]));
-        row_decode_codes<D, BITS>(blk, cw, scf, y);
-        if (cs != nullptr) {
-#pragma unroll
-            for (int q = 0; q < D / 4; ++q) rope_apply_pairs<D>(y, q, __ldg(cs + int64_t(q) * tokens));
-        }
-        store_rows<D, 0>(y, stage, lane, &out_map, cur.t0, int(cur.slice));
-        cur.next();
-    }
-    cp_async_wait<0>();
-    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
-// ------------------------------------- two threads per row (D = 64, 128)
+// ------------------------------------------------------ two threads per row
 
 // Encode + decode of the thread's half of row r (PairMap slots, RoPE removed).
 template <int D, int BITS, bool STRICT>
@@ -113,13 +41,16 @@ __device__ __forceinline__ void pair_round_trip(float (&y)[D / 2], int hf, float
     pair_decode_codes<D, BITS>(blk, cwl, scf, sgn, y);
 }
 
-// Values, and keys without RoPE: a warp per 16-token tile.
-template <int D, int BITS, bool STRICT>
+// Values, keys without RoPE, and keys of head_dim 96 (RoPE from the global
+// table, partners from the tile and by exchange): a warp per 16-token tile.
+template <int D, int BITS, bool STRICT, bool ROPE>
 __global__ void __launch_bounds__(kThreads, 2)
-    roundtrip_pair_kernel(const __half* __restrict__ x, const __grid_constant__ CUtensorMap out_map,
-                          int64_t slices, int tokens, int group) {
-    using PM = PairMap<D>;
+    roundtrip_pair_kernel(const __half* __restrict__ x, const float4* __restrict__ rope,
+                          const __grid_constant__ CUtensorMap out_map, int64_t slices, int tokens, int group) {
+    constexpr int DP = PaddedDim<D>::value;
+    using PM = PairMap<DP>;
     constexpr int HALF = PM::HALF;
+    constexpr int Q = PM::Q;
     constexpr int NBT = PM::NBT;
     using Walk = TileWalkT<kPairRows>;
 
@@ -148,9 +79,29 @@ __global__ void __launch_bounds__(kThreads, 2)
         cp_async_wait<kRtStages - 2>();
         __syncwarp();
         const uint32_t stage = ring + (i % kRtStages) * kPairTileBytes;
+        const int t = cur.t0 + r;
         float y[HALF];
 #pragma unroll
-        for (int c = 0; c < NBT; ++c) h8_to_f(lds128(stage + swz16(r, PM::chunk(hf, c))), &y[8 * c]);
+        for (int c = 0; c < NBT; ++c) {
+            const int gc = PM::chunk(hf, c);
+            if (D == DP || gc < D / 8) {
+                h8_to_f(lds128(stage + swz16(r, gc)), &y[8 * c]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) y[8 * c + j] = 0.0f;
+            }
+        }
+        const float4* cs = ROPE ? rope + (t < tokens ? t : 0) : nullptr;
+        if constexpr (ROPE) {
+            if constexpr (D == DP) {
+#pragma unroll
+                for (int qq = 0; qq < Q / 2; ++qq)
+                    pair_rope_remove<D>(y, qq, __ldg(cs + int64_t(hf * (Q / 2) + qq) * tokens));
+            } else {
+                pair_rope_remove_from_tile<D>(y, hf, stage, r, cs, tokens);
+            }
+        }
+        // the slot of tile i - 1 is refilled next: its store must have read it
         if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
         __syncwarp();
         if (pre.valid()) {
@@ -160,8 +111,17 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         cp_async_commit();
 
-        pair_round_trip<D, BITS, STRICT>(y, hf, sgn, group);
-        pair_store_rows<D, 0>(y, stage, r, hf, lane, &out_map, cur.t0, int(cur.slice));
+        pair_round_trip<DP, BITS, STRICT>(y, hf, sgn, group);
+        if constexpr (ROPE) {
+            if constexpr (D == DP) {
+#pragma unroll
+                for (int qq = 0; qq < Q / 2; ++qq)
+                    pair_rope_apply<D>(y, qq, __ldg(cs + int64_t(hf * (Q / 2) + qq) * tokens), sgn);
+            } else {
+                pair96_rope_apply(y, hf, cs, tokens);
+            }
+        }
+        pair_store_rows<DP, 0>(y, stage, r, hf, lane, &out_map, cur.t0, int(cur.slice));
         cur.next();
     }
     cp_async_wait<0>();
@@ -260,26 +220,23 @@ static int grid_for(K kern, int smem, int threads, int64_t items) {
 template <int D, int BITS, bool STRICT>
 static int launch_rt(const LaunchArgs& a, const __half* x, const float4* rope, const CUtensorMap& map) {
     const int64_t tiles16 = (a.tokens + kPairRows - 1) / kPairRows;
-    if constexpr (D == 96) {
-        auto kern = roundtrip_row_kernel<D, BITS, STRICT>;
-        const int64_t items = a.slices * ((a.tokens + kTileRows - 1) / kTileRows);
-        const int grid = grid_for(kern, kRtRowSmem, kThreads, (items + kWarpsPerBlock - 1) / kWarpsPerBlock);
-        if (grid < 0) return NQ_ERR_CUDA;
-        kern<<<grid, kThreads, kRtRowSmem, a.stream>>>(x, rope, map, a.slices, a.tokens, a.group);
-    } else if (rope != nullptr) {
-        auto kern = roundtrip_pair_rope_kernel<D, BITS, STRICT>;
-        constexpr int smem = RopeRing<D, kRtRopeWarps, kRtRopeStages>::SMEM;
-        const int64_t items = (a.slices + kRtRopeWarps - 1) / kRtRopeWarps * tiles16;
-        const int grid = grid_for(kern, smem, kRtRopeThreads, items);
-        if (grid < 0) return NQ_ERR_CUDA;
-        kern<<<grid, kRtRopeThreads, smem, a.stream>>>(x, rope, map, a.slices, a.tokens, a.group);
-    } else {
-        auto kern = roundtrip_pair_kernel<D, BITS, STRICT>;
-        const int64_t items = a.slices * tiles16;
-        const int grid = grid_for(kern, kRtPairSmem, kThreads, (items + kWarpsPerBlock - 1) / kWarpsPerBlock);
-        if (grid < 0) return NQ_ERR_CUDA;
-        kern<<<grid, kThreads, kRtPairSmem, a.stream>>>(x, map, a.slices, a.tokens, a.group);
+    if constexpr (D != 96) {
+        if (rope != nullptr) {
+            auto kern = roundtrip_pair_rope_kernel<D, BITS, STRICT>;
+            constexpr int smem = RopeRing<D, kRtRopeWarps, kRtRopeStages>::SMEM;
+            const int64_t items = (a.slices + kRtRopeWarps - 1) / kRtRopeWarps * tiles16;
+            const int grid = grid_for(kern, smem, kRtRopeThreads, items);
+            if (grid < 0) return NQ_ERR_CUDA;
+            kern<<<grid, kRtRopeThreads, smem, a.stream>>>(x, rope, map, a.slices, a.tokens, a.group);
+            return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
+        }
     }
+    auto kern = rope != nullptr ? roundtrip_pair_kernel<D, BITS, STRICT, true>
+                                : roundtrip_pair_kernel<D, BITS, STRICT, false>;
+    const int64_t items = a.slices * tiles16;
+    const int grid = grid_for(kern, kRtPairSmem, kThreads, (items + kWarpsPerBlock - 1) / kWarpsPerBlock);
+    if (grid < 0) return NQ_ERR_CUDA;
+    kern<<<grid, kThreads, kRtPairSmem, a.stream>>>(x, rope, map, a.slices, a.tokens, a.group);
     return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
 }
 
@@ -301,8 +258,7 @@ int launch_roundtrip_tensor(const LaunchArgs& a, int head_dim, int bits, bool st
                             const float* rope, void* x_out) {
     if (a.slices == 0 || a.tokens == 0) return NQ_OK;
     CUtensorMap map;
-    const int box_rows = head_dim == 96 ? kTileRows : kPairRows;
-    if (!make_row_tile_map(&map, x_out, head_dim, a.tokens, a.slices, box_rows)) return NQ_ERR_CUDA;
+    if (!make_row_tile_map(&map, x_out, head_dim, a.tokens, a.slices, kPairRows)) return NQ_ERR_CUDA;
     const __half* xh = static_cast<const __half*>(x);
     const float4* r = reinterpret_cast<const float4*>(rope);
     switch (head_dim) {
