@@ -1,14 +1,14 @@
 // nq_encode.cuh -- the encoding steps shared by the compression and the
-// round-trip kernels: tile loads, and per row the zero-padded Hadamard
-// rotation, the group scales and the E8 block codes, for the one-thread-per-row
-// layout (head_dim 96) and the two-threads-per-row layout (64, 128).
+// round-trip kernels (two threads per row): tile loads, the RoPE removal, and
+// per row the zero-padded Hadamard rotation, the group scales and the E8 block
+// codes.
 #pragma once
 
 #include "nq_internal.h"
 
 namespace nq {
 
-// Scaled coordinates u = y * inv of 8-block k of a one-thread row.
+// Scaled coordinates u = y * inv of 8-block k of the thread's coordinates.
 template <int N>
 __device__ __forceinline__ void row_block_u(const float (&y)[N], float inv, int k, float (&u)[8]) {
 #pragma unroll
@@ -19,31 +19,13 @@ __device__ __forceinline__ void row_block_u(const float (&y)[N], float inv, int 
     }
 }
 
-// The same for a two-thread row: slots at or above Q hold the odd thread's
+// With the two-thread layout: slots at or above Q hold the odd thread's
 // negated coordinates, so their reciprocal scale carries the thread's sign.
 template <int Q, int N, int NS>
 __device__ __forceinline__ void pair_block_u(const float (&y)[N], const float (&inv)[NS], float sgn, int k,
                                              float (&u)[8]) {
     const float ik = (8 * k >= Q) ? __fmul_rn(inv[(8 * k) / 32], sgn) : inv[(8 * k) / 32];
     row_block_u(y, ik, k, u);
-}
-
-// Copy the fp16 rows of a 32-row tile into a stage; rows past the chunk are
-// zeros.
-template <int D>
-__device__ __forceinline__ void load_tile(const __half* __restrict__ x, const TileWalk& w, uint32_t stage,
-                                          int lane) {
-    constexpr int CPR = D / 8;  // 16-byte chunks per row
-    const int nvalid = min(kTileRows, w.t_end - w.t0);
-    const __half* base = x + (w.slice * w.tokens + w.t0) * int64_t(D);
-#pragma unroll
-    for (int i = 0; i < CPR; ++i) {
-        const int g = lane + 32 * i;
-        const int r = g / CPR;
-        const int c = g - r * CPR;
-        const bool ok = r < nvalid;
-        cp_async16(stage + swz(r, c), ok ? base + 8 * g : base, ok ? 16 : 0);
-    }
 }
 
 // Copy the fp16 rows of a 16-row tile into a stage (rows past the slice are
@@ -61,77 +43,6 @@ __device__ __forceinline__ void load_pair_tile(const __half* __restrict__ x, int
         const int c = g - r * CPR;
         const bool ok = r < nvalid;
         cp_async16(stage + swz16(r, c), ok ? base + 8 * g : base, ok ? 16 : 0);
-    }
-}
-
-// Rotation, group scales and E8 codes of a one-thread row (y zero-padded to
-// Dp): block codes, coset word (bit k = block k) and the fp16 scale bits of the
-// row's 32-subgroups.
-template <int D, int BITS, bool STRICT>
-__device__ __forceinline__ void row_encode_codes(float (&y)[PaddedDim<D>::value], int group,
-                                                 unsigned (&blk)[PaddedDim<D>::value / 8], unsigned& cw,
-                                                 unsigned short (&sc)[PaddedDim<D>::value / 32]) {
-    constexpr int DP = PaddedDim<D>::value;
-    constexpr int NB = DP / 8;
-    constexpr int NSUB = DP / 32;
-    using C = Code<BITS>;
-    constexpr float STEP = float(DP) * C::H;
-
-    // ---- Hadamard rotation (compression stage order)
-    fwht_forward<DP>(y);
-
-    // ---- group absmax -> fp16 scale -> reciprocal (per 32-subgroup)
-    float amax[NSUB];
-#pragma unroll
-    for (int s = 0; s < NSUB; ++s) {
-        float m = 0.0f;
-#pragma unroll
-        for (int j = 32 * s; j < 32 * s + 32; j += 2) m = fmax3(m, fabsf(y[j]), fabsf(y[j + 1]));
-        amax[s] = m;
-    }
-    if (group >= 64) {
-#pragma unroll
-        for (int s = 0; s < NSUB; s += 2) amax[s] = amax[s + 1] = fmaxf(amax[s], amax[s + 1]);
-    }
-    if (group >= 128 && NSUB == 4) {
-        const float m = fmaxf(amax[0], amax[2]);
-#pragma unroll
-        for (int s = 0; s < NSUB; ++s) amax[s] = m;
-    }
-    float inv[NSUB];
-    bool fast = true;
-#pragma unroll
-    for (int s = 0; s < NSUB; ++s) {
-        sc[s] = group_scale(amax[s], STEP, 1.0f / STEP);
-        const float scf = __half2float(__ushort_as_half(sc[s]));
-        inv[s] = sc[s] ? __frcp_rn(__fmul_rn(scf, float(DP))) : 0.0f;
-        fast = fast && (__fmul_rn(amax[s], inv[s]) < C::H);
-    }
-
-    // ---- E8 nearest point per 8-block -> block codes
-    unsigned declined = 0;
-    cw = 0;
-#pragma unroll
-    for (int k = 0; k < NB; ++k) {
-        float u[8];
-        row_block_u(y, inv[k / 4], k, u);
-        unsigned c;
-        const bool ok = e8_fast<BITS, STRICT>(u, blk[k], c);
-        cw |= c << k;
-        declined |= unsigned(!ok) << k;
-    }
-    if (!fast) declined = (1u << NB) - 1u;
-    if (declined) {
-#pragma unroll
-        for (int k = 0; k < NB; ++k) {
-            if (!((declined >> k) & 1u)) continue;
-            float u[8];
-            row_block_u(y, inv[k / 4], k, u);
-            const uint2 res = e8_slow<BITS, STRICT>(make_float4(u[0], u[1], u[2], u[3]),
-                                                    make_float4(u[4], u[5], u[6], u[7]));
-            blk[k] = res.x;
-            cw = (cw & ~(1u << k)) | (res.y << k);
-        }
     }
 }
 
@@ -242,20 +153,6 @@ __device__ __forceinline__ float4 rope_tile_entry(uint32_t stage, int q, int rr)
     const uint4 raw = lds128(stage + rope_slot<D>(q, rr));
     return make_float4(__uint_as_float(raw.x), __uint_as_float(raw.y), __uint_as_float(raw.z),
                        __uint_as_float(raw.w));
-}
-
-// RoPE removal, one-thread row: rotate the pairs (2q, 2q + D/2) and
-// (2q + 1, 2q + 1 + D/2) by -angle; cs = (cos, sin) of both pairs.
-template <int D, int N>
-__device__ __forceinline__ void row_rope_remove(float (&y)[N], int q, float4 cs) {
-#pragma unroll
-    for (int p = 0; p < 2; ++p) {
-        const int j = 2 * q + p;
-        const float c = p ? cs.z : cs.x, s = p ? cs.w : cs.y;
-        const float a = y[j], b = y[j + D / 2];
-        y[j] = __fmaf_rn(a, c, __fmul_rn(b, s));
-        y[j + D / 2] = __fmaf_rn(b, c, -__fmul_rn(a, s));
-    }
 }
 
 // RoPE removal of one member of two consecutive pairs given the raw partner
