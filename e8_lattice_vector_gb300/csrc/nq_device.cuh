@@ -5,10 +5,13 @@
 // and the library is built with --fmad=false, so the compiler fuses nothing on
 // its own.  The op order is the one the method's steps define:
 //   RoPE removal   x_i' = fma(x_i, c, x_j*s),  x_j' = fma(x_j, c, -(x_i*s))
-//   Hadamard       textbook butterflies, stages h = 1, 2, 4, ..., Dp/2
+//   Hadamard       butterflies (a + b, a - b); compression runs the stages
+//                  h = 1, ..., Dp/8, Dp/2, Dp/4, decompression h = 1, ..., Dp/2
 //   scaling        u = y * inv,  inv = 1 / (sc * Dp)
 //   E8 distances   d = fma(e_j, e_j, d) over j = 0..7, plus 1 - 2*score for a
-//                  parity fix-up, as fma(-2, score, 1) added to d.
+//                  parity fix-up, as fma(-2, score, 1) added to d (the fast
+//                  path reaches the same coset choice from an estimate whose
+//                  sign provably agrees outside a narrow band; see e8_fast).
 #pragma once
 
 #include <cuda_fp16.h>
@@ -127,16 +130,6 @@ __device__ __forceinline__ void fwht(float (&y)[N]) {
     for (int h = 1; h < N; h *= 2) fwht_stage<N>(y, h);
 }
 
-// The compression direction: the textbook order with its last two stages
-// exchanged (h = 1, ..., N/8, then N/2, then N/4).
-template <int N>
-__device__ __forceinline__ void fwht_forward(float (&y)[N]) {
-#pragma unroll
-    for (int h = 1; h < N / 4; h *= 2) fwht_stage<N>(y, h);
-    fwht_stage<N>(y, N / 2);
-    fwht_stage<N>(y, N / 4);
-}
-
 // Butterfly stage on slot pairs (l, l + Q) with a per-thread sign:
 // (P, Q) -> (P + sgn*Q, P - sgn*Q).  fma(x, +-1, y) is exactly y +- x, so with
 // sgn = +1 this is the plain butterfly and with sgn = -1 it is the butterfly
@@ -185,12 +178,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
     return r;
 }
-__device__ __forceinline__ float fmin3(float a, float b, float c) {
-    float r;
-    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-    return r;
-}
-
 // ------------------------------------------------------------------- scale
 
 // Smallest binary16 v with v * step >= amax (step = Dp * (2^b - 1) / 2), as
@@ -464,14 +451,6 @@ __device__ __forceinline__ unsigned f2_to_h2_sat(float lo, float hi) {
 __device__ __forceinline__ uint4 f_to_h8(const float* y) {
     return make_uint4(f2_to_h2_sat(y[0], y[1]), f2_to_h2_sat(y[2], y[3]), f2_to_h2_sat(y[4], y[5]),
                       f2_to_h2_sat(y[6], y[7]));
-}
-
-__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
 }
 
 __device__ __forceinline__ void st_stream(uint4* p, const uint4& v) {
