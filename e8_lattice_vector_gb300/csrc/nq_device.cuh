@@ -341,11 +341,10 @@ __device__ __forceinline__ bool e8_fast(const float (&u)[8], unsigned& code, uns
     // moves up) or +2*cs_k*L^k to the half-integer code.  k is found on the FMA
     // pipe: i_j = sat(1 - (smax - s_j) * 2^127) is 1 at a maximum and 0
     // elsewhere (with smax > 2^-100, distinct scores differ by at least 2^-123),
-    // and G = sum_j i_j cs_j L^j picks cs_k L^k.  A tie (sum i != 1) goes to the
-    // general path.  Computed for every block (no branch), applied if needed.
+    // and G = sum_j i_j cs_j L^j picks cs_k L^k.  A tie goes to the general
+    // path.  Computed for every block (no branch), applied if needed.
     const bool fix = half ? odd1 : odd0;
     const float smax = half ? smax1 : smax0;
-    float2 cnt = make_float2(0.0f, 0.0f);
     float2 G[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
     for (int j = 0; j < 8; j += 2) {
@@ -355,13 +354,18 @@ __device__ __forceinline__ bool e8_fast(const float (&u)[8], unsigned& code, uns
         float2 ind;
         asm("fma.rn.sat.f32 %0, %1, 0fFF000000, 0f3F800000;" : "=f"(ind.x) : "f"(dlt.x));
         asm("fma.rn.sat.f32 %0, %1, 0fFF000000, 0f3F800000;" : "=f"(ind.y) : "f"(dlt.y));
-        cnt = __fadd2_rn(cnt, ind);
         const float2 cl = __fmul2_rn(make_float2(csv[j], csv[j + 1]), make_float2(Lp[j & 3], Lp[(j & 3) + 1]));
         G[j >> 2] = __ffma2_rn(ind, cl, G[j >> 2]);
     }
-    ok = ok && (!fix || (smax > 7.88860905e-31f && __fadd_rn(cnt.x, cnt.y) == 1.0f));  // 2^-100
+    const float G0 = __fadd_rn(G[0].x, G[0].y), G1 = __fadd_rn(G[1].x, G[1].y);
+    // A unique maximum leaves one term +-L^k / 2, a power of two, in exactly one
+    // half-block; ties leave sums of distinct +-L^j / 2 (L >= 4), which are
+    // never powers of two, or terms in both halves.
+    const bool one = (G0 == 0.0f) != (G1 == 0.0f);
+    const bool pow2 = (__float_as_uint(__fadd_rn(G0, G1)) & 0x7fffffu) == 0u;
+    ok = ok && (!fix || (smax > 7.88860905e-31f && one && pow2));  // 2^-100
     const float m = fix ? (half ? 2.0f : -2.0f) : 0.0f;
-    const float g[2] = {__fmul_rn(m, __fadd_rn(G[0].x, G[0].y)), __fmul_rn(m, __fadd_rn(G[1].x, G[1].y))};
+    const float g[2] = {__fmul_rn(m, G0), __fmul_rn(m, G1)};
 
     // integer codes m0 = r0 + (L/2 - 1), half-integer codes m1 = r1 + (L - 1)/2,
     // per half-block an exact integer below 2^16 in the low bits of 2^23 + m
