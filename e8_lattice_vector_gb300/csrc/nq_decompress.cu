@@ -39,6 +39,99 @@ __device__ __forceinline__ void load_records(const uint8_t* __restrict__ idx, co
     if (lane < nsch) cp_async16(stage + kRecScale + 16 * lane, scales + row0 * nsc + 8 * lane, 16);
 }
 
+// ------------------------------------------- temporal delta, tile-wise
+//
+// The delta is undone in place on the 32-row idx tile in shared memory, down
+// its columns: lane l takes column unit l % NU (a 32-bit word of 16 two-bit or
+// 8 four-bit fields, or a 3-word group holding four 24-bit block codes at 3
+// bits) of the rows of segment l / NU; it forms the running field-wise sums
+// (mod 2^b) down its segment, adds the exclusive sum of the segments above
+// (a shuffle scan over the segments) and the carry of the chunk's earlier
+// tiles, and writes the codes back.  Far fewer shuffles and additions than a
+// 32-lane scan of every block of every row.
+template <int BITS>
+struct DeltaUnit;
+template <>
+struct DeltaUnit<2> {  // one word, 16 fields
+    static constexpr int U = 1, NV = 1;
+    __device__ static void load(uint32_t a, unsigned (&v)[NV]) { v[0] = lds32(a); }
+    __device__ static void store(uint32_t a, const unsigned (&v)[NV]) { sts32(a, v[0]); }
+    __device__ static unsigned add(unsigned a, unsigned b) { return swar_add_word2(a, b); }
+};
+template <>
+struct DeltaUnit<4> {  // one word = one block of 8 fields
+    static constexpr int U = 1, NV = 1;
+    __device__ static void load(uint32_t a, unsigned (&v)[NV]) { v[0] = lds32(a); }
+    __device__ static void store(uint32_t a, const unsigned (&v)[NV]) { sts32(a, v[0]); }
+    __device__ static unsigned add(unsigned a, unsigned b) { return swar_add<4>(a, b); }
+};
+template <>
+struct DeltaUnit<3> {  // three words = four 24-bit blocks (fields straddle the words)
+    static constexpr int U = 3, NV = 4;
+    __device__ static void load(uint32_t a, unsigned (&v)[NV]) {
+        const unsigned w0 = lds32(a), w1 = lds32(a + 4), w2 = lds32(a + 8);
+        v[0] = w0 & 0xffffffu;
+        v[1] = (w0 >> 24) | ((w1 & 0xffffu) << 8);
+        v[2] = (w1 >> 16) | ((w2 & 0xffu) << 16);
+        v[3] = w2 >> 8;
+    }
+    __device__ static void store(uint32_t a, const unsigned (&v)[NV]) {
+        sts32(a, v[0] | (v[1] << 24));
+        sts32(a + 4, (v[1] >> 8) | (v[2] << 16));
+        sts32(a + 8, (v[2] >> 16) | (v[3] << 8));
+    }
+    __device__ static unsigned add(unsigned a, unsigned b) { return swar_add<3>(a, b); }
+};
+
+// rows: shared address of row 0 of the tile's idx rows (RB bytes each);
+// carry: the lane's unit in the previous tile's last row (unused when first).
+template <int BITS, int RB>
+__device__ __forceinline__ void undelta_tile(uint32_t rows, int lane, bool first,
+                                             unsigned (&carry)[DeltaUnit<BITS>::NV]) {
+    using DU = DeltaUnit<BITS>;
+    constexpr int NV = DU::NV;
+    constexpr int NU = RB / (4 * DU::U);  // units per row
+    constexpr int SEGS = 32 / NU;
+    constexpr int RPS = 32 / SEGS;         // rows per segment
+    static_assert(NU * SEGS == 32 && RPS * SEGS == 32, "tile split");
+    const int u = lane % NU, sg = lane / NU;
+    const uint32_t base = rows + uint32_t(sg * RPS * RB + 4 * DU::U * u);
+    unsigned v[RPS][NV];
+#pragma unroll
+    for (int i = 0; i < RPS; ++i) DU::load(base + i * RB, v[i]);
+#pragma unroll
+    for (int i = 1; i < RPS; ++i)
+#pragma unroll
+        for (int n = 0; n < NV; ++n) v[i][n] = DU::add(v[i][n], v[i - 1][n]);
+    unsigned run[NV], ex[NV];
+#pragma unroll
+    for (int n = 0; n < NV; ++n) run[n] = v[RPS - 1][n];
+#pragma unroll
+    for (int d = 1; d < SEGS; d *= 2) {
+#pragma unroll
+        for (int n = 0; n < NV; ++n) {
+            const unsigned t = __shfl_up_sync(kFull, run[n], d * NU);
+            if (sg >= d) run[n] = DU::add(run[n], t);
+        }
+    }
+#pragma unroll
+    for (int n = 0; n < NV; ++n) {
+        ex[n] = __shfl_up_sync(kFull, run[n], NU);
+        if (sg == 0) ex[n] = 0u;
+        if (!first) ex[n] = DU::add(ex[n], carry[n]);
+    }
+#pragma unroll
+    for (int i = 0; i < RPS; ++i) {
+#pragma unroll
+        for (int n = 0; n < NV; ++n) v[i][n] = DU::add(v[i][n], ex[n]);
+        DU::store(base + i * RB, v[i]);
+    }
+#pragma unroll
+    for (int n = 0; n < NV; ++n) carry[n] = __shfl_sync(kFull, v[RPS - 1][n], u + (SEGS - 1) * NU);
+}
+
+// One record row (the lane's row of a 32-row record tile in `stage`) ->
+// unscaled, inverse-transformed coordinates, before the RoPE re-apply.
 template <int D, int BITS, bool JOINT>
 __device__ __forceinline__ void decode_row(uint32_t stage, const uint8_t* stage_gen, int lane, int nsc, int gshift,
                                            bool delta, bool first,
@@ -49,6 +142,18 @@ __device__ __forceinline__ void decode_row(uint32_t stage, const uint8_t* stage_
     using C = Code<BITS>;
     using RP = RowPack<BITS, NB>;
     constexpr int RB = DP * BITS / 8;
+
+    // ---- undo the temporal delta of the idx tile in place (every lane takes part)
+    if (delta) {
+        constexpr int NV = DeltaUnit<BITS>::NV;
+        unsigned cu[NV];
+#pragma unroll
+        for (int n = 0; n < NV; ++n) cu[n] = carry[n];
+        undelta_tile<BITS, RB>(stage + kRecIdx, lane, first, cu);
+#pragma unroll
+        for (int n = 0; n < NV; ++n) carry[n] = cu[n];
+        __syncwarp();
+    }
 
     // ---- the lane's record
     unsigned w[RP::WORDS];
@@ -76,35 +181,19 @@ __device__ __forceinline__ void decode_row(uint32_t stage, const uint8_t* stage_
     for (int s = 0; s < DP / 32; ++s)
         scf[s] = __half2float(__ushort_as_half(stage_h[kRecScale / 2 + lane * nsc + ((32 * s) >> gshift)]));
     __syncwarp();  // the stage may be refilled
-
-    // ---- undo the temporal delta: inclusive scan over the tile + carry.  At
-    // 2 bits the fields never straddle a word, so the scan runs on the packed
-    // words (16 fields each, half the shuffles); otherwise on the block codes.
-    constexpr bool BY_WORD = BITS == 2;
-    constexpr int NS = BY_WORD ? RP::WORDS : NB;
     unsigned blk[NB];
-    if constexpr (!BY_WORD) RP::unpack(w, blk);
-    unsigned* sv = BY_WORD ? w : blk;
-    if (delta) {
+    RP::unpack(w, blk);
+
+    // ---- the coset words' delta: an exclusive-or scan over the tile + carry
+    if (delta && !JOINT) {
 #pragma unroll
         for (int off = 1; off < 32; off *= 2) {
-#pragma unroll
-            for (int k = 0; k < NS; ++k) {
-                const unsigned v = __shfl_up_sync(kFull, sv[k], off);
-                if (lane >= off) sv[k] = BY_WORD ? swar_add_word2(sv[k], v) : swar_add<BITS>(sv[k], v);
-            }
             const unsigned vc = __shfl_up_sync(kFull, cw, off);
             if (lane >= off) cw ^= vc;
-        }
-#pragma unroll
-        for (int k = 0; k < NS; ++k) {
-            if (!first) sv[k] = BY_WORD ? swar_add_word2(sv[k], carry[k]) : swar_add<BITS>(sv[k], carry[k]);
-            carry[k] = __shfl_sync(kFull, sv[k], 31);
         }
         if (!first) cw ^= carry_c;
         carry_c = __shfl_sync(kFull, cw, 31);
     }
-    if constexpr (BY_WORD) RP::unpack(w, blk);
 
     if constexpr (JOINT) {  // strict joint format: the coset bits come out of the block codes
 #pragma unroll
