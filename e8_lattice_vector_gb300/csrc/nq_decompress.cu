@@ -1,16 +1,19 @@
-// nq_decompress.cu -- fused decompression kernel: idx / coset / scale sections
-// -> undo temporal delta -> unpack -> unscale -> inverse Hadamard -> RoPE
-// re-apply (keys) -> fp16 rows.
+// nq_decompress.cu -- fused decompression kernels: idx / coset / scale
+// sections -> undo temporal delta -> unpack -> unscale -> inverse Hadamard ->
+// RoPE re-apply (keys) -> fp16 rows.
 //
-// Same work layout as compression: a warp per 32-token tile of a slice, lane r
-// owns row r.  A tile's records (idx rows, coset words, scales) are contiguous
-// and 16-byte aligned thanks to the per-slice padding of the record rows, so
-// they stream through a 3-stage shared-memory ring by cp.async.  The delta is
-// undone by an inclusive warp scan (field-wise addition modulo 2^b,
-// exclusive-or for the coset word) plus the running total of the chunk's
-// earlier tiles.  The reconstructed fp16 rows are written into a swizzled
-// shared-memory tile and leave by one TMA tensor store per 64 columns, which
-// clips the rows past the end of the slice and the columns past head_dim.
+// head_dim 96 / 128: a warp per 32-token tile of a slice, lane r owns row r
+// (one thread per row; for the decode this beats two threads per row).  A
+// tile's records (idx rows, coset words, scales) are contiguous and 16-byte
+// aligned thanks to the per-slice padding of the record rows, so they stream
+// through a 3-stage shared-memory ring by cp.async; keys run in blocks of
+// warps that also stage the tile's RoPE table rows once for the block.  The
+// delta is undone in place on the record tile, column-wise (field-wise
+// addition modulo 2^b), plus the running total of the chunk's earlier tiles;
+// the coset words by an exclusive-or warp scan.  The reconstructed fp16 rows
+// are written into a swizzled shared-memory tile and leave by one TMA tensor
+// store per 64 columns, which clips the rows past the end of the slice and the
+// columns past head_dim.  head_dim 64 uses two threads per row (16-row tiles).
 #include "nq_decode.cuh"
 
 namespace nq {
