@@ -42,14 +42,17 @@ bool ensure_smem(const void* kernel, int smem);
 // 64 columns x box_rows tokens x 1 slice, 128-byte swizzle.  false on failure.
 bool make_row_tile_map(CUtensorMap* map, void* base, int head_dim, int tokens, int64_t slices, int box_rows);
 
+// One tensor (K or V) of a call.  mode: 0 relaxed, 1 strict, 2 strict joint
+// format (coset == nullptr: no coset words).  rope: device table or nullptr.
 int launch_compress_tensor(const LaunchArgs& a, int head_dim, int bits, int mode, const void* x,
                            const float* rope, uint8_t* idx, uint16_t* coset, uint16_t* scales);
-
+// coset == nullptr: the joint format.
 int launch_decompress_tensor(const LaunchArgs& a, int head_dim, int bits, const uint8_t* idx,
                              const uint16_t* coset, const uint16_t* scales, const float* rope,
                              void* x_out);
 int launch_roundtrip_tensor(const LaunchArgs& a, int head_dim, int bits, bool strict, const void* x,
                             const float* rope, void* x_out);
+// Adds one tensor's symbol counts to counts[0, NQ_HIST_BINS) (zeroed by the caller).
 int launch_code_histogram(const LaunchArgs& a, int padded_dim, int bits, const uint8_t* idx,
                           const uint16_t* coset, uint64_t* counts);
 
