@@ -1,0 +1,38 @@
+"""bench.py's reference arm (the CPU oracle) keeps the JSON-line contract; runs
+on the host only."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.mark.timeout(600)
+def test_reference_arm_prints_one_json_line(tmp_path):
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "tiny",
+           "--steps", "2", "--warmup", "1", "--cpu-seconds", "1"]
+    r = subprocess.run(cmd, capture_output=True, text=True, cwd=str(tmp_path), timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    out = json.loads(lines[0])
+    assert out["impl"] == "reference"
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in out, key
+    assert out["value"] > 0 and out["unit"] == "GB/s" and out["steps"] == 2
+    cb = out["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == out["value"]
+    assert out["e2e"]["h2d_bytes_per_step"] == 0 and out["e2e"]["value"] == out["value"]
+
+
+def test_whole_job_rate_and_peak_helpers():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    assert bench.whole_job_gbs(4, 1e9, 500.0) == pytest.approx(8.0)
+    peak, kind = bench._peak_hbm()
+    assert peak > 0 and kind in ("measured", "fallback")

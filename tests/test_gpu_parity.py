@@ -466,3 +466,24 @@ def test_full_size_joint_format(nq, orc, name, kb, vb):
             assert _same_values(xr2[n], ref), (t_name, r)
     del buf, K2, V2
     torch.cuda.empty_cache()
+
+
+def test_entropy_report_on_the_tiny_cache(nq):
+    """The entropy report runs end to end on device counts: every field of every
+    real row is counted, and order-0 entropies stay within [0, b] bits."""
+    from e8_lattice_vector_gb300 import CodecParams
+    from e8_lattice_vector_gb300.entropy import report
+    from e8_lattice_vector_gb300.synth import CONFIGS, make_cache
+
+    cfg = CONFIGS["tiny"]
+    K, V = make_cache(cfg, device="cuda")
+    rope = nq.RopeTable.build(cfg.tokens, cfg.head_dim, 1e4)
+    for delta in (0, 32):
+        p = CodecParams(3, 2, 64, 0, delta, 1e4)
+        rep = report(K, V, p, rope)
+        for t, bits in (("k", 3), ("v", 2)):
+            r = rep[t]
+            assert r["fields"] == cfg.rows * 128
+            assert 0.0 < r["field_entropy_bits"] <= bits
+            assert 0.0 <= r["byte_entropy_bits_per_byte"] <= 8.0
+            assert r["raw_bits_per_coord"] == pytest.approx(bits + 1 / 8 + 16 * 2 / 128)
