@@ -86,17 +86,17 @@ struct DeltaUnit<3> {  // three words = four 24-bit blocks (fields straddle the 
     __device__ static unsigned add(unsigned a, unsigned b) { return swar_add<3>(a, b); }
 };
 
-// rows: shared address of row 0 of the tile's idx rows (RB bytes each);
+// rows: shared address of row 0 of the tile's ROWS idx rows (RB bytes each);
 // carry: the lane's unit in the previous tile's last row (unused when first).
-template <int BITS, int RB>
+template <int BITS, int RB, int ROWS = 32>
 __device__ __forceinline__ void undelta_tile(uint32_t rows, int lane, bool first,
                                              unsigned (&carry)[DeltaUnit<BITS>::NV]) {
     using DU = DeltaUnit<BITS>;
     constexpr int NV = DU::NV;
     constexpr int NU = RB / (4 * DU::U);  // units per row
     constexpr int SEGS = 32 / NU;
-    constexpr int RPS = 32 / SEGS;         // rows per segment
-    static_assert(NU * SEGS == 32 && RPS * SEGS == 32, "tile split");
+    constexpr int RPS = ROWS / SEGS;       // rows per segment
+    static_assert(NU * SEGS == 32 && RPS * SEGS == ROWS, "tile split");
     const int u = lane % NU, sg = lane / NU;
     const uint32_t base = rows + uint32_t(sg * RPS * RB + 4 * DU::U * u);
     unsigned v[RPS][NV];
@@ -489,6 +489,19 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint8_t* gstage = gbase + (stage - base);
         const int t = cur.t0 + r;
 
+        // ---- undo the temporal delta of the idx tile in place (every lane takes part)
+        const bool first = cur.t0 == cur.t_begin;
+        if (delta) {
+            constexpr int NV = DeltaUnit<BITS>::NV;
+            unsigned cu[NV];
+#pragma unroll
+            for (int n = 0; n < NV; ++n) cu[n] = carry[n];
+            undelta_tile<BITS, RB, kPairRows>(stage + kPairRecIdx, lane, first, cu);
+#pragma unroll
+            for (int n = 0; n < NV; ++n) carry[n] = cu[n];
+            __syncwarp();
+        }
+
         // ---- the thread's half of the record
         unsigned w[RP::WORDS];
         lds_words<RBT>(stage + kPairRecIdx + r * RB + hf * RBT, w);
@@ -502,23 +515,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         unsigned blk[NBT];
         RP::unpack(w, blk);
 
-        // ---- undo the temporal delta: inclusive scan over rows (lane stride 2) + carry
-        if (delta) {
+        // ---- the coset words' delta: an exclusive-or scan over the rows (lane stride 2) + carry
+        if (delta && !JOINT) {
 #pragma unroll
             for (int off = 2; off < 32; off *= 2) {
-#pragma unroll
-                for (int k = 0; k < NBT; ++k) {
-                    const unsigned v = __shfl_up_sync(kFull, blk[k], off);
-                    if (lane >= off) blk[k] = swar_add<BITS>(blk[k], v);
-                }
                 const unsigned vc = __shfl_up_sync(kFull, cw, off);
                 if (lane >= off) cw ^= vc;
-            }
-            const bool first = cur.t0 == cur.t_begin;
-#pragma unroll
-            for (int k = 0; k < NBT; ++k) {
-                if (!first) blk[k] = swar_add<BITS>(blk[k], carry[k]);
-                carry[k] = __shfl_sync(kFull, blk[k], 30 + hf);
             }
             if (!first) cw ^= carry_c;
             carry_c = __shfl_sync(kFull, cw, 30 + hf);
