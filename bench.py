@@ -313,11 +313,14 @@ def run_ours(a):
         "decompress": {"ms": round(decomp_avg, 4), "gbs": round(alg_bytes / (decomp_avg * 1e-3) / 1e9, 1),
                        "launches": "key + value"},
     }
+    for kname in kernels:
+        kernels[kname]["frac_of_peak"] = round(kernels[kname]["gbs"] / peak, 4)
     dom = "compress" if comp_avg >= decomp_avg else "decompress"
     achieved = kernels[dom]["gbs"]
     trec = _traffic_record(dom) if a.config == "llama31_8b" else None
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                "frac_of_nominal_8000": round(achieved / 8000.0, 4),
                 "traffic": (int(trec["dram_bytes_per_call"]) if trec else None),
                 "algorithmic_bytes": int(alg_bytes)}
 
