@@ -299,8 +299,9 @@ def run_ours(a):
     # ---- algorithmic bytes and roofline
     rows = cfg.rows
     fp16_row = cfg.head_dim * 2
-    rec_row = {"k": lay.k_idx_row_bytes + 2 + lay.scales_per_row * 2,
-               "v": lay.v_idx_row_bytes + 2 + lay.scales_per_row * 2}
+    cos_row = 0 if int(params.strict) == 2 else 2  # the joint format has no coset words
+    rec_row = {"k": lay.k_idx_row_bytes + cos_row + lay.scales_per_row * 2,
+               "v": lay.v_idx_row_bytes + cos_row + lay.scales_per_row * 2}
     alg_bytes = rows * (2 * fp16_row + rec_row["k"] + rec_row["v"])  # one direction, K + V
     comp_avg = sum(comp_ms) / len(comp_ms)
     decomp_avg = sum(decomp_ms) / len(decomp_ms)
