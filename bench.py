@@ -40,6 +40,7 @@ def _args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="llama31_8b")
     ap.add_argument("--strict", action="store_true", help="strict E8 parity instead of relaxed")
+    ap.add_argument("--joint", action="store_true", help="strict E8 in the joint 8b-bit format (no coset words)")
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--fused-steps", type=int, default=10, help="timed nq_roundtrip_kv calls (0: skip)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
@@ -74,6 +75,19 @@ def _traffic_record(kernel):
     except Exception:
         pass
     return None
+
+
+def _pick_params(cfg, a):
+    """The config's first codec mode with the requested parity; --joint turns it
+    into the strict joint format."""
+    strict = a.strict or a.joint
+    params = ([m for m in cfg.modes if bool(m.strict) == strict] or list(cfg.modes))[0]
+    if a.joint:
+        from e8_lattice_vector_gb300 import CodecParams
+
+        params = CodecParams(params.key_bits, params.value_bits, params.group_size, 2, params.delta_chunk,
+                             params.rope_theta)
+    return params
 
 
 class ClockSampler:
@@ -173,8 +187,7 @@ def run_ours(a):
     from e8_lattice_vector_gb300.synth import CONFIGS, make_cache
 
     cfg = CONFIGS[a.config]
-    params = [m for m in cfg.modes if bool(m.strict) == a.strict] or list(cfg.modes)
-    params = params[0]
+    params = _pick_params(cfg, a)
     K, V = make_cache(cfg, device=dev)
     rope = nq.RopeTable.build(cfg.tokens, cfg.head_dim, params.rope_theta, device=dev)
     lay = nq.plan(cfg.shape, params)
@@ -343,7 +356,7 @@ def run_ours(a):
         "config": {
             "workload": "%s KV cache %s fp16, K%dV%d group %d %s E8, delta %s, compress+decompress round trip"
                         % (cfg.name, list(cfg.shape), params.key_bits, params.value_bits, params.group_size,
-                           "strict" if params.strict else "relaxed", params.delta_chunk or "off"),
+                           {0: "relaxed", 1: "strict", 2: "strict (joint format)"}[int(params.strict)], params.delta_chunk or "off"),
             "fp16_bytes_per_direction": cfg.fp16_bytes,
             "l2": "inputs (%.1f GiB) larger than L2; no flush" % (cfg.fp16_bytes / 2 ** 30),
             "parallelism": "replicas" if world > 1 else "single",
@@ -501,8 +514,7 @@ def run_reference(a):
     from e8_lattice_vector_gb300.synth import CONFIGS
 
     cfg = CONFIGS[a.config]
-    params = [m for m in cfg.modes if bool(m.strict) == a.strict] or list(cfg.modes)
-    params = params[0]
+    params = _pick_params(cfg, a)
     from e8_lattice_vector_gb300.synth import layer_kv
 
     k, v = layer_kv(cfg, 0, device="cpu", batch=1)
@@ -533,7 +545,7 @@ def run_reference(a):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": "%s KV cache (sampled), K%dV%d group %d %s E8" % (
             cfg.name, params.key_bits, params.value_bits, params.group_size,
-            "strict" if params.strict else "relaxed")},
+            {0: "relaxed", 1: "strict", 2: "strict (joint format)"}[int(params.strict)])},
         "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
