@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         __syncwarp();  // every lane has read its coordinates: the stage may be refilled
 
-        pair_encode_row<DP, BITS, MODE>(y, hf, r, sgn, t, active, delta, cur.t0 == cur.t_begin, cur.t_begin,
+        pair_encode_row<DP, BITS, MODE>(y, hf, r, sgn, t, active, delta, cur.t0 == cur.t_begin(), cur.t_begin(),
                                          cur.slice * tpad + t, group, carry, carry_c, idx, coset, scales);
         cur.next();
     }
@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(kCompressRopeThreads, 2)
             // RoPE removal with the block's table tile: pairs (i, i + D/2) are slots (l, l + Q)
 #pragma unroll
             for (int qq = 0; qq < Q / 2; ++qq) pair_rope_remove<D>(y, qq, rope_tile_entry<D>(stage, hf * (Q / 2) + qq, r));
-            pair_encode_row<D, BITS, MODE>(y, hf, r, sgn, t, active, delta, cur.t0 == cur.t_begin, cur.t_begin,
+            pair_encode_row<D, BITS, MODE>(y, hf, r, sgn, t, active, delta, cur.t0 == cur.t_begin(), cur.t_begin(),
                                              slice * tpad + t, group, carry, carry_c, idx, coset, scales);
         }
         cur.next();

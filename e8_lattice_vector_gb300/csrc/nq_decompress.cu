@@ -259,12 +259,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         const uint8_t* stage_gen = smem + (stage - smem_u32(smem));
         float y[DP];
-        decode_row<D, BITS, JOINT>(stage, stage_gen, lane, nsc, gshift, delta, cur.t0 == cur.t_begin, carry, carry_c,
+        decode_row<D, BITS, JOINT>(stage, stage_gen, lane, nsc, gshift, delta, cur.t0 == cur.t_begin(), carry, carry_c,
                                    y);
 
         // ---- RoPE re-apply on keys: rotate each (i, i + D/2) pair by +angle
         if (rope != nullptr) {
-            const float4* cs = rope + (t < cur.t_end ? t : cur.t_begin);  // [D/4][tokens]
+            const float4* cs = rope + (t < cur.t_end() ? t : cur.t_begin());  // [D/4][tokens]
 #pragma unroll
             for (int q = 0; q < D / 4; ++q) rope_apply_pairs<D>(y, q, __ldg(cs + int64_t(q) * tokens));
         }
@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(kKeyThreads, 1)
             const uint32_t rec = stage + KS::TABLE + wib * kRecStage;
             float y[DP];
             decode_row<D, BITS, JOINT>(rec, gbase + (rec - base), lane, nsc, gshift, delta,
-                                       cur.t0 == cur.t_begin, carry, carry_c, y);
+                                       cur.t0 == cur.t_begin(), carry, carry_c, y);
 #pragma unroll
             for (int q = 0; q < D / 4; ++q) {
                 const uint4 raw = lds128(stage + 16 * (q * kTileRows + lane));
@@ -490,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int t = cur.t0 + r;
 
         // ---- undo the temporal delta of the idx tile in place (every lane takes part)
-        const bool first = cur.t0 == cur.t_begin;
+        const bool first = cur.t0 == cur.t_begin();
         if (delta) {
             constexpr int NV = DeltaUnit<BITS>::NV;
             unsigned cu[NV];
@@ -540,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
         // ---- RoPE re-apply on keys: pairs (i, i + D/2) are slots (l, l + Q)
         if (rope != nullptr) {
-            const float4* cs = rope + (t < cur.t_end ? t : cur.t_begin);
+            const float4* cs = rope + (t < cur.t_end() ? t : cur.t_begin());
 #pragma unroll
             for (int qq = 0; qq < Q / 2; ++qq)
                 pair_rope_apply<D>(y, qq, __ldg(cs + int64_t(hf * (Q / 2) + qq) * tokens), sgn);

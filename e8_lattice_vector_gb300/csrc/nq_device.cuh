@@ -291,7 +291,12 @@ __device__ __forceinline__ bool e8_fast(const float (&u)[8], unsigned& code, uns
     constexpr float TWO23 = 8388608.0f;
     constexpr float BAND = 1.52587890625e-05f;  // 2^-16
     const float2 M2 = make_float2(kMagic, kMagic);
-    float eb1[8], s0[8], csv[8];
+    // clv_j = cs_j L^j with cs_j = copysign(1/2, e~0_j): the sign bit of e~0_j
+    // on the power of two L^j / 2 (one logic op, exact)
+    float eb1[8], s0[8], clv[8];
+    // S = sum |e~0_j| in two accumulators (even and odd j); the strict decoder
+    // sums cs_j e~0_j = |e~0_j| / 2 instead (it needs cs_j for e~1 anyway);
+    // both are exact rescalings of each other term by term
     float2 S = make_float2(0.0f, 0.0f);
     // A = 2^23 + (L/2 - 1) SUML + sum r0_j L^j: 2^23 plus the integer code
     // B = sum cs_j L^j - SUML / 2, so that A - B = 2^23 plus the half code
@@ -306,21 +311,25 @@ __device__ __forceinline__ bool e8_fast(const float (&u)[8], unsigned& code, uns
         const float2 t = __fadd2_rn(uu, M2);
         const float2 r0 = fsub2(t, M2);
         const float2 e0 = fsub2(r0, uu);
-        const float2 cs = make_float2(copysignf(0.5f, e0.x), copysignf(0.5f, e0.y));
         const float2 lp = make_float2(Lp[j & 3], Lp[(j & 3) + 1]);
-        csv[j] = cs.x;
-        csv[j + 1] = cs.y;
-        S = __ffma2_rn(cs, e0, S);  // |e~0| / 2 per coordinate (exact products)
+        const float2 cl = make_float2(copysignf(0.5f * Lp[j & 3], e0.x), copysignf(0.5f * Lp[(j & 3) + 1], e0.y));
+        clv[j] = cl.x;
+        clv[j + 1] = cl.y;
         A[j >> 2] = __ffma2_rn(r0, lp, A[j >> 2]);
-        B[j >> 2] = __ffma2_rn(cs, lp, B[j >> 2]);
+        B[j >> 2] = __fadd2_rn(B[j >> 2], cl);
         s0[j] = fminf(fabsf(e0.x), __fsub_rn(C::HI0, fabsf(uu.x)));
         s0[j + 1] = fminf(fabsf(e0.y), __fsub_rn(C::HI0, fabsf(uu.y)));
         x0 ^= __float_as_uint(t.x) ^ __float_as_uint(t.y);
         if (STRICT) {
+            const float2 cs = make_float2(copysignf(0.5f, e0.x), copysignf(0.5f, e0.y));
+            S = __ffma2_rn(cs, e0, S);  // |e~0| / 2 per coordinate (exact products)
             const float2 e1 = fsub2(e0, cs);
             eb1[j] = e1.x;
             eb1[j + 1] = e1.y;
             xs ^= __float_as_uint(e0.x) ^ __float_as_uint(e0.y);
+        } else {
+            S.x = __fadd_rn(S.x, fabsf(e0.x));
+            S.y = __fadd_rn(S.y, fabsf(e0.y));
         }
     }
     const float smax0 = fmax3(fmax3(s0[0], s0[1], s0[2]), fmax3(s0[3], s0[4], s0[5]), fmaxf(s0[6], s0[7]));
@@ -330,7 +339,7 @@ __device__ __forceinline__ bool e8_fast(const float (&u)[8], unsigned& code, uns
                       fmax3(fabsf(eb1[3]), fabsf(eb1[4]), fabsf(eb1[5])), fmaxf(fabsf(eb1[6]), fabsf(eb1[7])));
     const bool odd0 = (x0 & 1u) != 0;
     const bool odd1 = STRICT && (((x0 ^ (xs >> 31)) & 1u) != 0);  // + number of e~0 < 0
-    float D = __fmaf_rn(2.0f, __fadd_rn(S.x, S.y), -2.0f);  // sum |e~0| - 2
+    float D = STRICT ? __fmaf_rn(2.0f, __fadd_rn(S.x, S.y), -2.0f) : __fsub_rn(__fadd_rn(S.x, S.y), 2.0f);  // sum |e~0| - 2
     if (odd0) D = __fadd_rn(D, __fmaf_rn(-2.0f, smax0, 1.0f));
     if (odd1) D = __fsub_rn(D, __fmaf_rn(-2.0f, smax1, 1.0f));
     bool ok = fabsf(D) > BAND;
@@ -354,8 +363,7 @@ __device__ __forceinline__ bool e8_fast(const float (&u)[8], unsigned& code, uns
         float2 ind;
         asm("fma.rn.sat.f32 %0, %1, 0fFF000000, 0f3F800000;" : "=f"(ind.x) : "f"(dlt.x));
         asm("fma.rn.sat.f32 %0, %1, 0fFF000000, 0f3F800000;" : "=f"(ind.y) : "f"(dlt.y));
-        const float2 cl = __fmul2_rn(make_float2(csv[j], csv[j + 1]), make_float2(Lp[j & 3], Lp[(j & 3) + 1]));
-        G[j >> 2] = __ffma2_rn(ind, cl, G[j >> 2]);
+        G[j >> 2] = __ffma2_rn(ind, make_float2(clv[j], clv[j + 1]), G[j >> 2]);
     }
     const float G0 = __fadd_rn(G[0].x, G[0].y), G1 = __fadd_rn(G[1].x, G[1].y);
     // A unique maximum leaves one term +-L^k / 2, a power of two, in exactly one
@@ -537,32 +545,44 @@ __device__ __forceinline__ void sts128(uint32_t a, const uint4& v) {
                  : "memory");
 }
 
-// Work items: (slice, chunk of `chunk` tokens); a warp walks its items'
-// tiles of ROWS tokens in order.  Two copies of the walk run one pipeline depth
-// apart (the one that prefetches and the one that computes).
+// Work items: (slice, chunk of `chunk` tokens), item = slice * nchunks + c; a
+// warp walks its items' tiles of ROWS tokens in order, items first, first +
+// step, ...  Two copies of the walk run one pipeline depth apart (the one that
+// prefetches and the one that computes).  The divisions happen once, in the
+// constructor: moving to the next item adds step = dslice * nchunks + dc as a
+// (slice, c) pair with one carry; the walk ends when slice reaches slices.
 template <int ROWS>
 struct TileWalkT {
-    int64_t item, items, step, slice;
-    int nchunks, chunk, tokens, t_begin, t_end, t0;
-    __device__ TileWalkT(int64_t first, int64_t step_, int64_t slices, int tokens_, int chunk_)
-        : items(0), step(step_), slice(0), chunk(chunk_), tokens(tokens_), t_begin(0), t_end(0), t0(0) {
+    int64_t slice, slices, dslice;
+    int nchunks, chunk, tokens, c, dc, t0;
+    __device__ TileWalkT(int64_t first, int64_t step, int64_t slices_, int tokens_, int chunk_)
+        : slices(slices_), chunk(chunk_), tokens(tokens_) {
         nchunks = (tokens_ + chunk_ - 1) / chunk_;
-        items = slices * nchunks;
-        set(first);
-    }
-    __device__ __forceinline__ void set(int64_t it) {
-        item = it;
-        if (it < items) {
-            slice = it / nchunks;
-            t_begin = int(it - slice * nchunks) * chunk;
-            t_end = min(t_begin + chunk, tokens);
-            t0 = t_begin;
+        slice = slices_;  // no work when there are no chunks
+        dslice = 0;
+        c = dc = 0;
+        if (nchunks > 0) {
+            slice = first / nchunks;
+            c = int(first - slice * nchunks);
+            dslice = step / nchunks;
+            dc = int(step - dslice * nchunks);
         }
+        t0 = c * chunk;
     }
-    __device__ __forceinline__ bool valid() const { return item < items; }
+    __device__ __forceinline__ bool valid() const { return slice < slices; }
+    __device__ __forceinline__ int t_begin() const { return c * chunk; }
+    __device__ __forceinline__ int t_end() const { return min(c * chunk + chunk, tokens); }
     __device__ __forceinline__ void next() {
         t0 += ROWS;
-        if (t0 >= t_end) set(item + step);
+        if (t0 >= t_end()) {
+            slice += dslice;
+            c += dc;
+            if (c >= nchunks) {
+                c -= nchunks;
+                ++slice;
+            }
+            t0 = c * chunk;
+        }
     }
 };
 using TileWalk = TileWalkT<kTileRows>;
