@@ -92,32 +92,37 @@ __device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
     return d;
 }
 
-// One butterfly stage (a, b) -> (a + b, a - b) over pairs (i, i + h).  For
-// h >= 2 the butterflies (i, i+h) and (i+1, i+1+h) share one packed f32x2 add
-// and one subtract (each half is an ordinary IEEE round-to-nearest operation,
-// so the results are those of the scalar butterflies).
-template <int N>
+// One butterfly stage (a, b) -> (a + b, a - b) over pairs (i, i + h).  The
+// packed f32x2 instructions pair slots (i, i + P): for h != P the butterflies
+// (i, i+h) and (i+P, i+P+h) share one packed add and one subtract (each half
+// is an ordinary IEEE round-to-nearest operation, so the results are those of
+// the scalar butterflies); the stage h == P runs scalar.  P = 1 pairs
+// neighbouring slots, P = 4 the two halves of an 8-block (the pairing the
+// compression side's E8 search wants).
+template <int N, int P = 1>
 __device__ __forceinline__ void fwht_stage(float (&y)[N], int h) {
-    if (h == 1) {
+    if (h == P) {
 #pragma unroll
-        for (int i = 0; i < N; i += 2) {
-            const float a = y[i], b = y[i + 1];
-            y[i] = __fadd_rn(a, b);
-            y[i + 1] = __fsub_rn(a, b);
+        for (int i = 0; i < N; ++i) {
+            if ((i & P) == 0) {
+                const float a = y[i], b = y[i + P];
+                y[i] = __fadd_rn(a, b);
+                y[i + P] = __fsub_rn(a, b);
+            }
         }
         return;
     }
 #pragma unroll
-    for (int i = 0; i < N; i += 2) {
-        if ((i & h) == 0) {
-            const float2 a = make_float2(y[i], y[i + 1]);
-            const float2 b = make_float2(y[i + h], y[i + h + 1]);
+    for (int i = 0; i < N; ++i) {
+        if ((i & P) == 0 && (i & h) == 0) {
+            const float2 a = make_float2(y[i], y[i + P]);
+            const float2 b = make_float2(y[i + h], y[i + h + P]);
             const float2 s = __fadd2_rn(a, b);
             const float2 d = fsub2(a, b);
             y[i] = s.x;
-            y[i + 1] = s.y;
+            y[i + P] = s.y;
             y[i + h] = d.x;
-            y[i + h + 1] = d.y;
+            y[i + h + P] = d.y;
         }
     }
 }
@@ -133,42 +138,46 @@ __device__ __forceinline__ void fwht(float (&y)[N]) {
 // Butterfly stage on slot pairs (l, l + Q) with a per-thread sign:
 // (P, Q) -> (P + sgn*Q, P - sgn*Q).  fma(x, +-1, y) is exactly y +- x, so with
 // sgn = +1 this is the plain butterfly and with sgn = -1 it is the butterfly
-// with its two outputs exchanged.
-template <int N>
+// with its two outputs exchanged.  Packed pairs as in fwht_stage.
+template <int N, int P = 1>
 __device__ __forceinline__ void stage_signed(float (&y)[N], float sgn) {
     constexpr int Q = N / 2;
 #pragma unroll
-    for (int l = 0; l < Q; l += 2) {
-        const float2 p = make_float2(y[l], y[l + 1]);
-        const float2 q = make_float2(y[l + Q], y[l + Q + 1]);
-        const float2 a = __ffma2_rn(q, make_float2(sgn, sgn), p);
-        const float2 b = __ffma2_rn(q, make_float2(-sgn, -sgn), p);
-        y[l] = a.x;
-        y[l + 1] = a.y;
-        y[l + Q] = b.x;
-        y[l + Q + 1] = b.y;
+    for (int l = 0; l < Q; ++l) {
+        if ((l & P) == 0) {
+            const float2 p = make_float2(y[l], y[l + P]);
+            const float2 q = make_float2(y[l + Q], y[l + Q + P]);
+            const float2 a = __ffma2_rn(q, make_float2(sgn, sgn), p);
+            const float2 b = __ffma2_rn(q, make_float2(-sgn, -sgn), p);
+            y[l] = a.x;
+            y[l + P] = a.y;
+            y[l + Q] = b.x;
+            y[l + Q + P] = b.y;
+        }
     }
 }
 
 // Exchange stage between the two threads of a row: each sends slots
 // [N/2, N) to its partner and makes (own + recv, own - recv) from slots
-// [0, N/2) and the received values.
-template <int N>
+// [0, N/2) and the received values.  Packed pairs as in fwht_stage.
+template <int N, int P = 1>
 __device__ __forceinline__ void stage_exchange(float (&y)[N]) {
     constexpr int Q = N / 2;
     float r[Q];
 #pragma unroll
     for (int l = 0; l < Q; ++l) r[l] = __shfl_xor_sync(kFull, y[l + Q], 1);
 #pragma unroll
-    for (int l = 0; l < Q; l += 2) {
-        const float2 a = make_float2(y[l], y[l + 1]);
-        const float2 b = make_float2(r[l], r[l + 1]);
-        const float2 s = __fadd2_rn(a, b);
-        const float2 d = fsub2(a, b);
-        y[l] = s.x;
-        y[l + 1] = s.y;
-        y[l + Q] = d.x;
-        y[l + Q + 1] = d.y;
+    for (int l = 0; l < Q; ++l) {
+        if ((l & P) == 0) {
+            const float2 a = make_float2(y[l], y[l + P]);
+            const float2 b = make_float2(r[l], r[l + P]);
+            const float2 s = __fadd2_rn(a, b);
+            const float2 d = fsub2(a, b);
+            y[l] = s.x;
+            y[l + P] = s.y;
+            y[l + Q] = d.x;
+            y[l + Q + P] = d.y;
+        }
     }
 }
 
@@ -277,11 +286,13 @@ __device__ __forceinline__ int e8_general(const float (&u)[8], bool strict, floa
 //
 // The codes are accumulated as exact integer-valued floats on the FMA pipe
 // (sum of r_j * L^j over half-blocks of 4 coordinates, < 2^16), the parities
-// by xor of the magic-rounded bit patterns.  Pairs of coordinates share packed
-// f32x2 instructions (each half an ordinary IEEE operation).  A block whose
-// chosen coset needs a fix-up with a tie for the maximal score or a maximal
-// score <= 2^-100 (every coordinate nearly an integer or past the box edge) is
-// not handled here either.
+// by xor of the magic-rounded bit patterns.  Coordinates j and j + 4 share
+// packed f32x2 instructions (each half an ordinary IEEE operation), so the
+// two lanes of an accumulator are the two half-blocks and every sum comes out
+// of the packed operations whole.  A block whose chosen coset needs a fix-up
+// with a tie for the maximal score or a maximal score <= 2^-100 (every
+// coordinate nearly an integer or past the box edge) is not handled here
+// either.
 template <int BITS, bool STRICT>
 __device__ __forceinline__ bool e8_fast(const float (&u)[8], unsigned& code, unsigned& coset) {
     using C = Code<BITS>;
@@ -294,38 +305,38 @@ __device__ __forceinline__ bool e8_fast(const float (&u)[8], unsigned& code, uns
     // clv_j = cs_j L^j with cs_j = copysign(1/2, e~0_j): the sign bit of e~0_j
     // on the power of two L^j / 2 (one logic op, exact)
     float eb1[8], s0[8], clv[8];
-    // S = sum |e~0_j| in two accumulators (even and odd j); the strict decoder
-    // sums cs_j e~0_j = |e~0_j| / 2 instead (it needs cs_j for e~1 anyway);
-    // both are exact rescalings of each other term by term
+    // S = sum |e~0_j| in two accumulators; the strict decoder sums
+    // cs_j e~0_j = |e~0_j| / 2 instead (it needs cs_j for e~1 anyway), an
+    // exact rescaling of each term
     float2 S = make_float2(0.0f, 0.0f);
     // A = 2^23 + (L/2 - 1) SUML + sum r0_j L^j: 2^23 plus the integer code
     // B = sum cs_j L^j - SUML / 2, so that A - B = 2^23 plus the half code
+    // (lane x: coordinates 0-3, lane y: coordinates 4-7)
     constexpr float A0 = TWO23 + float(C::OFF0) * SUML;
     constexpr float B0 = -0.5f * SUML;
-    float2 A[2] = {make_float2(A0, 0.0f), make_float2(A0, 0.0f)};
-    float2 B[2] = {make_float2(B0, 0.0f), make_float2(B0, 0.0f)};
+    float2 A = make_float2(A0, A0);
+    float2 B = make_float2(B0, B0);
     unsigned x0 = 0, xs = 0;
 #pragma unroll
-    for (int j = 0; j < 8; j += 2) {
-        const float2 uu = make_float2(u[j], u[j + 1]);
+    for (int j = 0; j < 4; ++j) {
+        const float2 uu = make_float2(u[j], u[j + 4]);
         const float2 t = __fadd2_rn(uu, M2);
         const float2 r0 = fsub2(t, M2);
         const float2 e0 = fsub2(r0, uu);
-        const float2 lp = make_float2(Lp[j & 3], Lp[(j & 3) + 1]);
-        const float2 cl = make_float2(copysignf(0.5f * Lp[j & 3], e0.x), copysignf(0.5f * Lp[(j & 3) + 1], e0.y));
+        const float2 cl = make_float2(copysignf(0.5f * Lp[j], e0.x), copysignf(0.5f * Lp[j], e0.y));
         clv[j] = cl.x;
-        clv[j + 1] = cl.y;
-        A[j >> 2] = __ffma2_rn(r0, lp, A[j >> 2]);
-        B[j >> 2] = __fadd2_rn(B[j >> 2], cl);
+        clv[j + 4] = cl.y;
+        A = __ffma2_rn(r0, make_float2(Lp[j], Lp[j]), A);
+        B = __fadd2_rn(B, cl);
         s0[j] = fminf(fabsf(e0.x), __fsub_rn(C::HI0, fabsf(uu.x)));
-        s0[j + 1] = fminf(fabsf(e0.y), __fsub_rn(C::HI0, fabsf(uu.y)));
+        s0[j + 4] = fminf(fabsf(e0.y), __fsub_rn(C::HI0, fabsf(uu.y)));
         x0 ^= __float_as_uint(t.x) ^ __float_as_uint(t.y);
         if (STRICT) {
             const float2 cs = make_float2(copysignf(0.5f, e0.x), copysignf(0.5f, e0.y));
             S = __ffma2_rn(cs, e0, S);  // |e~0| / 2 per coordinate (exact products)
             const float2 e1 = fsub2(e0, cs);
             eb1[j] = e1.x;
-            eb1[j + 1] = e1.y;
+            eb1[j + 4] = e1.y;
             xs ^= __float_as_uint(e0.x) ^ __float_as_uint(e0.y);
         } else {
             S.x = __fadd_rn(S.x, fabsf(e0.x));
@@ -350,43 +361,36 @@ __device__ __forceinline__ bool e8_fast(const float (&u)[8], unsigned& code, uns
     // moves up) or +2*cs_k*L^k to the half-integer code.  k is found on the FMA
     // pipe: i_j = sat(1 - (smax - s_j) * 2^127) is 1 at a maximum and 0
     // elsewhere (with smax > 2^-100, distinct scores differ by at least 2^-123),
-    // and G = sum_j i_j cs_j L^j picks cs_k L^k.  A tie goes to the general
-    // path.  Computed for every block (no branch), applied if needed.
+    // and G = sum_j i_j cs_j L^j picks cs_k L^k (G.x over coordinates 0-3, G.y
+    // over 4-7).  A tie goes to the general path.  Computed for every block (no
+    // branch), applied if needed.
     const bool fix = half ? odd1 : odd0;
     const float smax = half ? smax1 : smax0;
-    float2 G[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+    float2 G = make_float2(0.0f, 0.0f);
 #pragma unroll
-    for (int j = 0; j < 8; j += 2) {
-        const float2 sj = (STRICT && half) ? make_float2(fabsf(eb1[j]), fabsf(eb1[j + 1]))
-                                           : make_float2(s0[j], s0[j + 1]);
+    for (int j = 0; j < 4; ++j) {
+        const float2 sj = (STRICT && half) ? make_float2(fabsf(eb1[j]), fabsf(eb1[j + 4]))
+                                           : make_float2(s0[j], s0[j + 4]);
         const float2 dlt = fsub2(make_float2(smax, smax), sj);
         float2 ind;
         asm("fma.rn.sat.f32 %0, %1, 0fFF000000, 0f3F800000;" : "=f"(ind.x) : "f"(dlt.x));
         asm("fma.rn.sat.f32 %0, %1, 0fFF000000, 0f3F800000;" : "=f"(ind.y) : "f"(dlt.y));
-        G[j >> 2] = __ffma2_rn(ind, make_float2(clv[j], clv[j + 1]), G[j >> 2]);
+        G = __ffma2_rn(ind, make_float2(clv[j], clv[j + 4]), G);
     }
-    const float G0 = __fadd_rn(G[0].x, G[0].y), G1 = __fadd_rn(G[1].x, G[1].y);
     // A unique maximum leaves one term +-L^k / 2, a power of two, in exactly one
     // half-block; ties leave sums of distinct +-L^j / 2 (L >= 4), which are
     // never powers of two, or terms in both halves.
-    const bool one = (G0 == 0.0f) != (G1 == 0.0f);
-    const bool pow2 = (__float_as_uint(__fadd_rn(G0, G1)) & 0x7fffffu) == 0u;
+    const bool one = (G.x == 0.0f) != (G.y == 0.0f);
+    const bool pow2 = (__float_as_uint(__fadd_rn(G.x, G.y)) & 0x7fffffu) == 0u;
     ok = ok && (!fix || (smax > 7.88860905e-31f && one && pow2));  // 2^-100
     const float m = fix ? (half ? 2.0f : -2.0f) : 0.0f;
-    const float g[2] = {__fmul_rn(m, G0), __fmul_rn(m, G1)};
+    const float hb = half ? 1.0f : 0.0f;
 
     // integer codes m0 = r0 + (L/2 - 1), half-integer codes m1 = r1 + (L - 1)/2,
     // per half-block an exact integer below 2^16 in the low bits of 2^23 + m
     // (every intermediate is a multiple of 1/2 below 2^24, so all of this is exact)
-    unsigned c = 0;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const float Ah = __fadd_rn(A[h].x, A[h].y);
-        const float Bh = half ? __fadd_rn(B[h].x, B[h].y) : 0.0f;
-        const float f = __fadd_rn(__fsub_rn(Ah, Bh), g[h]);
-        c |= (__float_as_uint(f) & 0xffffu) << (4 * BITS * h);
-    }
-    code = c;
+    const float2 f = __fadd2_rn(fsub2(A, __fmul2_rn(B, make_float2(hb, hb))), __fmul2_rn(make_float2(m, m), G));
+    code = (__float_as_uint(f.x) & 0xffffu) | ((__float_as_uint(f.y) & 0xffffu) << (4 * BITS));
     coset = half ? 1u : 0u;
     return ok;
 }

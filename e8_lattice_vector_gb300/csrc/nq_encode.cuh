@@ -8,14 +8,15 @@
 
 namespace nq {
 
-// Scaled coordinates u = y * inv of 8-block k of the thread's coordinates.
+// Scaled coordinates u = y * inv of 8-block k of the thread's coordinates
+// (packed pairs j, j + 4, as the E8 search and the transform use them).
 template <int N>
 __device__ __forceinline__ void row_block_u(const float (&y)[N], float inv, int k, float (&u)[8]) {
 #pragma unroll
-    for (int j = 0; j < 8; j += 2) {
-        const float2 p = __fmul2_rn(make_float2(y[8 * k + j], y[8 * k + j + 1]), make_float2(inv, inv));
+    for (int j = 0; j < 4; ++j) {
+        const float2 p = __fmul2_rn(make_float2(y[8 * k + j], y[8 * k + j + 4]), make_float2(inv, inv));
         u[j] = p.x;
-        u[j + 1] = p.y;
+        u[j + 4] = p.y;
     }
 }
 
@@ -66,9 +67,9 @@ __device__ __forceinline__ void pair_encode_codes(float (&y)[D / 2], int hf, flo
     // ---- Hadamard rotation, compression order: bits below DP/4 in-thread,
     //      bit DP/2 in-thread (signed), bit DP/4 by exchange
 #pragma unroll
-    for (int h = 1; h < Q; h *= 2) fwht_stage<HALF>(y, h);
-    stage_signed<HALF>(y, sgn);
-    stage_exchange<HALF>(y);
+    for (int h = 1; h < Q; h *= 2) fwht_stage<HALF, 4>(y, h);
+    stage_signed<HALF, 4>(y, sgn);
+    stage_exchange<HALF, 4>(y);
 
     // ---- group absmax -> fp16 scale -> reciprocal (per 32-subgroup)
     float amax[NSUB];
