@@ -379,10 +379,20 @@ __device__ __forceinline__ bool e8_fast(const float (&u)[8], unsigned& code, uns
     }
     // A unique maximum leaves one term +-L^k / 2, a power of two, in exactly one
     // half-block; ties leave sums of distinct +-L^j / 2 (L >= 4), which are
-    // never powers of two, or terms in both halves.
-    const bool one = (G.x == 0.0f) != (G.y == 0.0f);
-    const bool pow2 = (__float_as_uint(__fadd_rn(G.x, G.y)) & 0x7fffffu) == 0u;
-    ok = ok && (!fix || (smax > 7.88860905e-31f && one && pow2));  // 2^-100
+    // never powers of two (L^b times an odd number of magnitude >= 3), or terms
+    // in both halves.  For b <= 3 the upper half is weighted by L^4, making the
+    // eight terms distinct powers +-L^j / 2, j = 0..7, whose sum is exact (at
+    // most 7b + 1 <= 22 significant bits): one power-of-two test covers both
+    // cases.  For b = 4 that sum could round, so the halves are tested apart.
+    bool unique;
+    if constexpr (BITS <= 3) {
+        constexpr float L4 = L * L * L * L;
+        unique = (__float_as_uint(__fmaf_rn(G.y, L4, G.x)) & 0x7fffffu) == 0u;
+    } else {
+        const bool one = (G.x == 0.0f) != (G.y == 0.0f);
+        unique = one && (__float_as_uint(__fadd_rn(G.x, G.y)) & 0x7fffffu) == 0u;
+    }
+    ok = ok && (!fix || (smax > 7.88860905e-31f && unique));  // 2^-100
     const float m = fix ? (half ? 2.0f : -2.0f) : 0.0f;
     const float hb = half ? 1.0f : 0.0f;
 
