@@ -37,6 +37,22 @@ __device__ __forceinline__ void load_pair_tile(const __half* __restrict__ x, int
     constexpr int CPR = D / 8;  // 16-byte chunks per row
     const int nvalid = min(kPairRows, tokens - t0);
     const __half* base = x + (slice * tokens + min(t0, tokens - 1)) * int64_t(D);
+    if constexpr (CPR == 8 || CPR == 16) {
+        if (nvalid == kPairRows) {  // full tile (warp-uniform): no bounds, swizzle by parts
+            // copy i of the lane is chunk g = lane + 32 i: row r = r0 + (32 / CPR) i,
+            // column c = lane % CPR; (r & 7) = r0 + (32 / CPR) (i % (8 CPR / 32))
+            // with disjoint bits, so the swizzle term is x0 ^ that step.
+            constexpr int RS = 32 / CPR;   // rows per copy step
+            constexpr int PER = 8 / RS;    // steps until (r & 7) repeats
+            const int c = lane % CPR, r0 = lane / CPR;
+            const uint32_t d0 = stage + ((c >> 3) << 11) + (r0 << 7);
+            const uint32_t x0 = uint32_t((c & 7) ^ r0) << 4;
+#pragma unroll
+            for (int i = 0; i < CPR / 2; ++i)
+                cp_async16(d0 + ((RS * i) << 7) + (x0 ^ (uint32_t(RS * (i % PER)) << 4)), base + 8 * (lane + 32 * i), 16);
+            return;
+        }
+    }
 #pragma unroll
     for (int i = 0; i < CPR / 2; ++i) {  // 16 rows * CPR chunks / 32 lanes
         const int g = lane + 32 * i;
