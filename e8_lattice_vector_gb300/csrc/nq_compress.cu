@@ -230,12 +230,16 @@ __global__ void __launch_bounds__(kCompressRopeThreads, 2)
     Walk pre = cur;
 
     auto load_stage = [&](const Walk& w, uint32_t stage) {
-        for (int g = threadIdx.x; g < (D / 4) * kPairRows; g += kCompressRopeThreads) {
-            const int q = g / kPairRows, rr = g - q * kPairRows;
-            const int tok = w.t0 + rr;
-            const bool ok = tok < tokens;
-            cp_async16(stage + rope_slot<D>(q, rr), rope + int64_t(q) * tokens + (ok ? tok : 0), ok ? 16 : 0);
-        }
+        // the table tile: thread t copies token row t % 16 of planes t / 16 + 16 j
+        constexpr int QS = kCompressRopeThreads / kPairRows;  // plane step
+        static_assert((D / 4) % QS == 0, "table copies per thread");
+        const int rr = threadIdx.x % kPairRows, q0 = threadIdx.x / kPairRows;
+        const int tok = w.t0 + rr;
+        const bool ok = tok < tokens;
+        const float4* src = rope + int64_t(q0) * tokens + (ok ? tok : 0);
+#pragma unroll
+        for (int j = 0; j < (D / 4) / QS; ++j)
+            cp_async16(stage + rope_slot<D>(q0 + QS * j, rr), src + int64_t(QS * j) * tokens, ok ? 16 : 0);
         const int64_t sl = w.slice * kCompressRopeWarps + wib;
         if (sl < slices) load_pair_tile<D>(x, sl, w.t0, tokens, stage + RS::TABLE + wib * kPairTileBytes, lane);
     };

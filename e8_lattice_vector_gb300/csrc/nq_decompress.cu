@@ -322,12 +322,15 @@ __global__ void __launch_bounds__(kKeyThreads, 1)
     TileWalk pre = cur;
 
     auto load_stage = [&](const TileWalk& w, uint32_t stage) {
-        for (int g = threadIdx.x; g < (D / 4) * kTileRows; g += kKeyThreads) {
-            const int q = g / kTileRows, rr = g - q * kTileRows;
-            const int tok = w.t0 + rr;
-            const bool ok = tok < tokens;
-            cp_async16(stage + 16 * g, rope + int64_t(q) * tokens + (ok ? tok : 0), ok ? 16 : 0);
-        }
+        // the table tile: thread t copies token row t % 32 of planes t / 32 + 4 j
+        constexpr int QS = kKeyThreads / kTileRows;  // plane step
+        static_assert((D / 4) % QS == 0, "table copies per thread");
+        const int tok = w.t0 + lane;
+        const bool ok = tok < tokens;
+        const float4* src = rope + int64_t(wib) * tokens + (ok ? tok : 0);
+#pragma unroll
+        for (int j = 0; j < (D / 4) / QS; ++j)
+            cp_async16(stage + 16 * (threadIdx.x + kKeyThreads * j), src + int64_t(QS * j) * tokens, ok ? 16 : 0);
         const int64_t sl = w.slice * kKeyWarps + wib;
         if (sl < slices) load_records<RB>(idx, coset, scales, nsc, sl * tpad + w.t0, stage + KS::TABLE + wib * kRecStage, lane);
     };
