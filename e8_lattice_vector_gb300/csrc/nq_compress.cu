@@ -166,11 +166,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 
         // ---- the thread's 64 (32) coordinates of row r (zeros past head_dim)
         float y[HALF];
+        const PairTileAddr<DP> ta(stage, r, hf);
 #pragma unroll
         for (int c = 0; c < NBT; ++c) {
             const int gc = PM::chunk(hf, c);
             if (D == DP || gc < D / 8) {
-                h8_to_f(lds128(stage + swz16(r, gc)), &y[8 * c]);
+                h8_to_f(lds128(ta(c)), &y[8 * c]);
             } else {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) y[8 * c + j] = 0.0f;
@@ -273,8 +274,9 @@ __global__ void __launch_bounds__(kCompressRopeThreads, 2)
             const bool active = t < tokens;
             float y[HALF];
             const uint32_t tile = stage + RS::TABLE + wib * kPairTileBytes;
+            const PairTileAddr<DP> ta(tile, r, hf);
 #pragma unroll
-            for (int c = 0; c < NBT; ++c) h8_to_f(lds128(tile + swz16(r, PM::chunk(hf, c))), &y[8 * c]);
+            for (int c = 0; c < NBT; ++c) h8_to_f(lds128(ta(c)), &y[8 * c]);
             // RoPE removal with the block's table tile: pairs (i, i + D/2) are slots (l, l + Q)
 #pragma unroll
             for (int qq = 0; qq < Q / 2; ++qq) pair_rope_remove<D>(y, qq, rope_tile_entry<D>(stage, hf * (Q / 2) + qq, r));

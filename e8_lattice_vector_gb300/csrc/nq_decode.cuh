@@ -179,6 +179,7 @@ __device__ __forceinline__ void pair_store_rows(const float (&y)[D / 2], uint32_
     const unsigned negbits = hf ? 0x80008000u : 0u;
     if (lane == 0) asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(PENDING) : "memory");  // ob is free
     __syncwarp();
+    const PairTileAddr<D> ta(ob, r, hf);
 #pragma unroll
     for (int c = 0; c < NBT; ++c) {
         uint4 v = f_to_h8(&y[8 * c]);
@@ -188,7 +189,7 @@ __device__ __forceinline__ void pair_store_rows(const float (&y)[D / 2], uint32_
             v.z ^= negbits;
             v.w ^= negbits;
         }
-        sts128(ob + swz16(r, PM::chunk(hf, c)), v);
+        sts128(ta(c), v);
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();

@@ -521,6 +521,21 @@ struct PairMap {
     }
 };
 
+// Shared-memory address of the thread's slot chunk c of row r in a 16-row
+// tile, swz16(r, PairMap<DP>::chunk(hf, c)), split into the lane's part
+// (row offset, and the swizzle bits of hf * DP/32 and r) and the chunk's own
+// immediate: the chunk bits of slot chunk c are disjoint from hf * DP/32.
+template <int DP>
+struct PairTileAddr {
+    uint32_t base, x0;
+    __device__ __forceinline__ PairTileAddr(uint32_t stage, int r, int hf)
+        : base(stage + (uint32_t(r) << 7)), x0(uint32_t((hf * (DP / 32)) ^ (r & 7)) << 4) {}
+    __device__ __forceinline__ uint32_t operator()(int c) const {
+        const int cp = c < DP / 32 ? c : c + DP / 16 - DP / 32;  // chunk(hf, c) - hf * DP/32
+        return base + (uint32_t(cp >> 3) << 11) + (x0 ^ (uint32_t(cp & 7) << 4));
+    }
+};
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -81,11 +81,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint32_t stage = ring + (i % kRtStages) * kPairTileBytes;
         const int t = cur.t0 + r;
         float y[HALF];
+        const PairTileAddr<DP> ta(stage, r, hf);
 #pragma unroll
         for (int c = 0; c < NBT; ++c) {
             const int gc = PM::chunk(hf, c);
             if (D == DP || gc < D / 8) {
-                h8_to_f(lds128(stage + swz16(r, gc)), &y[8 * c]);
+                h8_to_f(lds128(ta(c)), &y[8 * c]);
             } else {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) y[8 * c + j] = 0.0f;
@@ -194,8 +195,9 @@ __global__ void __launch_bounds__(kRtRopeThreads, 1)
         if (slice < slices) {  // warp-uniform
             const uint32_t tile = stage + RS::TABLE + wib * kPairTileBytes;
             float y[HALF];
+            const PairTileAddr<D> ta(tile, r, hf);
 #pragma unroll
-            for (int c = 0; c < NBT; ++c) h8_to_f(lds128(tile + swz16(r, PM::chunk(hf, c))), &y[8 * c]);
+            for (int c = 0; c < NBT; ++c) h8_to_f(lds128(ta(c)), &y[8 * c]);
 #pragma unroll
             for (int qq = 0; qq < Q / 2; ++qq) pair_rope_remove<D>(y, qq, rope_tile_entry<D>(stage, hf * (Q / 2) + qq, r));
             pair_round_trip<D, BITS, STRICT>(y, hf, sgn, group);
