@@ -65,8 +65,10 @@ __device__ __forceinline__ void pair_encode_row(float (&y)[D / 2], int hf, int r
     using RP = RowPack<BITS, NBT>;
     constexpr int RB = DP * BITS / 8;  // idx bytes per row
     constexpr int RBT = RB / 2;        // idx bytes per thread
-    const int nsc = DP / group;
-    const int span = group / 32;  // 32-coordinate subgroups per scale group
+    // group is 32, 64 or 128: span = 2^gsh 32-coordinate subgroups per scale
+    // group, nsc = DP / group scales per row (shifts, not divisions)
+    const int gsh = group == 32 ? 0 : (group == 64 ? 1 : 2);
+    const int nsc = DP >> (5 + gsh);
 
     unsigned short sc[NSUB];
     unsigned blk[NBT];
@@ -111,7 +113,7 @@ __device__ __forceinline__ void pair_encode_row(float (&y)[D / 2], int hf, int r
 #pragma unroll
     for (int s = 0; s < NSUB; ++s) {
         const int gs = hf * NSUB + s;  // global 32-subgroup
-        if (gs % span == 0) scales[rrow * nsc + gs / span] = __ushort_as_half(sc[s]);
+        if ((gs & ((1 << gsh) - 1)) == 0) scales[rrow * nsc + (gs >> gsh)] = __ushort_as_half(sc[s]);
     }
 }
 

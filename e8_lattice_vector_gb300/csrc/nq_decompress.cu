@@ -226,8 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t ring = wbase + kOutBufs * kTileBytes;     // kStages x kRecStage
     const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
-    const int nsc = DP / group;
     const int gshift = group == 32 ? 5 : (group == 64 ? 6 : 7);
+    const int nsc = DP >> gshift;
 
     TileWalk cur(warp, nwarps, slices, tokens, chunk);
     TileWalk pre = cur;
@@ -314,8 +314,8 @@ __global__ void __launch_bounds__(kKeyThreads, 1)
     const int lane = threadIdx.x & 31;
     const uint32_t outbuf = base + wib * kTileBytes;  // 1024-aligned
     const uint32_t stages = base + KS::OUT;
-    const int nsc = DP / group;
     const int gshift = group == 32 ? 5 : (group == 64 ? 6 : 7);
+    const int nsc = DP >> gshift;
     const int64_t ngroups = (slices + kKeyWarps - 1) / kKeyWarps;
 
     TileWalk cur(blockIdx.x, gridDim.x, ngroups, tokens, chunk);
@@ -460,8 +460,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t ring = wbase + kOutBufs * kPairTileBytes;
     const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
-    const int nsc = DP / group;
-    const int span = group / 32;
+    const int gsh = group == 32 ? 0 : (group == 64 ? 1 : 2);  // log2 of 32-subgroups per scale
+    const int nsc = DP >> (5 + gsh);
 
     Walk cur(warp, nwarps, slices, tokens, chunk);
     Walk pre = cur;
@@ -513,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         float scf[NSUB];
 #pragma unroll
         for (int s = 0; s < NSUB; ++s)
-            scf[s] = __half2float(reinterpret_cast<const __half*>(gstage + kPairRecScale)[r * nsc + (hf * NSUB + s) / span]);
+            scf[s] = __half2float(reinterpret_cast<const __half*>(gstage + kPairRecScale)[r * nsc + ((hf * NSUB + s) >> gsh)]);
         __syncwarp();  // the stage may be refilled
         unsigned blk[NBT];
         RP::unpack(w, blk);
