@@ -154,15 +154,18 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
     for (int k = 0; k < NBT; ++k) carry[k] = 0;
 
+    RingSlots<kPairStages> rs;
+
     for (int i = 0; cur.valid(); ++i) {
         if (pre.valid()) {
-            load_pair_tile<D>(x, pre.slice, pre.t0, tokens, ring + ((i + kPairStages - 1) % kPairStages) * kPairTileBytes, lane);
+            load_pair_tile<D>(x, pre.slice, pre.t0, tokens, ring + rs.pre * kPairTileBytes, lane);
             pre.next();
         }
         cp_async_commit();
         cp_async_wait<kPairStages - 1>();
         __syncwarp();
-        const uint32_t stage = ring + (i % kPairStages) * kPairTileBytes;
+        const uint32_t stage = ring + rs.cur * kPairTileBytes;
+        rs.advance();
         const int t = cur.t0 + r;
         const bool active = t < tokens;
 
@@ -261,15 +264,18 @@ __global__ void __launch_bounds__(kCompressRopeThreads, 2)
 #pragma unroll
     for (int k = 0; k < NBT; ++k) carry[k] = 0;
 
+    RingSlots<kCompressRopeStages> rs;
+
     for (int i = 0; cur.valid(); ++i) {
         cp_async_wait<kCompressRopeStages - 2>();  // this thread's copies of tile i are done
         __syncthreads();                    // everyone's are; everyone is done with tile i - 1
         if (pre.valid()) {
-            load_stage(pre, sbase + ((i + kCompressRopeStages - 1) % kCompressRopeStages) * RS::BYTES);
+            load_stage(pre, sbase + rs.pre * RS::BYTES);
             pre.next();
         }
         cp_async_commit();
-        const uint32_t stage = sbase + (i % kCompressRopeStages) * RS::BYTES;
+        const uint32_t stage = sbase + rs.cur * RS::BYTES;
+        rs.advance();
         const int64_t slice = cur.slice * kCompressRopeWarps + wib;
         if (slice < slices) {  // warp-uniform
             const int t = cur.t0 + r;

@@ -574,6 +574,18 @@ __device__ __forceinline__ void sts128(uint32_t a, const uint4& v) {
                  : "memory");
 }
 
+// Slots of an S-deep ring for loop step i: cur = i mod S (the tile computed
+// now), pre = (i + S - 1) mod S (the tile being prefetched), kept by
+// wrapping increments instead of a modulo per step.
+template <int S>
+struct RingSlots {
+    int cur = 0, pre = S - 1;
+    __device__ __forceinline__ void advance() {
+        cur = cur + 1 == S ? 0 : cur + 1;
+        pre = pre + 1 == S ? 0 : pre + 1;
+    }
+};
+
 // Work items: (slice, chunk of `chunk` tokens), item = slice * nchunks + c; a
 // warp walks its items' tiles of ROWS tokens in order, items first, first +
 // step, ...  Two copies of the walk run one pipeline depth apart (the one that

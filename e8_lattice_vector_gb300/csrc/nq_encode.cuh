@@ -104,12 +104,23 @@ __device__ __forceinline__ void pair_encode_codes(float (&y)[D / 2], int hf, flo
     }
     float inv[NSUB];
     bool fast = true;
+    if (NSUB == 2 && span >= 2) {  // one scale group covers both subgroups: one scale, one reciprocal
+        const unsigned short v = group_scale(amax[0], STEP, 1.0f / STEP);
+        const float iv = v ? __frcp_rn(__fmul_rn(__half2float(__ushort_as_half(v)), float(DP))) : 0.0f;
 #pragma unroll
-    for (int s = 0; s < NSUB; ++s) {
-        sc[s] = group_scale(amax[s], STEP, 1.0f / STEP);
-        const float scf = __half2float(__ushort_as_half(sc[s]));
-        inv[s] = sc[s] ? __frcp_rn(__fmul_rn(scf, float(DP))) : 0.0f;
-        fast = fast && (__fmul_rn(amax[s], inv[s]) < C::H);
+        for (int s = 0; s < NSUB; ++s) {
+            sc[s] = v;
+            inv[s] = iv;
+        }
+        fast = __fmul_rn(amax[0], iv) < C::H;
+    } else {
+#pragma unroll
+        for (int s = 0; s < NSUB; ++s) {
+            sc[s] = group_scale(amax[s], STEP, 1.0f / STEP);
+            const float scf = __half2float(__ushort_as_half(sc[s]));
+            inv[s] = sc[s] ? __frcp_rn(__fmul_rn(scf, float(DP))) : 0.0f;
+            fast = fast && (__fmul_rn(amax[s], inv[s]) < C::H);
+        }
     }
 
     // ---- E8 nearest point per 8-block -> block codes

@@ -75,10 +75,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         cp_async_commit();
     }
 
+    RingSlots<kRtStages> rs;
     for (int i = 0; cur.valid(); ++i) {
         cp_async_wait<kRtStages - 2>();
         __syncwarp();
-        const uint32_t stage = ring + (i % kRtStages) * kPairTileBytes;
+        const uint32_t stage = ring + rs.cur * kPairTileBytes;
         const int t = cur.t0 + r;
         float y[HALF];
         const PairTileAddr<DP> ta(stage, r, hf);
@@ -106,11 +107,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
         __syncwarp();
         if (pre.valid()) {
-            load_pair_tile<D>(x, pre.slice, pre.t0, tokens,
-                              ring + ((i + kRtStages - 1) % kRtStages) * kPairTileBytes, lane);
+            load_pair_tile<D>(x, pre.slice, pre.t0, tokens, ring + rs.pre * kPairTileBytes, lane);
             pre.next();
         }
         cp_async_commit();
+        rs.advance();
 
         pair_round_trip<DP, BITS, STRICT>(y, hf, sgn, group);
         if constexpr (ROPE) {
@@ -179,6 +180,7 @@ __global__ void __launch_bounds__(kRtRopeThreads, 1)
         cp_async_commit();
     }
 
+    RingSlots<kRtRopeStages> rs;
     for (int i = 0; cur.valid(); ++i) {
         cp_async_wait<kRtRopeStages - 2>();  // this thread's copies of tile i are done
         // the ring slot about to be refilled held tile i - 1: this warp's store
@@ -186,11 +188,12 @@ __global__ void __launch_bounds__(kRtRopeThreads, 1)
         if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
         __syncthreads();
         if (pre.valid()) {
-            load_stage(pre, sbase + ((i + kRtRopeStages - 1) % kRtRopeStages) * RS::BYTES);
+            load_stage(pre, sbase + rs.pre * RS::BYTES);
             pre.next();
         }
         cp_async_commit();
-        const uint32_t stage = sbase + (i % kRtRopeStages) * RS::BYTES;
+        const uint32_t stage = sbase + rs.cur * RS::BYTES;
+        rs.advance();
         const int64_t slice = cur.slice * kRtRopeWarps + wib;
         if (slice < slices) {  // warp-uniform
             const uint32_t tile = stage + RS::TABLE + wib * kPairTileBytes;
