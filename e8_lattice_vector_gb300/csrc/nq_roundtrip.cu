@@ -17,11 +17,12 @@
 namespace nq {
 
 constexpr int kRtStages = 3;
-// keys: 16 warps share the table tile; a 3-deep ring, so the slot a store
-// reads from is refilled only two tiles later
-constexpr int kRtRopeWarps = 16;
+// keys: blocks of 8 warps share the table tile, two blocks per SM, a 2-deep
+// ring: the slot a store reads from is refilled at the next tile, after the
+// warp has waited for that store's read and the block barrier
+constexpr int kRtRopeWarps = 8;
 constexpr int kRtRopeThreads = kRtRopeWarps * 32;
-constexpr int kRtRopeStages = 3;
+constexpr int kRtRopeStages = 2;
 constexpr int kRtPairSmem = kWarpsPerBlock * kRtStages * kPairTileBytes + 1024;
 
 // ------------------------------------------------------ two threads per row
@@ -130,10 +131,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
-// Keys with RoPE: 16 warps share the tile's table rows (16 slices at the same
-// tokens), as in the compressor; one block barrier per tile.
+// Keys with RoPE: the warps of a block share the tile's table rows (8 slices
+// at the same tokens), as in the compressor; one block barrier per tile.
 template <int D, int BITS, bool STRICT>
-__global__ void __launch_bounds__(kRtRopeThreads, 1)
+__global__ void __launch_bounds__(kRtRopeThreads, 2)
     roundtrip_pair_rope_kernel(const __half* __restrict__ x, const float4* __restrict__ rope,
                                const __grid_constant__ CUtensorMap out_map, int64_t slices, int tokens,
                                int group) {
