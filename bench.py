@@ -471,7 +471,8 @@ def _oracle_all_cores(cfg, params, cpu_seconds, kv0, per_slice, op):
     kb = kv0[0].contiguous().view(torch.int16).numpy().view(np.uint16)
     vb = kv0[1].contiguous().view(torch.int16).numpy().view(np.uint16)
     cs = oracle.rope_table(T, D, params.rope_theta) if params.rope_theta > 0 else None
-    nrep = max(1, int(cpu_seconds / op.cores / max(per_slice, 1e-6)))
+    # at least three slices per process: the parallel wall time is then long enough to time stably
+    nrep = max(3, int(cpu_seconds / op.cores / max(per_slice, 1e-6)))
     p = {"key_bits": params.key_bits, "value_bits": params.value_bits, "group_size": params.group_size,
          "strict": int(params.strict), "delta_chunk": params.delta_chunk}
     jobs = [(kb[w % kb.shape[0]], vb[w % vb.shape[0]], T, D, p, nrep, cs) for w in range(op.cores)]
