@@ -458,7 +458,7 @@ class _OraclePool:
         self.pool.join()
 
 
-def _oracle_all_cores(cfg, params, cpu_seconds, kv0, per_slice, op):
+def _oracle_all_cores(cfg, params, cpu_seconds, kv0, per_slice, op, min_rep=3):
     """The oracle on every host core: each process repeats the round trip of one
     (layer 0, batch 0, head) slice; the wall time of the parallel part is
     timed.  Returns (GB/s, cores, slices, s)."""
@@ -472,7 +472,7 @@ def _oracle_all_cores(cfg, params, cpu_seconds, kv0, per_slice, op):
     vb = kv0[1].contiguous().view(torch.int16).numpy().view(np.uint16)
     cs = oracle.rope_table(T, D, params.rope_theta) if params.rope_theta > 0 else None
     # at least three slices per process: the parallel wall time is then long enough to time stably
-    nrep = max(3, int(cpu_seconds / op.cores / max(per_slice, 1e-6)))
+    nrep = max(min_rep, int(cpu_seconds / op.cores / max(per_slice, 1e-6)))
     p = {"key_bits": params.key_bits, "value_bits": params.value_bits, "group_size": params.group_size,
          "strict": int(params.strict), "delta_chunk": params.delta_chunk}
     jobs = [(kb[w % kb.shape[0]], vb[w % vb.shape[0]], T, D, p, nrep, cs) for w in range(op.cores)]
@@ -498,6 +498,7 @@ def cpu_baseline(cfg, params, target_s, kv0=None):
         kv0 = (k[0], v[0])
     op = _OraclePool()
     try:
+        _oracle_all_cores(cfg, params, 0.0, kv0, per_slice, op, min_rep=1)  # untimed: warm every process
         gbs, cores, slices, wall = _oracle_all_cores(cfg, params, target_s / 2, kv0, per_slice, op)
     finally:
         op.close()
