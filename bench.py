@@ -56,11 +56,23 @@ def _peak_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def _kernel_src_hash():
+def _code_lines(text):
+    """The source's code without // comments, blank lines or indentation: a
+    comment edit leaves the kernels, and so the hash, unchanged."""
+    out = []
+    for line in text.splitlines():
+        code = line.split("//", 1)[0].strip()
+        if code:
+            out.append(code)
+    return "\n".join(out)
+
+
+def _kernel_src_hash(src_dir=None):
     h = hashlib.sha256()
-    for f in sorted(os.listdir(CSRC)):
-        with open(os.path.join(CSRC, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+    d = src_dir or CSRC
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), encoding="utf-8") as fh:
+            h.update(f.encode() + _code_lines(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

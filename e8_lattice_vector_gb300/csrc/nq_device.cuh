@@ -302,8 +302,9 @@ __device__ __forceinline__ bool e8_fast(const float (&u)[8], unsigned& code, uns
     constexpr float TWO23 = 8388608.0f;
     constexpr float BAND = 1.52587890625e-05f;  // 2^-16
     const float2 M2 = make_float2(kMagic, kMagic);
-    // clv_j = cs_j L^j with cs_j = copysign(1/2, e~0_j): the sign bit of e~0_j
-    // on the power of two L^j / 2 (one logic op, exact)
+    // clv_j = cs_j L^(j mod 4) with cs_j = copysign(1/2, e~0_j): the sign bit
+    // of e~0_j on the power of two L^(j mod 4) / 2 (one logic op, exact); the
+    // weights restart at each half-block, whose code is a field of its own
     float eb1[8], s0[8], clv[8];
     // S = sum |e~0_j| in two accumulators; the strict decoder sums
     // cs_j e~0_j = |e~0_j| / 2 instead (it needs cs_j for e~1 anyway), an
