@@ -36,3 +36,24 @@ def test_whole_job_rate_and_peak_helpers():
     assert bench.whole_job_gbs(4, 1e9, 500.0) == pytest.approx(8.0)
     peak, kind = bench._peak_hbm()
     assert peak > 0 and kind in ("measured", "fallback")
+
+
+def test_kernel_source_hash_ignores_comments_only(tmp_path):
+    """The traffic record stays valid across comment edits and is voided by code edits."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    src = os.path.join(ROOT, "e8_lattice_vector_gb300", "csrc")
+    for name in ("a", "b", "c"):
+        (tmp_path / name).mkdir()
+    for f in sorted(os.listdir(src)):
+        text = open(os.path.join(src, f), encoding="utf-8").read()
+        (tmp_path / "a" / f).write_text(text, encoding="utf-8")
+        (tmp_path / "b" / f).write_text("// a new comment line\n" + text.replace("\n", "  // note\n", 1),
+                                        encoding="utf-8")
+        (tmp_path / "c" / f).write_text(text + ("\nint extra_symbol = 1;\n" if f.endswith(".cu") else ""),
+                                        encoding="utf-8")
+    ha, hb, hc = (bench._kernel_src_hash(str(tmp_path / n)) for n in ("a", "b", "c"))
+    assert ha == bench._kernel_src_hash()
+    assert hb == ha
+    assert hc != ha
