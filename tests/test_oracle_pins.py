@@ -311,7 +311,8 @@ def test_f2h_round_to_nearest_even(orc):
         [65504, 65519.99, 65520, 70000, -65520, 1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11, -0.0, 0.0],
     ]).astype(np.float32)
     ours = orc.f2h(x)
-    ref = x.astype(np.float16).view(np.uint16)
+    with np.errstate(over="ignore"):  # the inputs past 65520 overflow to infinity on purpose
+        ref = x.astype(np.float16).view(np.uint16)
     assert np.array_equal(ours, ref)
 
 
