@@ -118,17 +118,47 @@ def _check_kv(x, name):
         raise ValueError("%s must be a contiguous fp16 CUDA tensor" % name)
 
 
+def _check_buf(buf, name="buf"):
+    if not (buf.is_cuda and buf.dtype == torch.uint8 and buf.is_contiguous()):
+        raise ValueError("%s must be a contiguous uint8 CUDA tensor" % name)
+
+
+def _check_like(x, shape, device, name):
+    """An fp16 tensor the library writes or reads as `shape` on `device`."""
+    _check_kv(x, name)
+    if shape_of(x) != shape:
+        raise ValueError("%s has shape %s; the call's shape is %s" % (name, shape_of(x), shape))
+    if x.device != device:
+        raise ValueError("%s is on %s; the call runs on %s" % (name, x.device, device))
+
+
+def _norm_shape(shape):
+    """(layers, batch, kv_heads, tokens, head_dim); a 4-D shape means batch 1."""
+    shape = tuple(int(v) for v in shape)
+    if len(shape) == 4:
+        return (shape[0], 1, shape[1], shape[2], shape[3])
+    if len(shape) != 5:
+        raise ValueError("shape must be [L,B,H,T,D] or [L,H,T,D], got %s" % (shape,))
+    return shape
+
+
+def _kv_shape(K, V):
+    _check_kv(K, "K")
+    shape = shape_of(K)
+    _check_like(V, shape, K.device, "V")
+    return shape
+
+
 def compress_kv(K, V, params, rope=None, out=None):
     """Compress K and V; returns (or fills) a uint8 device buffer of
     plan(...).total_bytes bytes."""
-    _check_kv(K, "K")
-    _check_kv(V, "V")
-    shape = shape_of(K)
-    if shape_of(V) != shape:
-        raise ValueError("K and V shapes differ")
+    shape = _kv_shape(K, V)
     lay = plan(shape, params)
     if out is None:
         out = torch.empty(max(int(lay.total_bytes), 16), dtype=torch.uint8, device=K.device)
+    _check_buf(out, "out")
+    if out.device != K.device:
+        raise ValueError("out is on %s; the call runs on %s" % (out.device, K.device))
     rp = _rope_ptr(rope, params, shape[3], shape[4])
     st = _lib.lib().nq_compress_kv(ctypes_void(K.data_ptr()), ctypes_void(V.data_ptr()), rp,
                                    ctypes_ref(_cshape(shape)), ctypes_ref(params.c()),
@@ -140,13 +170,14 @@ def compress_kv(K, V, params, rope=None, out=None):
 def decompress_kv(buf, shape, params, rope=None, K_out=None, V_out=None):
     """Decompress a buffer produced by compress_kv; returns (K, V) fp16 tensors
     of `shape` ([L,B,H,T,D])."""
-    shape = tuple(int(v) for v in shape)
+    shape = _norm_shape(shape)
+    _check_buf(buf)
     if K_out is None:
         K_out = torch.empty(shape, dtype=torch.float16, device=buf.device)
     if V_out is None:
         V_out = torch.empty(shape, dtype=torch.float16, device=buf.device)
-    _check_kv(K_out, "K_out")
-    _check_kv(V_out, "V_out")
+    _check_like(K_out, shape, buf.device, "K_out")
+    _check_like(V_out, shape, buf.device, "V_out")
     rp = _rope_ptr(rope, params, shape[3], shape[4])
     st = _lib.lib().nq_decompress_kv(ctypes_void(buf.data_ptr()), int(buf.numel()), rp,
                                      ctypes_ref(_cshape(shape)), ctypes_ref(params.c()),
@@ -160,19 +191,13 @@ def roundtrip_kv(K, V, params, rope=None, K_out=None, V_out=None):
     """decompress_kv(compress_kv(K, V)) in one pass, without the compressed
     buffer; returns (K_out, V_out).  Passing K_out=K, V_out=V reconstructs the
     cache in place."""
-    _check_kv(K, "K")
-    _check_kv(V, "V")
-    shape = shape_of(K)
-    if shape_of(V) != shape:
-        raise ValueError("K and V shapes differ")
+    shape = _kv_shape(K, V)
     if K_out is None:
         K_out = torch.empty_like(K)
     if V_out is None:
         V_out = torch.empty_like(V)
-    _check_kv(K_out, "K_out")
-    _check_kv(V_out, "V_out")
-    if shape_of(K_out) != shape or shape_of(V_out) != shape:
-        raise ValueError("output shapes differ from the input's")
+    _check_like(K_out, shape, K.device, "K_out")
+    _check_like(V_out, shape, K.device, "V_out")
     rp = _rope_ptr(rope, params, shape[3], shape[4])
     st = _lib.lib().nq_roundtrip_kv(ctypes_void(K.data_ptr()), ctypes_void(V.data_ptr()), rp,
                                     ctypes_ref(_cshape(shape)), ctypes_ref(params.c()),
@@ -201,7 +226,7 @@ def layer_profile(layers, key_bits=3, value_bits=2, protect_boundary=0):
 
 def plan_layers(shape, params, layer_bits):
     """(offsets per layer, total bytes) of the per-layer buffer."""
-    shape = tuple(int(v) for v in shape)
+    shape = _norm_shape(shape)
     table = _layer_table(layer_bits, shape[0])
     offs = (ctypes.c_uint64 * max(shape[0], 1))()
     total = ctypes.c_uint64(0)
@@ -214,14 +239,13 @@ def plan_layers(shape, params, layer_bits):
 def compress_kv_layers(K, V, params, layer_bits, rope=None, out=None):
     """Compress with a per-layer table of (key_bits, value_bits); (0, 0) keeps
     a layer in fp16.  Returns (or fills) the uint8 device buffer."""
-    _check_kv(K, "K")
-    _check_kv(V, "V")
-    shape = shape_of(K)
-    if shape_of(V) != shape:
-        raise ValueError("K and V shapes differ")
+    shape = _kv_shape(K, V)
     _, total = plan_layers(shape, params, layer_bits)
     if out is None:
         out = torch.empty(max(total, 16), dtype=torch.uint8, device=K.device)
+    _check_buf(out, "out")
+    if out.device != K.device:
+        raise ValueError("out is on %s; the call runs on %s" % (out.device, K.device))
     rp = _rope_ptr(rope, params, shape[3], shape[4])
     st = _lib.lib().nq_compress_kv_layers(ctypes_void(K.data_ptr()), ctypes_void(V.data_ptr()), rp,
                                           ctypes_ref(_cshape(shape)), ctypes_ref(params.c()),
@@ -232,13 +256,14 @@ def compress_kv_layers(K, V, params, layer_bits, rope=None, out=None):
 
 
 def decompress_kv_layers(buf, shape, params, layer_bits, rope=None, K_out=None, V_out=None):
-    shape = tuple(int(v) for v in shape)
+    shape = _norm_shape(shape)
+    _check_buf(buf)
     if K_out is None:
         K_out = torch.empty(shape, dtype=torch.float16, device=buf.device)
     if V_out is None:
         V_out = torch.empty(shape, dtype=torch.float16, device=buf.device)
-    _check_kv(K_out, "K_out")
-    _check_kv(V_out, "V_out")
+    _check_like(K_out, shape, buf.device, "K_out")
+    _check_like(V_out, shape, buf.device, "V_out")
     rp = _rope_ptr(rope, params, shape[3], shape[4])
     st = _lib.lib().nq_decompress_kv_layers(ctypes_void(buf.data_ptr()), int(buf.numel()), rp,
                                             ctypes_ref(_cshape(shape)), ctypes_ref(params.c()),
@@ -249,13 +274,11 @@ def decompress_kv_layers(buf, shape, params, layer_bits, rope=None, K_out=None, 
 
 
 def roundtrip_kv_layers(K, V, params, layer_bits, rope=None, K_out=None, V_out=None):
-    _check_kv(K, "K")
-    _check_kv(V, "V")
-    shape = shape_of(K)
+    shape = _kv_shape(K, V)
     K_out = torch.empty_like(K) if K_out is None else K_out
     V_out = torch.empty_like(V) if V_out is None else V_out
-    _check_kv(K_out, "K_out")
-    _check_kv(V_out, "V_out")
+    _check_like(K_out, shape, K.device, "K_out")
+    _check_like(V_out, shape, K.device, "V_out")
     rp = _rope_ptr(rope, params, shape[3], shape[4])
     st = _lib.lib().nq_roundtrip_kv_layers(ctypes_void(K.data_ptr()), ctypes_void(V.data_ptr()), rp,
                                            ctypes_ref(_cshape(shape)), ctypes_ref(params.c()),
@@ -268,7 +291,8 @@ def roundtrip_kv_layers(K, V, params, layer_bits, rope=None, K_out=None, V_out=N
 def code_histogram(buf, shape, params, counts=None):
     """Symbol counts of a compressed buffer: int64 device tensor [2, 274] (K, V)
     of field values [0, 16), idx bytes [16, 272) and coset bits [272, 274)."""
-    shape = tuple(int(v) for v in shape)
+    shape = _norm_shape(shape)
+    _check_buf(buf)
     if counts is None:
         counts = torch.empty((2, _lib.NQ_HIST_BINS), dtype=torch.int64, device=buf.device)
     if not (counts.is_cuda and counts.dtype == torch.int64 and counts.is_contiguous()

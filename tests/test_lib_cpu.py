@@ -214,3 +214,71 @@ def test_plan_joint_format_has_no_coset_words(nq):
     assert l2.k_idx_row_bytes == l1.k_idx_row_bytes  # 8b bits per block either way
     rows = l1.rows
     assert l1.total_bytes - l2.total_bytes >= 2 * (rows * 2 // 256 * 256)
+
+
+class _FakeCuda:
+    """Stand-in for a CUDA tensor: the binding's argument checks read only
+    these attributes, and every case below is rejected before any CUDA call."""
+
+    def __init__(self, shape, dtype, device="cuda:0", contiguous=True):
+        import torch
+
+        self.shape = torch.Size(shape)
+        self.dtype = dtype
+        self.device = torch.device(device)
+        self.is_cuda = True
+        self._contiguous = contiguous
+
+    def dim(self):
+        return len(self.shape)
+
+    def is_contiguous(self):
+        return self._contiguous
+
+    def numel(self):
+        n = 1
+        for v in self.shape:
+            n *= v
+        return n
+
+    def data_ptr(self):
+        return 256
+
+
+def test_binding_rejects_mismatched_outputs_before_the_gpu():
+    import torch
+
+    import e8_lattice_vector_gb300 as nq
+    from e8_lattice_vector_gb300 import CodecParams, codec
+
+    p = CodecParams(2, 2, 64, 0, 0, 0.0)
+    shp = (2, 1, 8, 64, 128)
+    K = _FakeCuda(shp, torch.float16)
+    buf = _FakeCuda((1 << 20,), torch.uint8)
+
+    def raises(fn, text):
+        with pytest.raises(ValueError, match=text):
+            fn()
+
+    raises(lambda: nq.compress_kv(K, _FakeCuda((2, 1, 8, 32, 128), torch.float16), p), "V has shape")
+    raises(lambda: nq.compress_kv(K, _FakeCuda(shp, torch.float16, "cuda:1"), p), "V is on")
+    raises(lambda: nq.compress_kv(K, K, p, out=_FakeCuda((1 << 20,), torch.float32)), "out must be")
+    raises(lambda: nq.compress_kv(K, K, p, out=_FakeCuda((1 << 20,), torch.uint8, "cuda:1")), "out is on")
+    small = _FakeCuda((2, 1, 8, 32, 128), torch.float16)
+    raises(lambda: nq.decompress_kv(buf, shp, p, K_out=small, V_out=K), "K_out has shape")
+    raises(lambda: nq.decompress_kv(buf, shp, p, K_out=K, V_out=_FakeCuda(shp, torch.float16, "cuda:1")),
+           "V_out is on")
+    raises(lambda: nq.decompress_kv(_FakeCuda((1 << 20,), torch.int32), shp, p, K_out=K, V_out=K), "buf must be")
+    raises(lambda: nq.decompress_kv(buf, shp, p, K_out=_FakeCuda(shp, torch.float16, contiguous=False), V_out=K),
+           "K_out must be")
+    raises(lambda: nq.roundtrip_kv(K, K, p, K_out=small, V_out=K), "K_out has shape")
+    table = [(2, 2), (0, 0)]
+    raises(lambda: nq.roundtrip_kv_layers(K, small, p, table), "V has shape")
+    raises(lambda: nq.decompress_kv_layers(buf, shp, p, table, K_out=K, V_out=small), "V_out has shape")
+    raises(lambda: nq.code_histogram(_FakeCuda((64,), torch.float16), shp, p), "buf must be")
+    # 4-D shapes mean batch 1; anything else is refused
+    assert codec._norm_shape((2, 8, 64, 128)) == (2, 1, 8, 64, 128)
+    raises(lambda: codec._norm_shape((8, 64, 128)), "shape must be")
+    # a 4-D K with a 4-D output of the same cache passes the shape check (then stops at V's device)
+    K4 = _FakeCuda((2, 8, 64, 128), torch.float16)
+    raises(lambda: nq.roundtrip_kv(K4, _FakeCuda((2, 8, 64, 128), torch.float16, "cuda:1"), p), "V is on")
