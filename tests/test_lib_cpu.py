@@ -282,3 +282,54 @@ def test_binding_rejects_mismatched_outputs_before_the_gpu():
     # a 4-D K with a 4-D output of the same cache passes the shape check (then stops at V's device)
     K4 = _FakeCuda((2, 8, 64, 128), torch.float16)
     raises(lambda: nq.roundtrip_kv(K4, _FakeCuda((2, 8, 64, 128), torch.float16, "cuda:1"), p), "V is on")
+
+
+def test_binding_passes_valid_calls_through_to_the_library(monkeypatch):
+    """The call shapes the benchmark, smoke check and parity tests use (5-D and
+    4-D caches, per-layer slices as outputs, in-place round trips) pass the
+    argument checks and reach the C entry point once each."""
+    import torch
+
+    import e8_lattice_vector_gb300 as nq
+    from e8_lattice_vector_gb300 import CodecParams, _lib, codec
+
+    real = _lib.lib()
+    calls = []
+
+    class _Recorder:
+        def __getattr__(self, name):
+            if name.startswith("nq_plan"):
+                return getattr(real, name)  # host-only sizing
+
+            def entry(*args):
+                calls.append(name)
+                return 0
+
+            return entry
+
+    monkeypatch.setattr(_lib, "lib", lambda: _Recorder())
+    monkeypatch.setattr(codec, "_stream_handle", lambda device: None)
+    p = CodecParams(2, 2, 64, 0, 0, 0.0)
+    shp = (2, 1, 8, 64, 128)
+    K, V = _FakeCuda(shp, torch.float16), _FakeCuda(shp, torch.float16)
+    lay = nq.plan(shp, p)
+    buf = _FakeCuda((int(lay.total_bytes),), torch.uint8)
+    nq.compress_kv(K, V, p, out=buf)
+    nq.decompress_kv(buf, shp, p, K_out=K, V_out=V)
+    nq.roundtrip_kv(K, V, p, K_out=K, V_out=V)
+    lshape = (1,) + shp[1:]  # one layer of the cache into a slice of the outputs
+    lbuf = _FakeCuda((int(nq.plan(lshape, p).total_bytes),), torch.uint8)
+    nq.compress_kv(_FakeCuda(lshape, torch.float16), _FakeCuda(lshape, torch.float16), p, out=lbuf)
+    nq.decompress_kv(lbuf, lshape, p, K_out=_FakeCuda(lshape, torch.float16), V_out=_FakeCuda(lshape, torch.float16))
+    K4 = _FakeCuda((2, 8, 64, 128), torch.float16)
+    nq.roundtrip_kv(K4, _FakeCuda((2, 8, 64, 128), torch.float16), p, K_out=K4, V_out=_FakeCuda(shp, torch.float16))
+    table = [(2, 2), (0, 0)]
+    _, total = nq.plan_layers(shp, p, table)
+    nbuf = _FakeCuda((total,), torch.uint8)
+    nq.compress_kv_layers(K, V, p, table, out=nbuf)
+    nq.decompress_kv_layers(nbuf, shp, p, table, K_out=K, V_out=V)
+    nq.roundtrip_kv_layers(K, V, p, table, K_out=K, V_out=V)
+    nq.code_histogram(buf, shp, p, counts=_FakeCuda((2, _lib.NQ_HIST_BINS), torch.int64))
+    assert calls == ["nq_compress_kv", "nq_decompress_kv", "nq_roundtrip_kv", "nq_compress_kv", "nq_decompress_kv",
+                     "nq_roundtrip_kv", "nq_compress_kv_layers", "nq_decompress_kv_layers", "nq_roundtrip_kv_layers",
+                     "nq_code_histogram"]
