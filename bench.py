@@ -41,7 +41,7 @@ def _args():
     ap.add_argument("--config", default="llama31_8b")
     ap.add_argument("--strict", action="store_true", help="strict E8 parity instead of relaxed")
     ap.add_argument("--joint", action="store_true", help="strict E8 in the joint 8b-bit format (no coset words)")
-    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--e2e-steps", type=int, default=4)
     ap.add_argument("--fused-steps", type=int, default=10, help="timed nq_roundtrip_kv calls (0: skip)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
