@@ -305,8 +305,10 @@ void orc_decode_row(const uint8_t* idx, uint16_t coset, const uint16_t* scales,
 }
 
 /* [NEG, temporal delta entry]: subtract the previous token's index.  Reading:
- * per field modulo 2^b, the coset bits by exclusive or; scales are stored
- * as they are. */
+ * the forward difference (this token's code minus the previous token's) per
+ * field modulo 2^b, the coset bits by exclusive or; scales are stored as they
+ * are.  (The entry's wording, read literally, subtracts in the other order;
+ * both orders are lossless and give the same symbol entropy.) */
 void orc_delta_row(uint8_t* idx, uint16_t* coset, const uint8_t* prev_idx, uint16_t prev_coset,
                    int dp, int bits) {
     unsigned mask = (1u << bits) - 1u;

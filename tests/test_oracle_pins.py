@@ -401,6 +401,63 @@ def test_t7_delta_round_trip_and_field_ranges(orc, bits):
     assert np.all(fields[coset_bit == 0] <= L - 2)
 
 
+def _unpack_fields(idx, bits, n):
+    """b-bit fields of packed rows (field i at bit i*b, LSB first), [rows, n]."""
+    a = np.unpackbits(np.atleast_2d(np.asarray(idx, np.uint8)), axis=1, bitorder="little")[:, : n * bits]
+    return (a.reshape(a.shape[0], n, bits) * (1 << np.arange(bits))).sum(-1)
+
+
+# Hand-computed forward differences d = (cur - prev) mod 2^b, field by field, at
+# the start of the row (the rest of the 128 fields are zero in both rows).
+DELTA_CASES = {
+    2: ([0, 3, 1, 2, 3, 0, 2, 1], [3, 0, 2, 2, 1, 1, 3, 0], [1, 3, 3, 0, 2, 3, 3, 1]),
+    3: ([0, 7, 2, 5, 6, 1, 4, 3], [7, 0, 5, 5, 2, 6, 4, 1], [1, 7, 5, 0, 4, 3, 0, 2]),
+    4: ([0, 15, 3, 9, 14, 6, 8, 1], [15, 0, 12, 9, 2, 11, 8, 4], [1, 15, 7, 0, 12, 11, 0, 13]),
+}
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_t7_delta_row_hand_built(orc, bits):
+    """Temporal delta ("Negative results", entropy-coded indices entry: subtract
+    the previous token's index): every field of the delta row is the current
+    code minus the previous token's code modulo 2^b, wrap-around included, and
+    the coset word is XORed.  The expected rows are packed here independently
+    of the oracle.  A field-wise XOR, a reversed difference or a carry between
+    fields fails this."""
+    cur, prev, want = (list(v) + [0] * (128 - len(v)) for v in DELTA_CASES[bits])
+    d, cw = orc.delta_row(_pack_fields(cur, bits), 0xA5C3, _pack_fields(prev, bits), 0x0FF0, 128, bits)
+    assert list(_unpack_fields(d, bits, 128)[0]) == want
+    assert np.array_equal(d, _pack_fields(want, bits))
+    assert cw == 0xA5C3 ^ 0x0FF0 == 0xAA33
+    back, c2 = orc.undelta_row(_pack_fields(want, bits), 0xAA33, _pack_fields(prev, bits), 0x0FF0, 128, bits)
+    assert np.array_equal(back, _pack_fields(cur, bits)) and c2 == 0xA5C3
+
+
+@pytest.mark.parametrize("bits,chunk", [(2, 32), (3, 64), (4, 512)])
+def test_t7_delta_tensor_is_difference_of_raw_codes(orc, bits, chunk):
+    """Along the tokens of a slice, every delta row holds the raw codes of its
+    token minus those of the token before (not minus the previous stored
+    delta), each chunk's first token is stored raw, scales are untouched, and
+    chunk >= tokens is one chain per slice."""
+    rng = np.random.default_rng(30 + bits)
+    slices, T, D, G = 2, 100, 128, 64
+    x = _rand_fp16(rng, (slices, T, D))
+    raw_i, raw_c, raw_s = orc.compress_tensor(x, T, D, bits, G, 0, 0)
+    del_i, del_c, del_s = orc.compress_tensor(x, T, D, bits, G, 0, chunk)
+    assert np.array_equal(raw_s, del_s)
+    L = 1 << bits
+    f_raw = _unpack_fields(raw_i, bits, D).reshape(slices, T, D)
+    f_del = _unpack_fields(del_i, bits, D).reshape(slices, T, D)
+    c_raw = raw_c.reshape(slices, T)
+    c_del = del_c.reshape(slices, T)
+    for t in range(T):
+        if t % chunk == 0:
+            assert np.array_equal(f_del[:, t], f_raw[:, t]) and np.array_equal(c_del[:, t], c_raw[:, t])
+        else:
+            assert np.array_equal(f_del[:, t], (f_raw[:, t] - f_raw[:, t - 1]) % L), t
+            assert np.array_equal(c_del[:, t], c_raw[:, t] ^ c_raw[:, t - 1]), t
+
+
 def test_t7_delta_row_inverse(orc):
     rng = np.random.default_rng(17)
     for bits in (2, 3, 4):
