@@ -363,7 +363,7 @@ def run_ours(a):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32",
+        "dtype": "fp16",
         "data": "synthetic",
         "config": {
             "workload": "%s KV cache %s fp16, K%dV%d group %d %s E8, delta %s, compress+decompress round trip"
@@ -556,7 +556,7 @@ def run_reference(a):
         "metric": "KV compress/decompress GB/s (fp16 in) on 1 GB300; % of HBM roofline",
         "value": round(value, 5), "unit": "GB/s", "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup,
         "ms_per_step": round(dt / a.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "vs_baseline": None, "dtype": "fp16", "data": "synthetic",
         "config": {"workload": "%s KV cache (sampled), K%dV%d group %d %s E8" % (
             cfg.name, params.key_bits, params.value_bits, params.group_size,
             {0: "relaxed", 1: "strict", 2: "strict (joint format)"}[int(params.strict)])},

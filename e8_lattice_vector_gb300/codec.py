@@ -102,7 +102,7 @@ class RopeTable:
         return h.transpose(1, 0, 2).reshape(self.tokens, self.head_dim // 2, 2)
 
 
-def _rope_ptr(rope, params, tokens, head_dim):
+def _rope_ptr(rope, params, tokens, head_dim, device):
     if params.rope_theta <= 0:
         return None
     if rope is None:
@@ -110,7 +110,23 @@ def _rope_ptr(rope, params, tokens, head_dim):
     if rope.tokens != tokens or rope.head_dim != head_dim or rope.theta != params.rope_theta:
         raise ValueError("RopeTable (%d tokens, head_dim %d, theta %g) does not match the call"
                          % (rope.tokens, rope.head_dim, rope.theta))
+    if rope.device.device != device:
+        raise ValueError("RopeTable is on %s; the call runs on %s" % (rope.device.device, device))
     return ctypes_void(rope.device.data_ptr())
+
+
+def _on(device):
+    """The library sizes its grids and launches on the current device: make it
+    the tensors' device for the duration of a call."""
+    return torch.cuda.device(device)
+
+
+def _call(device, name, *args):
+    """One library call with `device` current (the library sizes its grids and
+    sets kernel attributes on the current device); raises on a bad status."""
+    with _on(device):
+        st = getattr(_lib.lib(), name)(*args)
+    _lib.check(name, st)
 
 
 def _check_kv(x, name):
@@ -159,11 +175,10 @@ def compress_kv(K, V, params, rope=None, out=None):
     _check_buf(out, "out")
     if out.device != K.device:
         raise ValueError("out is on %s; the call runs on %s" % (out.device, K.device))
-    rp = _rope_ptr(rope, params, shape[3], shape[4])
-    st = _lib.lib().nq_compress_kv(ctypes_void(K.data_ptr()), ctypes_void(V.data_ptr()), rp,
-                                   ctypes_ref(_cshape(shape)), ctypes_ref(params.c()),
-                                   ctypes_void(out.data_ptr()), int(out.numel()), _stream_handle(K.device))
-    _lib.check("nq_compress_kv", st)
+    rp = _rope_ptr(rope, params, shape[3], shape[4], K.device)
+    _call(K.device, "nq_compress_kv", ctypes_void(K.data_ptr()), ctypes_void(V.data_ptr()), rp,
+          ctypes_ref(_cshape(shape)), ctypes_ref(params.c()), ctypes_void(out.data_ptr()), int(out.numel()),
+          _stream_handle(K.device))
     return out
 
 
@@ -178,12 +193,10 @@ def decompress_kv(buf, shape, params, rope=None, K_out=None, V_out=None):
         V_out = torch.empty(shape, dtype=torch.float16, device=buf.device)
     _check_like(K_out, shape, buf.device, "K_out")
     _check_like(V_out, shape, buf.device, "V_out")
-    rp = _rope_ptr(rope, params, shape[3], shape[4])
-    st = _lib.lib().nq_decompress_kv(ctypes_void(buf.data_ptr()), int(buf.numel()), rp,
-                                     ctypes_ref(_cshape(shape)), ctypes_ref(params.c()),
-                                     ctypes_void(K_out.data_ptr()), ctypes_void(V_out.data_ptr()),
-                                     _stream_handle(buf.device))
-    _lib.check("nq_decompress_kv", st)
+    rp = _rope_ptr(rope, params, shape[3], shape[4], buf.device)
+    _call(buf.device, "nq_decompress_kv", ctypes_void(buf.data_ptr()), int(buf.numel()), rp,
+          ctypes_ref(_cshape(shape)), ctypes_ref(params.c()), ctypes_void(K_out.data_ptr()),
+          ctypes_void(V_out.data_ptr()), _stream_handle(buf.device))
     return K_out, V_out
 
 
@@ -198,12 +211,10 @@ def roundtrip_kv(K, V, params, rope=None, K_out=None, V_out=None):
         V_out = torch.empty_like(V)
     _check_like(K_out, shape, K.device, "K_out")
     _check_like(V_out, shape, K.device, "V_out")
-    rp = _rope_ptr(rope, params, shape[3], shape[4])
-    st = _lib.lib().nq_roundtrip_kv(ctypes_void(K.data_ptr()), ctypes_void(V.data_ptr()), rp,
-                                    ctypes_ref(_cshape(shape)), ctypes_ref(params.c()),
-                                    ctypes_void(K_out.data_ptr()), ctypes_void(V_out.data_ptr()),
-                                    _stream_handle(K.device))
-    _lib.check("nq_roundtrip_kv", st)
+    rp = _rope_ptr(rope, params, shape[3], shape[4], K.device)
+    _call(K.device, "nq_roundtrip_kv", ctypes_void(K.data_ptr()), ctypes_void(V.data_ptr()), rp,
+          ctypes_ref(_cshape(shape)), ctypes_ref(params.c()), ctypes_void(K_out.data_ptr()),
+          ctypes_void(V_out.data_ptr()), _stream_handle(K.device))
     return K_out, V_out
 
 
@@ -246,12 +257,10 @@ def compress_kv_layers(K, V, params, layer_bits, rope=None, out=None):
     _check_buf(out, "out")
     if out.device != K.device:
         raise ValueError("out is on %s; the call runs on %s" % (out.device, K.device))
-    rp = _rope_ptr(rope, params, shape[3], shape[4])
-    st = _lib.lib().nq_compress_kv_layers(ctypes_void(K.data_ptr()), ctypes_void(V.data_ptr()), rp,
-                                          ctypes_ref(_cshape(shape)), ctypes_ref(params.c()),
-                                          _layer_table(layer_bits, shape[0]), ctypes_void(out.data_ptr()),
-                                          int(out.numel()), _stream_handle(K.device))
-    _lib.check("nq_compress_kv_layers", st)
+    rp = _rope_ptr(rope, params, shape[3], shape[4], K.device)
+    _call(K.device, "nq_compress_kv_layers", ctypes_void(K.data_ptr()), ctypes_void(V.data_ptr()), rp,
+          ctypes_ref(_cshape(shape)), ctypes_ref(params.c()), _layer_table(layer_bits, shape[0]),
+          ctypes_void(out.data_ptr()), int(out.numel()), _stream_handle(K.device))
     return out
 
 
@@ -264,12 +273,10 @@ def decompress_kv_layers(buf, shape, params, layer_bits, rope=None, K_out=None, 
         V_out = torch.empty(shape, dtype=torch.float16, device=buf.device)
     _check_like(K_out, shape, buf.device, "K_out")
     _check_like(V_out, shape, buf.device, "V_out")
-    rp = _rope_ptr(rope, params, shape[3], shape[4])
-    st = _lib.lib().nq_decompress_kv_layers(ctypes_void(buf.data_ptr()), int(buf.numel()), rp,
-                                            ctypes_ref(_cshape(shape)), ctypes_ref(params.c()),
-                                            _layer_table(layer_bits, shape[0]), ctypes_void(K_out.data_ptr()),
-                                            ctypes_void(V_out.data_ptr()), _stream_handle(buf.device))
-    _lib.check("nq_decompress_kv_layers", st)
+    rp = _rope_ptr(rope, params, shape[3], shape[4], buf.device)
+    _call(buf.device, "nq_decompress_kv_layers", ctypes_void(buf.data_ptr()), int(buf.numel()), rp,
+          ctypes_ref(_cshape(shape)), ctypes_ref(params.c()), _layer_table(layer_bits, shape[0]),
+          ctypes_void(K_out.data_ptr()), ctypes_void(V_out.data_ptr()), _stream_handle(buf.device))
     return K_out, V_out
 
 
@@ -279,12 +286,10 @@ def roundtrip_kv_layers(K, V, params, layer_bits, rope=None, K_out=None, V_out=N
     V_out = torch.empty_like(V) if V_out is None else V_out
     _check_like(K_out, shape, K.device, "K_out")
     _check_like(V_out, shape, K.device, "V_out")
-    rp = _rope_ptr(rope, params, shape[3], shape[4])
-    st = _lib.lib().nq_roundtrip_kv_layers(ctypes_void(K.data_ptr()), ctypes_void(V.data_ptr()), rp,
-                                           ctypes_ref(_cshape(shape)), ctypes_ref(params.c()),
-                                           _layer_table(layer_bits, shape[0]), ctypes_void(K_out.data_ptr()),
-                                           ctypes_void(V_out.data_ptr()), _stream_handle(K.device))
-    _lib.check("nq_roundtrip_kv_layers", st)
+    rp = _rope_ptr(rope, params, shape[3], shape[4], K.device)
+    _call(K.device, "nq_roundtrip_kv_layers", ctypes_void(K.data_ptr()), ctypes_void(V.data_ptr()), rp,
+          ctypes_ref(_cshape(shape)), ctypes_ref(params.c()), _layer_table(layer_bits, shape[0]),
+          ctypes_void(K_out.data_ptr()), ctypes_void(V_out.data_ptr()), _stream_handle(K.device))
     return K_out, V_out
 
 
@@ -298,10 +303,8 @@ def code_histogram(buf, shape, params, counts=None):
     if not (counts.is_cuda and counts.dtype == torch.int64 and counts.is_contiguous()
             and counts.numel() == 2 * _lib.NQ_HIST_BINS):
         raise ValueError("counts must be a contiguous int64 CUDA tensor of 2 * 274 entries")
-    st = _lib.lib().nq_code_histogram(ctypes_void(buf.data_ptr()), int(buf.numel()), ctypes_ref(_cshape(shape)),
-                                      ctypes_ref(params.c()), ctypes_void(counts.data_ptr()),
-                                      _stream_handle(buf.device))
-    _lib.check("nq_code_histogram", st)
+    _call(buf.device, "nq_code_histogram", ctypes_void(buf.data_ptr()), int(buf.numel()), ctypes_ref(_cshape(shape)),
+          ctypes_ref(params.c()), ctypes_void(counts.data_ptr()), _stream_handle(buf.device))
     return counts
 
 
@@ -310,9 +313,8 @@ def e8_nearest(u, strict, bits):
     if not (u.is_cuda and u.dtype == torch.float32 and u.is_contiguous() and u.shape[-1] == 8):
         raise ValueError("u must be a contiguous float32 CUDA tensor [..., 8]")
     out = torch.empty_like(u)
-    st = _lib.lib().nq_e8_nearest(ctypes_void(u.data_ptr()), ctypes_void(out.data_ptr()), u.numel() // 8,
-                                  int(bool(strict)), int(bits), _stream_handle(u.device))
-    _lib.check("nq_e8_nearest", st)
+    _call(u.device, "nq_e8_nearest", ctypes_void(u.data_ptr()), ctypes_void(out.data_ptr()), u.numel() // 8,
+          int(bool(strict)), int(bits), _stream_handle(u.device))
     return out
 
 

@@ -34,6 +34,13 @@ uint64_t layer_bytes(const nq_shape* s) {  // fp16 bytes of one tensor's layer
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Keys carry RoPE: the table every compressed layer will need, checked before
+// the first layer is enqueued (a kept layer's copies would otherwise be in
+// flight when a later layer rejects the table).
+bool rope_ok(const nq_params* p, const float* rope_table) {
+    return !(p->rope_theta > 0.0f) || (rope_table && aligned16(rope_table));
+}
+
 // Plan, then check the pointers the loop will use.
 int prepare(const nq_shape* shape, const nq_params* params, const nq_layer_bits* per_layer,
             std::vector<uint64_t>& offs, uint64_t* total) {
@@ -86,6 +93,7 @@ int nq_compress_kv_layers(const void* k_f16, const void* v_f16, const float* rop
     const uint64_t lb = layer_bytes(shape);
     if (offs.empty() || lb == 0) return NQ_OK;
     if (!k_f16 || !v_f16 || !out || !aligned16(k_f16) || !aligned16(v_f16) || !aligned16(out)) return NQ_ERR_ARG;
+    if (!rope_ok(params, rope_table)) return NQ_ERR_ARG;
     if (out_bytes < total) return NQ_ERR_SIZE;
     const nq_shape s1 = one_layer(shape);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -116,6 +124,7 @@ int nq_decompress_kv_layers(const void* in, size_t in_bytes, const float* rope_t
     if (offs.empty() || lb == 0) return NQ_OK;
     if (!in || !k_f16_out || !v_f16_out || !aligned16(in) || !aligned16(k_f16_out) || !aligned16(v_f16_out))
         return NQ_ERR_ARG;
+    if (!rope_ok(params, rope_table)) return NQ_ERR_ARG;
     if (in_bytes < total) return NQ_ERR_SIZE;
     const nq_shape s1 = one_layer(shape);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -147,6 +156,7 @@ int nq_roundtrip_kv_layers(const void* k_f16, const void* v_f16, const float* ro
     if (!k_f16 || !v_f16 || !k_f16_out || !v_f16_out || !aligned16(k_f16) || !aligned16(v_f16) ||
         !aligned16(k_f16_out) || !aligned16(v_f16_out))
         return NQ_ERR_ARG;
+    if (!rope_ok(params, rope_table)) return NQ_ERR_ARG;
     const nq_shape s1 = one_layer(shape);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     for (size_t l = 0; l < offs.size() && st == NQ_OK; ++l) {

@@ -110,9 +110,12 @@ typedef struct {
 } nq_layout;
 
 /* Validate shape and params and describe the compressed buffer.  Host only.
- * Format: the section table above; the method's "lattice indices (packed
- * uint8)" and "one FP16 scale per group" ("E8 walkthrough", sections "Bit
- * Rate Accounting" and "Why Per-Group Scaling?"). */
+ * Format: the section table above.  The method stores the lattice indices
+ * packed into bytes ("E8 walkthrough", section "Bit Rate Accounting") and
+ * gives every group of coordinates an fp16 scale; that section and "Why
+ * Per-Group Scaling?" scale every 8 values (and the per-head variant every
+ * 128), while this format keeps one fp16 scale per group_size coordinates
+ * (64 in the target workloads). */
 int nq_plan(const nq_shape* shape, const nq_params* params, nq_layout* out);
 
 /* RoPE (cos, sin) table for split-half rotary embedding ("E8 walkthrough",

@@ -139,8 +139,10 @@ static uint16_t half_next_down(uint16_t v) { return (uint16_t)(v - 1); } /* v > 
 /* [WALK "Python Implementation" quantize(): sc = amax / (levels/2)].
  * Reading: the divisor is (levels - 1)/2 so that the half-integer grid of the
  * box holds exactly 2^bits levels (the pages' levels/2 box holds more lattice
- * points than b bits can index).  The scale is stored as binary16 [WALK "Why
- * Per-Group Scaling?": one FP16 scale per group]; the smallest binary16 value
+ * points than b bits can index).  The scale is stored as binary16, one per
+ * group [WALK "Why Per-Group Scaling?" uses groups of 8 values and the
+ * per-head variant groups of 128; this format takes the group size as a
+ * parameter, 64 in the target workloads]; the smallest binary16 value
  * that does not clip is taken, so no scaled coordinate leaves the box.  The
  * Hadamard gain dp is folded in so the stored scale never overflows binary16. */
 uint16_t orc_group_scale(float amax, int bits, int dp) {

@@ -362,70 +362,103 @@ def _sample_rows(rng, cfg, n):
     return np.unique(np.concatenate([pick, extra]) % rows)
 
 
+def _full_size_check(nq, orc, cfg, K, V, params, rows, cs):
+    """One codec mode on a full-size cache: the sampled rows' records against
+    the oracle's encoding of those rows (delta rows against the oracle's
+    encoding of the previous token too), the sampled reconstructions against
+    the oracle's decoding, and the one-pass round trip against
+    decompress(compress(.)) on every element.  cs: the oracle's own RoPE
+    table [tokens, head_dim/2, 2]."""
+    T, D = cfg.tokens, cfg.head_dim
+    rope = nq.RopeTable.build(T, D, params.rope_theta)
+    buf = nq.compress_kv(K, V, params, rope)
+    lay = nq.plan(cfg.shape, params)
+    tp = int(lay.tokens_padded)
+    full = nq.sections(buf, lay)
+    rec = torch.from_numpy((rows // T) * tp + rows % T).cuda()  # record rows of the sampled tokens
+    got = {}
+    for t in ("k", "v"):
+        got[t] = (full[t + "_idx"][rec].cpu().numpy(),
+                  full[t + "_coset"][rec].cpu().numpy().view(np.uint16),
+                  full[t + "_scale"][rec].contiguous().view(torch.int16).cpu().numpy().view(np.uint16))
+    Kf = K.view(-1, D)
+    Vf = V.view(-1, D)
+    rows_t = torch.from_numpy(rows).cuda()
+    prev_t = torch.from_numpy(np.maximum(rows - 1, 0)).cuda()
+    for name_t, X, bits, rope_on in (("k", Kf, params.key_bits, True), ("v", Vf, params.value_bits, False)):
+        xr = _bits(X[rows_t])
+        xp = _bits(X[prev_t])
+        gi, gc, gs = got[name_t]
+        for n, r in enumerate(rows):
+            t = int(r % T)
+            csr = cs[t] if rope_on else None
+            idx, cw, sc = orc.encode_row(xr[n], D, bits, params.group_size, int(params.strict), csr)
+            if params.delta_chunk and t % params.delta_chunk != 0:
+                pidx, pcw, _ = orc.encode_row(xp[n], D, bits, params.group_size, int(params.strict),
+                                              cs[t - 1] if rope_on else None)
+                idx, cw = orc.delta_row(idx, cw, pidx, pcw, orc.padded_dim(D), bits)
+            assert np.array_equal(gs[n], sc), (name_t, r)
+            assert gc[n] == cw, (name_t, r)
+            assert np.array_equal(gi[n], idx), (name_t, r)
+    # decompression of the same rows against the oracle's decoding of its own
+    # encoding of the raw rows (the GPU side restores them through the delta chain)
+    K2, V2 = nq.decompress_kv(buf, cfg.shape, params, rope)
+    for name_t, X2, bits, rope_on in (("k", K2, params.key_bits, True), ("v", V2, params.value_bits, False)):
+        xr2 = _bits(X2.view(-1, D)[rows_t])
+        xr = _bits((K if name_t == "k" else V).view(-1, D)[rows_t])
+        ref = np.empty_like(xr2)
+        for n, r in enumerate(rows):
+            t = int(r % T)
+            csr = cs[t] if rope_on else None
+            idx, cw, sc = orc.encode_row(xr[n], D, bits, params.group_size, int(params.strict), csr)
+            ref[n] = orc.decode_row(idx, cw, sc, D, bits, params.group_size, csr)
+        _assert_recon(xr2, ref)
+        assert _same_values(xr2, ref)
+    # the one-pass round trip equals decompress(compress(.)) everywhere
+    K3, V3 = nq.roundtrip_kv(K, V, params, rope)
+    assert bool((K3 == K2).all()) and bool((V3 == V2).all())
+    del buf, K2, V2, K3, V3
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("name", ["mistral7b", "phi3mini", "llama31_8b", "qwen25_14b"])
 def test_full_size_sampled_parity(nq, orc, name):
-    """Each full-size cache compressed and decompressed by the same library call
-    the benchmark times; a sample of rows re-computed one by one by the oracle."""
+    """Each full-size cache in every codec mode it is served in, compressed and
+    decompressed by the same library calls the benchmark times; a sample of
+    rows re-computed one by one by the oracle, with the oracle's own RoPE
+    table."""
     from e8_lattice_vector_gb300.synth import CONFIGS, make_cache
 
     cfg = CONFIGS[name]
     K, V = make_cache(cfg, device="cuda")
-    T, D = cfg.tokens, cfg.head_dim
-    rng = np.random.default_rng(1234)
-    rows = _sample_rows(rng, cfg, 600)
-    cs = None
-    for params in cfg.modes[:2]:
-        rope = nq.RopeTable.build(T, D, params.rope_theta)
-        if cs is None:
-            cs = rope.pairs()
-        buf = nq.compress_kv(K, V, params, rope)
-        lay = nq.plan(cfg.shape, params)
-        tp = int(lay.tokens_padded)
-        full = nq.sections(buf, lay)
-        rec = torch.from_numpy((rows // T) * tp + rows % T).cuda()  # record rows of the sampled tokens
-        got = {}
-        for t in ("k", "v"):
-            got[t] = (full[t + "_idx"][rec].cpu().numpy(),
-                      full[t + "_coset"][rec].cpu().numpy().view(np.uint16),
-                      full[t + "_scale"][rec].contiguous().view(torch.int16).cpu().numpy().view(np.uint16))
-        Kf = K.view(-1, D)
-        Vf = V.view(-1, D)
-        rows_t = torch.from_numpy(rows).cuda()
-        prev_t = torch.from_numpy(np.maximum(rows - 1, 0)).cuda()
-        for name_t, X, bits, rope_on in (("k", Kf, params.key_bits, True), ("v", Vf, params.value_bits, False)):
-            xr = _bits(X[rows_t])
-            xp = _bits(X[prev_t])
-            gi, gc, gs = got[name_t]
-            for n, r in enumerate(rows):
-                t = int(r % T)
-                csr = cs[t] if rope_on else None
-                idx, cw, sc = orc.encode_row(xr[n], D, bits, params.group_size, int(params.strict), csr)
-                if params.delta_chunk and t % params.delta_chunk != 0:
-                    pidx, pcw, _ = orc.encode_row(xp[n], D, bits, params.group_size, int(params.strict),
-                                                  cs[t - 1] if rope_on else None)
-                    idx, cw = orc.delta_row(idx, cw, pidx, pcw, orc.padded_dim(D), bits)
-                assert np.array_equal(gs[n], sc), (name_t, r)
-                assert gc[n] == cw, (name_t, r)
-                assert np.array_equal(gi[n], idx), (name_t, r)
-        # decompression of the same rows against the oracle's decoding of the
-        # (already verified) GPU records, restored from the raw codes
-        K2, V2 = nq.decompress_kv(buf, cfg.shape, params, rope)
-        for name_t, X2, bits, rope_on in (("k", K2, params.key_bits, True), ("v", V2, params.value_bits, False)):
-            xr2 = _bits(X2.view(-1, D)[torch.from_numpy(rows).cuda()])
-            xr = _bits((K if name_t == "k" else V).view(-1, D)[torch.from_numpy(rows).cuda()])
-            ref = np.empty_like(xr2)
-            for n, r in enumerate(rows):
-                t = int(r % T)
-                csr = cs[t] if rope_on else None
-                idx, cw, sc = orc.encode_row(xr[n], D, bits, params.group_size, int(params.strict), csr)
-                ref[n] = orc.decode_row(idx, cw, sc, D, bits, params.group_size, csr)
-            _assert_recon(xr2, ref)
-            assert _same_values(xr2, ref)
-        # the one-pass round trip equals decompress(compress(.)) everywhere
-        K3, V3 = nq.roundtrip_kv(K, V, params, rope)
-        assert bool((K3 == K2).all()) and bool((V3 == V2).all())
-        del buf, K2, V2, K3, V3
-        torch.cuda.empty_cache()
+    rows = _sample_rows(np.random.default_rng(1234), cfg, 600)
+    cs = orc.rope_table(cfg.tokens, cfg.head_dim, cfg.theta)
+    for params in cfg.modes:
+        assert params.rope_theta == cfg.theta
+        _full_size_check(nq, orc, cfg, K, V, params, rows, cs)
+
+
+@pytest.mark.parametrize("name,kb,vb", [("mistral7b", 2, 2), ("phi3mini", 3, 2)])
+def test_full_size_single_chain_delta(nq, orc, name, kb, vb):
+    """The pages' temporal delta as one chain per slice (delta_chunk >= tokens)
+    on a full-size cache: sampled rows deep in the chain (their predecessors
+    span many tiles) are checked against the oracle, and their reconstructions
+    need every earlier delta row of the slice."""
+    from e8_lattice_vector_gb300 import CodecParams
+    from e8_lattice_vector_gb300.synth import CONFIGS, make_cache
+
+    cfg = CONFIGS[name]
+    K, V = make_cache(cfg, device="cuda")
+    T = cfg.tokens
+    chain = (T + 31) // 32 * 32
+    rng = np.random.default_rng(4321)
+    rows = _sample_rows(rng, cfg, 400)
+    # the last tokens of a few slices depend on the whole chain
+    ends = (rng.choice(cfg.rows // T, size=8, replace=False) + 1) * T - 1
+    rows = np.unique(np.concatenate([rows, ends, ends - 33]))
+    cs = orc.rope_table(T, cfg.head_dim, cfg.theta)
+    params = CodecParams(kb, vb, 64, 0, chain, cfg.theta)
+    _full_size_check(nq, orc, cfg, K, V, params, rows, cs)
 
 
 @pytest.mark.parametrize("name,kb,vb", [("mistral7b", 2, 2), ("phi3mini", 3, 2)])
@@ -441,7 +474,7 @@ def test_full_size_joint_format(nq, orc, name, kb, vb):
     T, D = cfg.tokens, cfg.head_dim
     params = CodecParams(kb, vb, 64, 2, 0, cfg.theta)
     rope = nq.RopeTable.build(T, D, params.rope_theta)
-    cs = rope.pairs()
+    cs = orc.rope_table(T, D, params.rope_theta)  # the oracle's own table
     buf = nq.compress_kv(K, V, params, rope)
     lay = nq.plan(cfg.shape, params)
     assert lay.k_coset == lay.k_scale and lay.v_coset == lay.v_scale

@@ -1,6 +1,7 @@
 """Host-side checks of libnq that need no GPU: the library loads, exports every
 symbol include/nq.h declares, and its host-only entry points (layout, RoPE
 table, argument validation) behave as specified."""
+import contextlib
 import ctypes
 import os
 import re
@@ -203,6 +204,13 @@ def test_layers_validate_before_touching_the_gpu(nq):
     assert L.nq_roundtrip_kv_layers(p16, p16, p16, sh, pr, half, p16, p16, None) == nq.NQ_ERR_UNSUPPORTED
     empty = nq.Shape(0, 1, 8, 64, 128)
     assert L.nq_compress_kv_layers(None, None, None, ctypes.byref(empty), pr, None, None, 0, None) == 0
+    # a kept first layer: the missing or misaligned RoPE table is refused before its copies are enqueued
+    p17 = ctypes.c_void_p(17)
+    for table in (None, p17):
+        assert L.nq_compress_kv_layers(p16, p16, table, sh, pr, ok_kept_first := (nq.LayerBits * 2)(
+            nq.LayerBits(0, 0), nq.LayerBits(2, 2)), p16, 1 << 30, None) == nq.NQ_ERR_ARG
+        assert L.nq_decompress_kv_layers(p16, 1 << 30, table, sh, pr, ok_kept_first, p16, p16, None) == nq.NQ_ERR_ARG
+        assert L.nq_roundtrip_kv_layers(p16, p16, table, sh, pr, ok_kept_first, p16, p16, None) == nq.NQ_ERR_ARG
 
 
 def test_plan_joint_format_has_no_coset_words(nq):
@@ -309,6 +317,7 @@ def test_binding_passes_valid_calls_through_to_the_library(monkeypatch):
 
     monkeypatch.setattr(_lib, "lib", lambda: _Recorder())
     monkeypatch.setattr(codec, "_stream_handle", lambda device: None)
+    monkeypatch.setattr(codec, "_on", lambda device: contextlib.nullcontext())
     p = CodecParams(2, 2, 64, 0, 0, 0.0)
     shp = (2, 1, 8, 64, 128)
     K, V = _FakeCuda(shp, torch.float16), _FakeCuda(shp, torch.float16)
@@ -333,3 +342,24 @@ def test_binding_passes_valid_calls_through_to_the_library(monkeypatch):
     assert calls == ["nq_compress_kv", "nq_decompress_kv", "nq_roundtrip_kv", "nq_compress_kv", "nq_decompress_kv",
                      "nq_roundtrip_kv", "nq_compress_kv_layers", "nq_decompress_kv_layers", "nq_roundtrip_kv_layers",
                      "nq_code_histogram"]
+
+
+def test_binding_rejects_a_rope_table_on_another_device():
+    """The RoPE table must live on the call's device (a table on another GPU
+    would be read across devices by the kernels)."""
+    import torch
+
+    import e8_lattice_vector_gb300 as nq
+    from e8_lattice_vector_gb300 import CodecParams
+
+    p = CodecParams(2, 2, 64, 0, 0, 1e4)
+    shp = (2, 1, 8, 64, 128)
+    K = _FakeCuda(shp, torch.float16, "cuda:1")
+    table = nq.RopeTable(None, _FakeCuda((32, 64, 4), torch.float32, "cuda:0"), 64, 128, 1e4)
+    buf = _FakeCuda((1 << 24,), torch.uint8, "cuda:1")
+    for fn in (lambda: nq.compress_kv(K, K, p, table, out=buf),
+               lambda: nq.decompress_kv(buf, shp, p, table, K_out=K, V_out=K),
+               lambda: nq.roundtrip_kv(K, K, p, table, K_out=K, V_out=K),
+               lambda: nq.roundtrip_kv_layers(K, K, p, [(2, 2), (0, 0)], table, K_out=K, V_out=K)):
+        with pytest.raises(ValueError, match="RopeTable is on cuda:0; the call runs on cuda:1"):
+            fn()
