@@ -180,17 +180,48 @@ def whole_job_gbs(world, bytes_per_rank, ms):
 # ----------------------------------------------------------------- our arm
 
 
-def run_ours(a):
+def _free_port():
+    import socket
+
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def launch_ranks(gpus, argv, script=None):
+    """Start `gpus` ranks of `script` (this file by default) under
+    torch.distributed.run on this node, one process per GPU, rendezvous on
+    127.0.0.1; returns the launcher's exit status.  Used when --gpus N > 1 is
+    given without a torchrun environment."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", str(gpus),
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()),
+           script or os.path.abspath(__file__)] + list(argv)
+    return subprocess.call(cmd)
+
+
+def init_ranks():
+    """(world, rank, local rank) from the torchrun environment; joins the
+    process group when there is more than one rank (NCCL on GPUs, gloo
+    otherwise).  Every rank then works on its own replica of the cache: the
+    slices are independent, so nothing is exchanged on the data path."""
     import torch
     import torch.distributed as dist
-
-    from e8_lattice_vector_gb300 import build as nqbuild
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def run_ours(a):
+    import torch
+    import torch.distributed as dist
+
+    from e8_lattice_vector_gb300 import build as nqbuild
+
+    world, rank, local = init_ranks()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
@@ -204,6 +235,7 @@ def run_ours(a):
     rope = nq.RopeTable.build(cfg.tokens, cfg.head_dim, params.rope_theta, device=dev)
     lay = nq.plan(cfg.shape, params)
     buf = torch.empty(int(lay.total_bytes), dtype=torch.uint8, device=dev)
+    ws = nq.workspace(int(lay.workspace_bytes), dev)  # a temporal delta's decompression scratch
     K2 = torch.empty_like(K)
     V2 = torch.empty_like(V)
     stream = torch.cuda.current_stream(dev)
@@ -214,7 +246,7 @@ def run_ours(a):
         nq.compress_kv(K, V, params, rope, out=buf)
         if ev:
             ev[1].record(stream)
-        nq.decompress_kv(buf, cfg.shape, params, rope, K_out=K2, V_out=V2)
+        nq.decompress_kv(buf, cfg.shape, params, rope, K_out=K2, V_out=V2, ws=ws)
         if ev:
             ev[2].record(stream)
 
@@ -276,6 +308,7 @@ def run_ours(a):
         lshape = (1,) + tuple(cfg.shape[1:])
         llay = nq.plan(lshape, params)
         lbufs = [torch.empty(int(llay.total_bytes), dtype=torch.uint8, device=dev) for _ in range(nl)]
+        lws = nq.workspace(int(llay.workspace_bytes), dev)
         s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
         ev_in = [torch.cuda.Event() for _ in range(nl)]
         ev_cmp = [torch.cuda.Event() for _ in range(nl)]
@@ -289,7 +322,7 @@ def run_ours(a):
                 with torch.cuda.stream(s_cmp):
                     s_cmp.wait_event(ev_in[l])
                     nq.compress_kv(K[l:l + 1], V[l:l + 1], params, rope, out=lbufs[l])
-                    nq.decompress_kv(lbufs[l], lshape, params, rope, K_out=K2[l:l + 1], V_out=V2[l:l + 1])
+                    nq.decompress_kv(lbufs[l], lshape, params, rope, K_out=K2[l:l + 1], V_out=V2[l:l + 1], ws=lws)
                     ev_cmp[l].record(s_cmp)
                 with torch.cuda.stream(s_out):
                     s_out.wait_event(ev_cmp[l])
@@ -383,7 +416,7 @@ def run_ours(a):
         "gpu_launches": 4 * a.steps,
     }
     kv0 = (K[0, 0].cpu(), V[0, 0].cpu()) if rank == 0 and not a.no_cpu_baseline else None
-    del K, V, K2, V2, buf
+    del K, V, K2, V2, buf, ws
     torch.cuda.empty_cache()
     if kv0 is not None:
         out["cpu_baseline"] = cpu_baseline(cfg, params, a.cpu_seconds, kv0)
@@ -569,6 +602,8 @@ def run_reference(a):
 
 def main():
     a = _args()
+    if a.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(launch_ranks(a.gpus, sys.argv[1:]))
     if a.impl == "reference":
         run_reference(a)
     else:

@@ -34,7 +34,7 @@ class Layout(ctypes.Structure):
                 ("scales_per_row", ctypes.c_uint64),
                 ("k_idx", ctypes.c_uint64), ("k_coset", ctypes.c_uint64), ("k_scale", ctypes.c_uint64),
                 ("v_idx", ctypes.c_uint64), ("v_coset", ctypes.c_uint64), ("v_scale", ctypes.c_uint64),
-                ("total_bytes", ctypes.c_uint64)]
+                ("total_bytes", ctypes.c_uint64), ("workspace_bytes", ctypes.c_uint64)]
 
 
 # name -> (restype, argtypes); the exported C ABI, in header order
@@ -54,17 +54,18 @@ SIGNATURES = {
                                       ctypes.c_size_t, ctypes.c_void_p]),
     "nq_decompress_kv": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
                                         ctypes.POINTER(Shape), ctypes.POINTER(Params), ctypes.c_void_p,
-                                        ctypes.c_void_p, ctypes.c_void_p]),
+                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "nq_get_status": (ctypes.c_int, [ctypes.c_void_p]),
     "nq_roundtrip_kv": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                        ctypes.POINTER(Shape), ctypes.POINTER(Params), ctypes.c_void_p,
                                        ctypes.c_void_p, ctypes.c_void_p]),
-    "nq_plan_layers": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Params), _LB, _U64P, _U64P]),
+    "nq_plan_layers": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Params), _LB, _U64P, _U64P, _U64P]),
     "nq_compress_kv_layers": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                              ctypes.POINTER(Shape), ctypes.POINTER(Params), _LB, ctypes.c_void_p,
                                              ctypes.c_size_t, ctypes.c_void_p]),
     "nq_decompress_kv_layers": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
                                                ctypes.POINTER(Shape), ctypes.POINTER(Params), _LB, ctypes.c_void_p,
-                                               ctypes.c_void_p, ctypes.c_void_p]),
+                                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "nq_roundtrip_kv_layers": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                               ctypes.POINTER(Shape), ctypes.POINTER(Params), _LB, ctypes.c_void_p,
                                               ctypes.c_void_p, ctypes.c_void_p]),

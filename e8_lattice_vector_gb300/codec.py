@@ -17,7 +17,7 @@ import torch
 from . import _lib
 
 __all__ = ["CodecParams", "RopeTable", "plan", "shape_of", "compress_kv", "decompress_kv",
-           "e8_nearest", "sections"]
+           "e8_nearest", "sections", "workspace", "get_status"]
 
 
 @dataclass(frozen=True)
@@ -182,9 +182,32 @@ def compress_kv(K, V, params, rope=None, out=None):
     return out
 
 
-def decompress_kv(buf, shape, params, rope=None, K_out=None, V_out=None):
+def workspace(nbytes, device):
+    """A device workspace of `nbytes` bytes (None when nothing is needed): the
+    scratch that decompression with a temporal delta uses.  Reuse it across
+    calls on one stream."""
+    if nbytes <= 0:
+        return None
+    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
+def _ws_args(ws, need, device):
+    if need <= 0:
+        return None, 0
+    if ws is None:
+        raise ValueError("this call needs a workspace of %d bytes" % need)
+    _check_buf(ws, "workspace")
+    if ws.device != device:
+        raise ValueError("workspace is on %s; the call runs on %s" % (ws.device, device))
+    if ws.numel() < need:
+        raise ValueError("workspace has %d bytes; the call needs %d" % (ws.numel(), need))
+    return ctypes_void(ws.data_ptr()), int(ws.numel())
+
+
+def decompress_kv(buf, shape, params, rope=None, K_out=None, V_out=None, ws=None):
     """Decompress a buffer produced by compress_kv; returns (K, V) fp16 tensors
-    of `shape` ([L,B,H,T,D])."""
+    of `shape` ([L,B,H,T,D]).  ws: the workspace (see workspace()) that a
+    temporal delta needs, allocated here when not given."""
     shape = _norm_shape(shape)
     _check_buf(buf)
     if K_out is None:
@@ -194,10 +217,22 @@ def decompress_kv(buf, shape, params, rope=None, K_out=None, V_out=None):
     _check_like(K_out, shape, buf.device, "K_out")
     _check_like(V_out, shape, buf.device, "V_out")
     rp = _rope_ptr(rope, params, shape[3], shape[4], buf.device)
+    need = int(plan(shape, params).workspace_bytes)
+    if ws is None and need > 0:
+        ws = workspace(need, buf.device)
+    wp, wn = _ws_args(ws, need, buf.device)
     _call(buf.device, "nq_decompress_kv", ctypes_void(buf.data_ptr()), int(buf.numel()), rp,
           ctypes_ref(_cshape(shape)), ctypes_ref(params.c()), ctypes_void(K_out.data_ptr()),
-          ctypes_void(V_out.data_ptr()), _stream_handle(buf.device))
+          ctypes_void(V_out.data_ptr()), wp, wn, _stream_handle(buf.device))
     return K_out, V_out
+
+
+def get_status(device=None):
+    """The deferred status of the work enqueued on the device's current
+    stream (waits for it): raises NQError when the stream or an earlier launch
+    failed."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    _call(dev, "nq_get_status", _stream_handle(dev))
 
 
 def roundtrip_kv(K, V, params, rope=None, K_out=None, V_out=None):
@@ -235,16 +270,22 @@ def layer_profile(layers, key_bits=3, value_bits=2, protect_boundary=0):
     return [(0, 0) if l in keep else (key_bits, value_bits) for l in range(layers)]
 
 
-def plan_layers(shape, params, layer_bits):
-    """(offsets per layer, total bytes) of the per-layer buffer."""
+def _plan_layers3(shape, params, layer_bits):
     shape = _norm_shape(shape)
     table = _layer_table(layer_bits, shape[0])
     offs = (ctypes.c_uint64 * max(shape[0], 1))()
     total = ctypes.c_uint64(0)
+    ws = ctypes.c_uint64(0)
     st = _lib.lib().nq_plan_layers(ctypes_ref(_cshape(shape)), ctypes_ref(params.c()), table, offs,
-                                   ctypes.byref(total))
+                                   ctypes.byref(total), ctypes.byref(ws))
     _lib.check("nq_plan_layers", st)
-    return [int(offs[i]) for i in range(shape[0])], int(total.value)
+    return [int(offs[i]) for i in range(shape[0])], int(total.value), int(ws.value)
+
+
+def plan_layers(shape, params, layer_bits):
+    """(offsets per layer, total bytes) of the per-layer buffer."""
+    offs, total, _ = _plan_layers3(shape, params, layer_bits)
+    return offs, total
 
 
 def compress_kv_layers(K, V, params, layer_bits, rope=None, out=None):
@@ -264,7 +305,7 @@ def compress_kv_layers(K, V, params, layer_bits, rope=None, out=None):
     return out
 
 
-def decompress_kv_layers(buf, shape, params, layer_bits, rope=None, K_out=None, V_out=None):
+def decompress_kv_layers(buf, shape, params, layer_bits, rope=None, K_out=None, V_out=None, ws=None):
     shape = _norm_shape(shape)
     _check_buf(buf)
     if K_out is None:
@@ -274,9 +315,13 @@ def decompress_kv_layers(buf, shape, params, layer_bits, rope=None, K_out=None, 
     _check_like(K_out, shape, buf.device, "K_out")
     _check_like(V_out, shape, buf.device, "V_out")
     rp = _rope_ptr(rope, params, shape[3], shape[4], buf.device)
+    _, _, need = _plan_layers3(shape, params, layer_bits)
+    if ws is None and need > 0:
+        ws = workspace(need, buf.device)
+    wp, wn = _ws_args(ws, need, buf.device)
     _call(buf.device, "nq_decompress_kv_layers", ctypes_void(buf.data_ptr()), int(buf.numel()), rp,
           ctypes_ref(_cshape(shape)), ctypes_ref(params.c()), _layer_table(layer_bits, shape[0]),
-          ctypes_void(K_out.data_ptr()), ctypes_void(V_out.data_ptr()), _stream_handle(buf.device))
+          ctypes_void(K_out.data_ptr()), ctypes_void(V_out.data_ptr()), wp, wn, _stream_handle(buf.device))
     return K_out, V_out
 
 

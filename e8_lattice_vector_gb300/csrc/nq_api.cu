@@ -72,6 +72,8 @@ void make_layout(const nq_shape* s, const nq_params* p, nq_layout* L) {
     L->v_scale = off;
     off = align256(off + rows * L->scales_per_row * 2);
     L->total_bytes = off;
+    L->workspace_bytes = chain_plan(int64_t(slices), s->tokens, s->head_dim, std::max(p->key_bits, p->value_bits),
+                                    p->delta_chunk).total;
 }
 
 }  // namespace
@@ -313,7 +315,7 @@ int nq_code_histogram(const void* in, size_t in_bytes, const nq_shape* shape, co
 
 int nq_decompress_kv(const void* in, size_t in_bytes, const float* rope_table,
                      const nq_shape* shape, const nq_params* params, void* k_f16_out,
-                     void* v_f16_out, void* stream) {
+                     void* v_f16_out, void* workspace, size_t workspace_bytes, void* stream) {
     int st = nq::check(shape, params);
     if (st != NQ_OK) return st;
     nq_layout L;
@@ -324,8 +326,10 @@ int nq_decompress_kv(const void* in, size_t in_bytes, const float* rope_table,
     if (!nq::aligned16(in) || !nq::aligned16(k_f16_out) || !nq::aligned16(v_f16_out) ||
         (rope && !nq::aligned16(rope_table)))
         return NQ_ERR_ARG;
-    if (in_bytes < L.total_bytes) return NQ_ERR_SIZE;
+    if (L.workspace_bytes > 0 && (!workspace || !nq::aligned16(workspace))) return NQ_ERR_ARG;
+    if (in_bytes < L.total_bytes || workspace_bytes < L.workspace_bytes) return NQ_ERR_SIZE;
     nq::LaunchArgs a;
+    a.workspace = static_cast<uint8_t*>(workspace);
     a.slices = int64_t(shape->layers) * shape->batch * shape->kv_heads;
     a.tokens = shape->tokens;
     a.tpad = int(L.tokens_padded);
@@ -333,15 +337,21 @@ int nq_decompress_kv(const void* in, size_t in_bytes, const float* rope_table,
     a.delta_chunk = params->delta_chunk;
     a.stream = static_cast<cudaStream_t>(stream);
     const uint8_t* base = static_cast<const uint8_t*>(in);
-    st = nq::launch_decompress_tensor(a, shape->head_dim, params->key_bits, base + L.k_idx,
+    const int max_bits = std::max(params->key_bits, params->value_bits);
+    st = nq::launch_decompress_tensor(a, shape->head_dim, params->key_bits, max_bits, base + L.k_idx,
                                       nq::coset_section(base, L.k_coset, params),
                                       reinterpret_cast<const uint16_t*>(base + L.k_scale),
                                       rope ? rope_table : nullptr, k_f16_out);
     if (st != NQ_OK) return st;
-    return nq::launch_decompress_tensor(a, shape->head_dim, params->value_bits, base + L.v_idx,
+    return nq::launch_decompress_tensor(a, shape->head_dim, params->value_bits, max_bits, base + L.v_idx,
                                         nq::coset_section(base, L.v_coset, params),
                                         reinterpret_cast<const uint16_t*>(base + L.v_scale), nullptr,
                                         v_f16_out);
+}
+
+int nq_get_status(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return NQ_ERR_CUDA;
+    return cudaPeekAtLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
 }
 
 int nq_e8_nearest(const float* u, float* out, int64_t n_blocks, int strict, int bits, void* stream) {

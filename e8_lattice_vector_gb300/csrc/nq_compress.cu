@@ -48,12 +48,14 @@ __device__ __forceinline__ void store_words(uint8_t* dst, const unsigned* w) {
 
 // The per-row work after the RoPE removal, shared by both two-thread
 // kernels: the block codes (rotation, group scale, E8 search), the temporal
-// delta, and the store of record row rrow.  y: the thread's
-// coordinates in PairMap slots.  t: token index of the row; first: the tile
-// starts a delta chunk at t_begin.
+// delta, and the store of record row rrow.  y: the thread's coordinates in
+// PairMap slots.  chain_start: row 0 of the tile begins a delta chain (it is
+// stored raw); otherwise row 0's predecessor is the previous tile's last row,
+// whose raw codes are in carry.  store: false for a halo tile (codes and
+// carry only).
 template <int D, int BITS, int MODE>
-__device__ __forceinline__ void pair_encode_row(float (&y)[D / 2], int hf, int r, float sgn, int t, bool active,
-                                                bool delta, bool first, int t_begin, int64_t rrow, int group,
+__device__ __forceinline__ void pair_encode_row(float (&y)[D / 2], int hf, int r, float sgn, bool active,
+                                                bool delta, bool chain_start, bool store, int64_t rrow, int group,
                                                 unsigned (&carry)[D / 16], unsigned& carry_c,
                                                 uint8_t* __restrict__ idx, uint16_t* __restrict__ coset,
                                                 __half* __restrict__ scales) {
@@ -83,20 +85,22 @@ __device__ __forceinline__ void pair_encode_row(float (&y)[D / 2], int hf, int r
 
     // ---- temporal delta against the previous token (row r - 1: lane - 2)
     if (delta) {
+        const bool raw = r == 0 && chain_start;
 #pragma unroll
         for (int k = 0; k < NBT; ++k) {
             unsigned prev = __shfl_up_sync(kFull, blk[k], 2);
             const unsigned last = __shfl_sync(kFull, blk[k], 30 + hf);
-            if (r == 0) prev = first ? 0u : carry[k];
-            if (t != t_begin) blk[k] = swar_sub<BITS>(blk[k], prev);
+            if (r == 0) prev = carry[k];
+            if (!raw) blk[k] = swar_sub<BITS>(blk[k], prev);
             carry[k] = last;  // raw codes of the tile's last token
         }
         unsigned pc = __shfl_up_sync(kFull, cw, 2);
         const unsigned lastc = __shfl_sync(kFull, cw, 30);
-        if (r == 0) pc = first ? 0u : carry_c;
-        if (t != t_begin) cw ^= pc;
+        if (r == 0) pc = carry_c;
+        if (!raw) cw ^= pc;
         carry_c = lastc;
     }
+    if (!store) return;  // a halo tile: only the carry was wanted
 
     // ---- store (padding rows past the slice get zeros)
     if (!active) {
@@ -120,14 +124,15 @@ __device__ __forceinline__ void pair_encode_row(float (&y)[D / 2], int hf, int r
 template <int D, int BITS, int MODE>
 __global__ void __launch_bounds__(kThreads, 2)
     compress_pair_kernel(const __half* __restrict__ x, const float4* __restrict__ rope, int64_t slices,
-                         int tokens, int tpad, int group, int chunk, bool delta, uint8_t* __restrict__ idx,
+                         int tokens, int tpad, int group, int seg, int dchunk, uint8_t* __restrict__ idx,
                          uint16_t* __restrict__ coset, __half* __restrict__ scales) {
     constexpr int DP = PaddedDim<D>::value;  // head_dim 96 runs zero-padded to 128
     using PM = PairMap<DP>;
     constexpr int HALF = PM::HALF;
     constexpr int Q = PM::Q;
     constexpr int NBT = PM::NBT;
-    using Walk = TileWalkT<kPairRows>;
+    using Walk = SegWalk<kPairRows>;
+    const bool delta = dchunk > 0;
 
     extern __shared__ __align__(1024) uint8_t smem[];
     const int lane = threadIdx.x & 31;
@@ -138,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
 
-    Walk cur(warp, nwarps, slices, tpad, chunk);
+    Walk cur(warp, nwarps, slices, tpad, seg, dchunk);
     Walk pre = cur;
 #pragma unroll
     for (int s = 0; s < kPairStages - 1; ++s) {
@@ -196,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         __syncwarp();  // every lane has read its coordinates: the stage may be refilled
 
-        pair_encode_row<DP, BITS, MODE>(y, hf, r, sgn, t, active, delta, cur.t0 == cur.t_begin(), cur.t_begin(),
+        pair_encode_row<DP, BITS, MODE>(y, hf, r, sgn, active, delta, cur.chain_start(), !cur.halo(),
                                          cur.slice * tpad + t, group, carry, carry_c, idx, coset, scales);
         cur.next();
     }
@@ -212,7 +217,7 @@ constexpr int kCompressRopeStages = 2;
 template <int D, int BITS, int MODE>
 __global__ void __launch_bounds__(kCompressRopeThreads, 2)
     compress_pair_rope_kernel(const __half* __restrict__ x, const float4* __restrict__ rope, int64_t slices,
-                              int tokens, int tpad, int group, int chunk, bool delta, uint8_t* __restrict__ idx,
+                              int tokens, int tpad, int group, int seg, int dchunk, uint8_t* __restrict__ idx,
                               uint16_t* __restrict__ coset, __half* __restrict__ scales) {
     constexpr int DP = D;
     using PM = PairMap<DP>;
@@ -220,7 +225,8 @@ __global__ void __launch_bounds__(kCompressRopeThreads, 2)
     constexpr int Q = PM::Q;
     constexpr int NBT = PM::NBT;
     using RS = RopeRing<D, kCompressRopeWarps, kCompressRopeStages>;
-    using Walk = TileWalkT<kPairRows>;
+    using Walk = SegWalk<kPairRows>;
+    const bool delta = dchunk > 0;
 
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = (smem_u32(smem) + 1023u) & ~1023u;
@@ -232,7 +238,7 @@ __global__ void __launch_bounds__(kCompressRopeThreads, 2)
     const int64_t ngroups = (slices + kCompressRopeWarps - 1) / kCompressRopeWarps;
 
     // the walk runs over slice groups; the warp's slice is 16 * group + wib
-    Walk cur(blockIdx.x, gridDim.x, ngroups, tpad, chunk);
+    Walk cur(blockIdx.x, gridDim.x, ngroups, tpad, seg, dchunk);
     Walk pre = cur;
 
     auto load_stage = [&](const Walk& w, uint32_t stage) {
@@ -288,7 +294,7 @@ __global__ void __launch_bounds__(kCompressRopeThreads, 2)
             // RoPE removal with the block's table tile: pairs (i, i + D/2) are slots (l, l + Q)
 #pragma unroll
             for (int qq = 0; qq < Q / 2; ++qq) pair_rope_remove<D>(y, qq, rope_tile_entry<D>(stage, hf * (Q / 2) + qq, r));
-            pair_encode_row<D, BITS, MODE>(y, hf, r, sgn, t, active, delta, cur.t0 == cur.t_begin(), cur.t_begin(),
+            pair_encode_row<D, BITS, MODE>(y, hf, r, sgn, active, delta, cur.chain_start(), !cur.halo(),
                                              slice * tpad + t, group, carry, carry_c, idx, coset, scales);
         }
         cur.next();
@@ -296,20 +302,37 @@ __global__ void __launch_bounds__(kCompressRopeThreads, 2)
     cp_async_wait<0>();
 }
 
+// Segment length of the compression work items.  Without a delta every tile
+// is an item.  With a delta, chains restart every delta_chunk tokens; a chunk
+// of at most kMaxSeg tokens is one item, and a longer chain (the method's own
+// single chain per slice when delta_chunk >= tokens) is cut into segments of
+// at most kMaxSeg tokens, each preceded by one halo tile, halved down to
+// kMinSeg while there are fewer than 4 items per resident warp.
+constexpr int kMaxSeg = 1024;
+constexpr int kMinSeg = 256;
+
+static int compress_segment(const LaunchArgs& a, int64_t units, int64_t resident_warps) {
+    if (a.delta_chunk <= 0) return kPairRows;
+    if (a.delta_chunk <= kMaxSeg) return a.delta_chunk;
+    int seg = kMaxSeg;
+    while (seg > kMinSeg && units * ((a.tpad + seg - 1) / seg) < 4 * resident_warps) seg /= 2;
+    return seg;
+}
+
 template <int D, int BITS, int MODE>
 static int launch_pair(const LaunchArgs& a, const __half* x, const float4* rope, uint8_t* idx,
                        uint16_t* coset, __half* scales) {
     auto kern = compress_pair_kernel<D, BITS, MODE>;
     if (!ensure_smem(reinterpret_cast<const void*>(kern), kPairCompressSmem)) return NQ_ERR_CUDA;
-    const int chunk = a.delta_chunk > 0 ? a.delta_chunk : kPairRows;
-    const int64_t items = a.slices * ((a.tpad + chunk - 1) / chunk);
-    const int64_t want = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    if (want == 0) return NQ_OK;
     const int cap = grid_capacity(reinterpret_cast<const void*>(kern), kPairCompressSmem);
     if (cap <= 0) return NQ_ERR_CUDA;
+    const int seg = compress_segment(a, a.slices, int64_t(cap) * kWarpsPerBlock);
+    const int64_t items = a.slices * ((a.tpad + seg - 1) / seg);
+    const int64_t want = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    if (want == 0) return NQ_OK;
     const int grid = int(std::min<int64_t>(want, cap));
-    kern<<<grid, kThreads, kPairCompressSmem, a.stream>>>(x, rope, a.slices, a.tokens, a.tpad, a.group, chunk,
-                                                          a.delta_chunk > 0, idx, coset, scales);
+    kern<<<grid, kThreads, kPairCompressSmem, a.stream>>>(x, rope, a.slices, a.tokens, a.tpad, a.group, seg,
+                                                          a.delta_chunk, idx, coset, scales);
     return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
 }
 
@@ -319,15 +342,15 @@ static int launch_pair_rope(const LaunchArgs& a, const __half* x, const float4* 
     auto kern = compress_pair_rope_kernel<D, BITS, MODE>;
     constexpr int smem = RopeRing<D, kCompressRopeWarps, kCompressRopeStages>::SMEM;
     if (!ensure_smem(reinterpret_cast<const void*>(kern), smem)) return NQ_ERR_CUDA;
-    const int chunk = a.delta_chunk > 0 ? a.delta_chunk : kPairRows;
-    const int64_t groups = (a.slices + kCompressRopeWarps - 1) / kCompressRopeWarps;
-    const int64_t items = groups * ((a.tpad + chunk - 1) / chunk);
-    if (items == 0) return NQ_OK;
     const int cap = grid_capacity_threads(reinterpret_cast<const void*>(kern), smem, kCompressRopeThreads);
     if (cap <= 0) return NQ_ERR_CUDA;
+    const int64_t groups = (a.slices + kCompressRopeWarps - 1) / kCompressRopeWarps;
+    const int seg = compress_segment(a, groups, cap);  // items are block-wide
+    const int64_t items = groups * ((a.tpad + seg - 1) / seg);
+    if (items == 0) return NQ_OK;
     const int grid = int(std::min<int64_t>(items, cap));
-    kern<<<grid, kCompressRopeThreads, smem, a.stream>>>(x, rope, a.slices, a.tokens, a.tpad, a.group, chunk,
-                                                 a.delta_chunk > 0, idx, coset, scales);
+    kern<<<grid, kCompressRopeThreads, smem, a.stream>>>(x, rope, a.slices, a.tokens, a.tpad, a.group, seg,
+                                                 a.delta_chunk, idx, coset, scales);
     return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
 }
 

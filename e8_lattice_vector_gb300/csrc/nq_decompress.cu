@@ -7,13 +7,18 @@
 // tile's records (idx rows, coset words, scales) are contiguous and 16-byte
 // aligned thanks to the per-slice padding of the record rows, so they stream
 // through a 3-stage shared-memory ring by cp.async; keys run in blocks of
-// warps that also stage the tile's RoPE table rows once for the block.  The
-// delta is undone in place on the record tile, column-wise (field-wise
-// addition modulo 2^b), plus the running total of the chunk's earlier tiles;
-// the coset words by an exclusive-or warp scan.  The reconstructed fp16 rows
+// warps that also stage the tile's RoPE table rows once for the block.
+// Without a temporal delta every tile is a work item; with one, a run of up
+// to 32 consecutive tiles of a chain is, walked in order.  The delta is undone
+// in place on the record tile, column-wise (field-wise addition modulo 2^b),
+// plus the running sum of the chain's earlier rows, carried in registers from
+// tile to tile; a run that does not start its chain takes its starting sum
+// from the workspace, where two light passes over the idx section leave it
+// (nq_chain.cuh).  Coset words by an exclusive-or warp scan.  The reconstructed fp16 rows
 // are written into a swizzled shared-memory tile and leave by one TMA tensor
 // store per 64 columns, which clips the rows past the end of the slice and the
 // columns past head_dim.  head_dim 64 uses two threads per row (16-row tiles).
+#include "nq_chain.cuh"
 #include "nq_decode.cuh"
 
 namespace nq {
@@ -52,40 +57,6 @@ __device__ __forceinline__ void load_records(const uint8_t* __restrict__ idx, co
 // (a shuffle scan over the segments) and the carry of the chunk's earlier
 // tiles, and writes the codes back.  Far fewer shuffles and additions than a
 // 32-lane scan of every block of every row.
-template <int BITS>
-struct DeltaUnit;
-template <>
-struct DeltaUnit<2> {  // one word, 16 fields
-    static constexpr int U = 1, NV = 1;
-    __device__ static void load(uint32_t a, unsigned (&v)[NV]) { v[0] = lds32(a); }
-    __device__ static void store(uint32_t a, const unsigned (&v)[NV]) { sts32(a, v[0]); }
-    __device__ static unsigned add(unsigned a, unsigned b) { return swar_add_word2(a, b); }
-};
-template <>
-struct DeltaUnit<4> {  // one word = one block of 8 fields
-    static constexpr int U = 1, NV = 1;
-    __device__ static void load(uint32_t a, unsigned (&v)[NV]) { v[0] = lds32(a); }
-    __device__ static void store(uint32_t a, const unsigned (&v)[NV]) { sts32(a, v[0]); }
-    __device__ static unsigned add(unsigned a, unsigned b) { return swar_add<4>(a, b); }
-};
-template <>
-struct DeltaUnit<3> {  // three words = four 24-bit blocks (fields straddle the words)
-    static constexpr int U = 3, NV = 4;
-    __device__ static void load(uint32_t a, unsigned (&v)[NV]) {
-        const unsigned w0 = lds32(a), w1 = lds32(a + 4), w2 = lds32(a + 8);
-        v[0] = w0 & 0xffffffu;
-        v[1] = (w0 >> 24) | ((w1 & 0xffffu) << 8);
-        v[2] = (w1 >> 16) | ((w2 & 0xffu) << 16);
-        v[3] = w2 >> 8;
-    }
-    __device__ static void store(uint32_t a, const unsigned (&v)[NV]) {
-        sts32(a, v[0] | (v[1] << 24));
-        sts32(a + 4, (v[1] >> 8) | (v[2] << 16));
-        sts32(a + 8, (v[2] >> 16) | (v[3] << 8));
-    }
-    __device__ static unsigned add(unsigned a, unsigned b) { return swar_add<3>(a, b); }
-};
-
 // rows: shared address of row 0 of the tile's ROWS idx rows (RB bytes each);
 // carry: the lane's unit in the previous tile's last row (unused when first).
 template <int BITS, int RB, int ROWS = 32>
@@ -214,10 +185,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     decompress_kernel(const uint8_t* __restrict__ idx, const uint16_t* __restrict__ coset,
                       const __half* __restrict__ scales, const float4* __restrict__ rope,
                       const __grid_constant__ CUtensorMap out_map, int64_t slices, int tokens, int tpad,
-                      int group, int chunk, bool delta) {
+                      int group, const ChainState cs) {
     constexpr int DP = PaddedDim<D>::value;
     constexpr int NB = DP / 8;
     constexpr int RB = DP * BITS / 8;
+    constexpr int NU = RB / (4 * DeltaUnit<BITS>::U);  // column units of the tile scan
 
     extern __shared__ __align__(1024) uint8_t smem[];
     const int lane = threadIdx.x & 31;
@@ -229,49 +201,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int gshift = group == 32 ? 5 : (group == 64 ? 6 : 7);
     const int nsc = DP >> gshift;
 
-    TileWalk cur(warp, nwarps, slices, tokens, chunk);
-    TileWalk pre = cur;
-#pragma unroll
-    for (int s = 0; s < kStages - 1; ++s) {
-        if (pre.valid()) {
-            load_records<RB>(idx, coset, scales, nsc, pre.slice * tpad + pre.t0, ring + s * kRecStage, lane);
-            pre.next();
-        }
-        cp_async_commit();
-    }
-
     unsigned carry[NB];
     unsigned carry_c = 0;
 #pragma unroll
     for (int k = 0; k < NB; ++k) carry[k] = 0;
 
-    for (int i = 0; cur.valid(); ++i) {
-        if (pre.valid()) {
-            load_records<RB>(idx, coset, scales, nsc, pre.slice * tpad + pre.t0,
-                             ring + ((i + kStages - 1) % kStages) * kRecStage, lane);
-            pre.next();
-        }
-        cp_async_commit();
-        cp_async_wait<kStages - 1>();
-        __syncwarp();
-        const uint32_t stage = ring + (i % kStages) * kRecStage;
-        const int t = cur.t0 + lane;
-
-        const uint8_t* stage_gen = smem + (stage - smem_u32(smem));
-        float y[DP];
-        decode_row<D, BITS, JOINT>(stage, stage_gen, lane, nsc, gshift, delta, cur.t0 == cur.t_begin(), carry, carry_c,
-                                   y);
-
-        // ---- RoPE re-apply on keys: rotate each (i, i + D/2) pair by +angle
-        if (rope != nullptr) {
-            const float4* cs = rope + (t < cur.t_end() ? t : cur.t_begin());  // [D/4][tokens]
+    // single tiles without a delta, groups of a chain's tiles with one
+    auto run = [&](auto cur) {
+        auto pre = cur;
 #pragma unroll
-            for (int q = 0; q < D / 4; ++q) rope_apply_pairs<D>(y, q, __ldg(cs + int64_t(q) * tokens));
+        for (int s = 0; s < kStages - 1; ++s) {
+            if (pre.valid()) {
+                load_records<RB>(idx, coset, scales, nsc, pre.slice * tpad + pre.t0, ring + s * kRecStage, lane);
+                pre.next();
+            }
+            cp_async_commit();
         }
-
-        store_rows<D, 1>(y, outbuf + (i & 1) * kTileBytes, lane, &out_map, cur.t0, int(cur.slice));
-        cur.next();
-    }
+        for (int i = 0; cur.valid(); ++i) {
+            if (pre.valid()) {
+                load_records<RB>(idx, coset, scales, nsc, pre.slice * tpad + pre.t0,
+                                 ring + ((i + kStages - 1) % kStages) * kRecStage, lane);
+                pre.next();
+            }
+            cp_async_commit();
+            cp_async_wait<kStages - 1>();
+            __syncwarp();
+            const uint32_t stage = ring + (i % kStages) * kRecStage;
+            const int t = cur.t0 + lane;
+            bool first = false;  // row 0 starts its chain: no carry
+            if constexpr (decltype(cur)::kGroups) {
+                if (cur.group_start()) {
+                    if (cs.gexcl != nullptr)
+                        load_group_carry<BITS, RB>(cs, cur.G, lane % NU, carry, carry_c, !JOINT);
+                    else
+                        first = true;
+                }
+            }
+            const uint8_t* stage_gen = smem + (stage - smem_u32(smem));
+            float y[DP];
+            decode_row<D, BITS, JOINT>(stage, stage_gen, lane, nsc, gshift, cs.delta, first, carry, carry_c, y);
+            // ---- RoPE re-apply on keys: rotate each (i, i + D/2) pair by +angle
+            if (rope != nullptr) {
+                const float4* tab = rope + (t < tokens ? t : cur.t0);  // [D/4][tokens]
+#pragma unroll
+                for (int q = 0; q < D / 4; ++q) rope_apply_pairs<D>(y, q, __ldg(tab + int64_t(q) * tokens));
+            }
+            store_rows<D, 1>(y, outbuf + (i & 1) * kTileBytes, lane, &out_map, cur.t0, int(cur.slice));
+            cur.next();
+        }
+    };
+    if (!cs.delta)
+        run(TileWalk(warp, nwarps, slices, tokens, kTileRows));
+    else
+        run(GroupWalk<kTileRows>(warp, nwarps, slices, cs.geo));
     cp_async_wait<0>();
     if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
@@ -301,10 +283,11 @@ __global__ void __launch_bounds__(kKeyThreads, 1)
     decompress_key_kernel(const uint8_t* __restrict__ idx, const uint16_t* __restrict__ coset,
                           const __half* __restrict__ scales, const float4* __restrict__ rope,
                           const __grid_constant__ CUtensorMap out_map, int64_t slices, int tokens, int tpad,
-                          int group, int chunk, bool delta) {
+                          int group, const ChainState cs) {
     constexpr int DP = PaddedDim<D>::value;
     constexpr int NB = DP / 8;
     constexpr int RB = DP * BITS / 8;
+    constexpr int NU = RB / (4 * DeltaUnit<BITS>::U);
     using KS = KeyStage<D>;
 
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -318,62 +301,77 @@ __global__ void __launch_bounds__(kKeyThreads, 1)
     const int nsc = DP >> gshift;
     const int64_t ngroups = (slices + kKeyWarps - 1) / kKeyWarps;
 
-    TileWalk cur(blockIdx.x, gridDim.x, ngroups, tokens, chunk);
-    TileWalk pre = cur;
-
-    auto load_stage = [&](const TileWalk& w, uint32_t stage) {
+    // stage the table rows of tokens t0.. and the warp's record tile of slice group grp
+    auto load_stage = [&](int64_t grp, int t0, uint32_t stage) {
         // the table tile: thread t copies token row t % 32 of planes t / 32 + 4 j
         constexpr int QS = kKeyThreads / kTileRows;  // plane step
         static_assert((D / 4) % QS == 0, "table copies per thread");
-        const int tok = w.t0 + lane;
+        const int tok = t0 + lane;
         const bool ok = tok < tokens;
         const float4* src = rope + int64_t(wib) * tokens + (ok ? tok : 0);
 #pragma unroll
         for (int j = 0; j < (D / 4) / QS; ++j)
             cp_async16(stage + 16 * (threadIdx.x + kKeyThreads * j), src + int64_t(QS * j) * tokens, ok ? 16 : 0);
-        const int64_t sl = w.slice * kKeyWarps + wib;
-        if (sl < slices) load_records<RB>(idx, coset, scales, nsc, sl * tpad + w.t0, stage + KS::TABLE + wib * kRecStage, lane);
+        const int64_t sl = grp * kKeyWarps + wib;
+        if (sl < slices) load_records<RB>(idx, coset, scales, nsc, sl * tpad + t0, stage + KS::TABLE + wib * kRecStage, lane);
     };
-
-#pragma unroll
-    for (int st = 0; st < kKeyStages - 1; ++st) {
-        if (pre.valid()) {
-            load_stage(pre, stages + st * KS::BYTES);
-            pre.next();
-        }
-        cp_async_commit();
-    }
 
     unsigned carry[NB];
     unsigned carry_c = 0;
 #pragma unroll
     for (int k = 0; k < NB; ++k) carry[k] = 0;
 
-    for (int i = 0; cur.valid(); ++i) {
-        cp_async_wait<kKeyStages - 2>();  // this thread's copies of tile i are done
-        __syncthreads();                  // everyone's are; everyone is done with tile i - 1
-        if (pre.valid()) {
-            load_stage(pre, stages + ((i + kKeyStages - 1) % kKeyStages) * KS::BYTES);
-            pre.next();
-        }
-        cp_async_commit();
-        const uint32_t stage = stages + (i % kKeyStages) * KS::BYTES;
-        const int64_t slice = cur.slice * kKeyWarps + wib;
-        if (slice < slices) {  // warp-uniform
-            const uint32_t rec = stage + KS::TABLE + wib * kRecStage;
-            float y[DP];
-            decode_row<D, BITS, JOINT>(rec, gbase + (rec - base), lane, nsc, gshift, delta,
-                                       cur.t0 == cur.t_begin(), carry, carry_c, y);
+    // single tiles without a delta, groups of a chain's tiles with one (items over slice groups)
+    auto run = [&](auto cur) {
+        auto pre = cur;
 #pragma unroll
-            for (int q = 0; q < D / 4; ++q) {
-                const uint4 raw = lds128(stage + 16 * (q * kTileRows + lane));
-                rope_apply_pairs<D>(y, q, make_float4(__uint_as_float(raw.x), __uint_as_float(raw.y),
-                                                      __uint_as_float(raw.z), __uint_as_float(raw.w)));
+        for (int st = 0; st < kKeyStages - 1; ++st) {
+            if (pre.valid()) {
+                load_stage(pre.slice, pre.t0, stages + st * KS::BYTES);
+                pre.next();
             }
-            store_rows<D, 0>(y, outbuf, lane, &out_map, cur.t0, int(slice));
+            cp_async_commit();
         }
-        cur.next();
-    }
+        for (int i = 0; cur.valid(); ++i) {
+            cp_async_wait<kKeyStages - 2>();  // this thread's copies of tile i are done
+            __syncthreads();                  // everyone's are; everyone is done with tile i - 1
+            if (pre.valid()) {
+                load_stage(pre.slice, pre.t0, stages + ((i + kKeyStages - 1) % kKeyStages) * KS::BYTES);
+                pre.next();
+            }
+            cp_async_commit();
+            const uint32_t stage = stages + (i % kKeyStages) * KS::BYTES;
+            const int64_t slice = cur.slice * kKeyWarps + wib;
+            if (slice < slices) {  // warp-uniform
+                bool first = false;
+                if constexpr (decltype(cur)::kGroups) {
+                    if (cur.group_start()) {
+                        if (cs.gexcl != nullptr)
+                            load_group_carry<BITS, RB>(cs, cur.slice_group(uint64_t(slice)), lane % NU, carry, carry_c,
+                                                       !JOINT);
+                        else
+                            first = true;
+                    }
+                }
+                const uint32_t rec = stage + KS::TABLE + wib * kRecStage;
+                float y[DP];
+                decode_row<D, BITS, JOINT>(rec, gbase + (rec - base), lane, nsc, gshift, cs.delta, first, carry,
+                                           carry_c, y);
+#pragma unroll
+                for (int q = 0; q < D / 4; ++q) {
+                    const uint4 raw = lds128(stage + 16 * (q * kTileRows + lane));
+                    rope_apply_pairs<D>(y, q, make_float4(__uint_as_float(raw.x), __uint_as_float(raw.y),
+                                                          __uint_as_float(raw.z), __uint_as_float(raw.w)));
+                }
+                store_rows<D, 0>(y, outbuf, lane, &out_map, cur.t0, int(slice));
+            }
+            cur.next();
+        }
+    };
+    if (!cs.delta)
+        run(TileWalk(blockIdx.x, gridDim.x, ngroups, tokens, kTileRows));
+    else
+        run(GroupWalk<kTileRows>(blockIdx.x, gridDim.x, ngroups, cs.geo));
     cp_async_wait<0>();
     if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
@@ -436,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     decompress_pair_kernel(const uint8_t* __restrict__ idx, const uint16_t* __restrict__ coset,
                            const __half* __restrict__ scales, const float4* __restrict__ rope,
                            const __grid_constant__ CUtensorMap out_map, int64_t slices, int tokens, int tpad,
-                           int group, int chunk, bool delta) {
+                           int group, const ChainState cs) {
     constexpr int DP = D;
     using PM = PairMap<DP>;
     constexpr int HALF = PM::HALF;
@@ -446,7 +444,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     using RP = RowPack<BITS, NBT>;
     constexpr int RB = DP * BITS / 8;
     constexpr int RBT = RB / 2;
-    using Walk = TileWalkT<kPairRows>;
+    constexpr int NV = DeltaUnit<BITS>::NV;
+    constexpr int NU = RB / (4 * DeltaUnit<BITS>::U);
 
     extern __shared__ __align__(1024) uint8_t smem[];
     const int lane = threadIdx.x & 31;
@@ -463,185 +462,238 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int gsh = group == 32 ? 0 : (group == 64 ? 1 : 2);  // log2 of 32-subgroups per scale
     const int nsc = DP >> (5 + gsh);
 
-    Walk cur(warp, nwarps, slices, tokens, chunk);
-    Walk pre = cur;
-#pragma unroll
-    for (int s = 0; s < kStages - 1; ++s) {
-        if (pre.valid()) {
-            load_pair_records<RB>(idx, coset, scales, nsc, pre.slice * tpad + pre.t0, ring + s * kPairRecStage, lane);
-            pre.next();
-        }
-        cp_async_commit();
-    }
-
     unsigned carry[NBT];
     unsigned carry_c = 0;
 #pragma unroll
     for (int k = 0; k < NBT; ++k) carry[k] = 0;
 
-    for (int i = 0; cur.valid(); ++i) {
-        if (pre.valid()) {
-            load_pair_records<RB>(idx, coset, scales, nsc, pre.slice * tpad + pre.t0,
-                                  ring + ((i + kStages - 1) % kStages) * kPairRecStage, lane);
-            pre.next();
+    // single tiles without a delta, groups of a chain's tiles with one
+    auto run = [&](auto cur) {
+        auto pre = cur;
+#pragma unroll
+        for (int s = 0; s < kStages - 1; ++s) {
+            if (pre.valid()) {
+                load_pair_records<RB>(idx, coset, scales, nsc, pre.slice * tpad + pre.t0, ring + s * kPairRecStage, lane);
+                pre.next();
+            }
+            cp_async_commit();
         }
-        cp_async_commit();
-        cp_async_wait<kStages - 1>();
-        __syncwarp();
-        const uint32_t stage = ring + (i % kStages) * kPairRecStage;
-        const uint8_t* gstage = gbase + (stage - base);
-        const int t = cur.t0 + r;
-
-        // ---- undo the temporal delta of the idx tile in place (every lane takes part)
-        const bool first = cur.t0 == cur.t_begin();
-        if (delta) {
-            constexpr int NV = DeltaUnit<BITS>::NV;
-            unsigned cu[NV];
-#pragma unroll
-            for (int n = 0; n < NV; ++n) cu[n] = carry[n];
-            undelta_tile<BITS, RB, kPairRows>(stage + kPairRecIdx, lane, first, cu);
-#pragma unroll
-            for (int n = 0; n < NV; ++n) carry[n] = cu[n];
+        for (int i = 0; cur.valid(); ++i) {
+            if (pre.valid()) {
+                load_pair_records<RB>(idx, coset, scales, nsc, pre.slice * tpad + pre.t0,
+                                      ring + ((i + kStages - 1) % kStages) * kPairRecStage, lane);
+                pre.next();
+            }
+            cp_async_commit();
+            cp_async_wait<kStages - 1>();
             __syncwarp();
-        }
+            const uint32_t stage = ring + (i % kStages) * kPairRecStage;
+            const uint8_t* gstage = gbase + (stage - base);
+            const int t = cur.t0 + r;
 
-        // ---- the thread's half of the record
-        unsigned w[RP::WORDS];
-        lds_words<RBT>(stage + kPairRecIdx + r * RB + hf * RBT, w);
-        const unsigned cw_full = JOINT ? 0u : unsigned(reinterpret_cast<const uint16_t*>(gstage + kPairRecCoset)[r]);
-        unsigned cw = (cw_full >> (hf * NBT)) & ((1u << NBT) - 1u);
-        float scf[NSUB];
+            // ---- undo the temporal delta of the idx tile in place (every lane takes part)
+            bool first = false;  // row 0 starts its chain: no carry
+            if constexpr (decltype(cur)::kGroups) {
+                if (cur.group_start()) {
+                    if (cs.gexcl != nullptr) {
+                        load_group_carry<BITS, RB>(cs, cur.G, lane % NU, carry, carry_c, !JOINT);
+                        carry_c = (carry_c >> (hf * NBT)) & ((1u << NBT) - 1u);  // the thread's half of the word
+                    } else {
+                        first = true;
+                    }
+                }
+                unsigned cu[NV];
 #pragma unroll
-        for (int s = 0; s < NSUB; ++s)
-            scf[s] = __half2float(reinterpret_cast<const __half*>(gstage + kPairRecScale)[r * nsc + ((hf * NSUB + s) >> gsh)]);
-        __syncwarp();  // the stage may be refilled
-        unsigned blk[NBT];
-        RP::unpack(w, blk);
-
-        // ---- the coset words' delta: an exclusive-or scan over the rows (lane stride 2) + carry
-        if (delta && !JOINT) {
+                for (int n = 0; n < NV; ++n) cu[n] = carry[n];
+                undelta_tile<BITS, RB, kPairRows>(stage + kPairRecIdx, lane, first, cu);
 #pragma unroll
-            for (int off = 2; off < 32; off *= 2) {
-                const unsigned vc = __shfl_up_sync(kFull, cw, off);
-                if (lane >= off) cw ^= vc;
+                for (int n = 0; n < NV; ++n) carry[n] = cu[n];
+                __syncwarp();
             }
-            if (!first) cw ^= carry_c;
-            carry_c = __shfl_sync(kFull, cw, 30 + hf);
-        }
 
-        if constexpr (JOINT) {  // strict joint format: the coset bits come out of the block codes
+            // ---- the thread's half of the record
+            unsigned w[RP::WORDS];
+            lds_words<RBT>(stage + kPairRecIdx + r * RB + hf * RBT, w);
+            const unsigned cw_full = JOINT ? 0u : unsigned(reinterpret_cast<const uint16_t*>(gstage + kPairRecCoset)[r]);
+            unsigned cw = (cw_full >> (hf * NBT)) & ((1u << NBT) - 1u);
+            float scf[NSUB];
 #pragma unroll
-            for (int k = 0; k < NBT; ++k) {
-                unsigned c;
-                blk[k] = joint_split<BITS>(blk[k], c);
-                cw |= c << k;
+            for (int s = 0; s < NSUB; ++s)
+                scf[s] = __half2float(reinterpret_cast<const __half*>(gstage + kPairRecScale)[r * nsc + ((hf * NSUB + s) >> gsh)]);
+            __syncwarp();  // the stage may be refilled
+            unsigned blk[NBT];
+            RP::unpack(w, blk);
+
+            // ---- the coset words' delta: an exclusive-or scan over the rows (lane stride 2) + carry
+            if (decltype(cur)::kGroups && !JOINT) {
+#pragma unroll
+                for (int off = 2; off < 32; off *= 2) {
+                    const unsigned vc = __shfl_up_sync(kFull, cw, off);
+                    if (lane >= off) cw ^= vc;
+                }
+                if (!first) cw ^= carry_c;
+                carry_c = __shfl_sync(kFull, cw, 30 + hf);
             }
-        }
 
-        float y[HALF];
-        pair_decode_codes<D, BITS>(blk, cw, scf, sgn, y);
-
-        // ---- RoPE re-apply on keys: pairs (i, i + D/2) are slots (l, l + Q)
-        if (rope != nullptr) {
-            const float4* cs = rope + (t < cur.t_end() ? t : cur.t_begin());
+            if constexpr (JOINT) {  // strict joint format: the coset bits come out of the block codes
 #pragma unroll
-            for (int qq = 0; qq < Q / 2; ++qq)
-                pair_rope_apply<D>(y, qq, __ldg(cs + int64_t(hf * (Q / 2) + qq) * tokens), sgn);
-        }
+                for (int k = 0; k < NBT; ++k) {
+                    unsigned c;
+                    blk[k] = joint_split<BITS>(blk[k], c);
+                    cw |= c << k;
+                }
+            }
 
-        pair_store_rows<D, 1>(y, outbuf + (i & 1) * kPairTileBytes, r, hf, lane, &out_map, cur.t0, int(cur.slice));
-        cur.next();
-    }
+            float y[HALF];
+            pair_decode_codes<D, BITS>(blk, cw, scf, sgn, y);
+
+            // ---- RoPE re-apply on keys: pairs (i, i + D/2) are slots (l, l + Q)
+            if (rope != nullptr) {
+                const float4* tab = rope + (t < tokens ? t : cur.t0);
+#pragma unroll
+                for (int qq = 0; qq < Q / 2; ++qq)
+                    pair_rope_apply<D>(y, qq, __ldg(tab + int64_t(hf * (Q / 2) + qq) * tokens), sgn);
+            }
+
+            pair_store_rows<D, 1>(y, outbuf + (i & 1) * kPairTileBytes, r, hf, lane, &out_map, cur.t0, int(cur.slice));
+            cur.next();
+        }
+    };
+    if (!cs.delta)
+        run(TileWalkT<kPairRows>(warp, nwarps, slices, tokens, kPairRows));
+    else
+        run(GroupWalk<kPairRows>(warp, nwarps, slices, cs.geo));
     cp_async_wait<0>();
     if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Work items: single tiles without a delta, groups of a chain's tiles with
+// one (units: slices, or the key kernel's groups of slices).
+static int64_t work_items(const LaunchArgs& a, int64_t units, int rows, const ChainState& cs) {
+    if (!cs.delta) return units * ((a.tokens + rows - 1) / rows);
+    return units * int64_t(cs.geo.cps) * cs.geo.gpc;
+}
+
 template <int D, int BITS, bool JOINT>
 static int launch_pair(const LaunchArgs& a, const uint8_t* idx, const uint16_t* coset, const __half* scales,
-                       const float4* rope, const CUtensorMap& map) {
+                       const float4* rope, const CUtensorMap& map, const ChainState& cs) {
     auto kern = decompress_pair_kernel<D, BITS, JOINT>;
     if (!ensure_smem(reinterpret_cast<const void*>(kern), kPairDecompressSmem)) return NQ_ERR_CUDA;
-    const int chunk = a.delta_chunk > 0 ? a.delta_chunk : kPairRows;
-    const int64_t items = a.slices * ((a.tokens + chunk - 1) / chunk);
+    const int64_t items = work_items(a, a.slices, kPairRows, cs);
     const int64_t want = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
     if (want == 0) return NQ_OK;
     const int cap = grid_capacity(reinterpret_cast<const void*>(kern), kPairDecompressSmem);
     if (cap <= 0) return NQ_ERR_CUDA;
     const int grid = int(std::min<int64_t>(want, cap));
     kern<<<grid, kThreads, kPairDecompressSmem, a.stream>>>(idx, coset, scales, rope, map, a.slices, a.tokens,
-                                                            a.tpad, a.group, chunk, a.delta_chunk > 0);
+                                                            a.tpad, a.group, cs);
     return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
 }
 
 template <int D, int BITS, bool JOINT>
 static int launch(const LaunchArgs& a, const uint8_t* idx, const uint16_t* coset, const __half* scales,
-                  const float4* rope, const CUtensorMap& map) {
+                  const float4* rope, const CUtensorMap& map, const ChainState& cs) {
     auto kern = decompress_kernel<D, BITS, JOINT>;
     if (!ensure_smem(reinterpret_cast<const void*>(kern), kDecompressSmem)) return NQ_ERR_CUDA;
-    const int chunk = a.delta_chunk > 0 ? a.delta_chunk : kTileRows;
-    const int64_t items = a.slices * ((a.tokens + chunk - 1) / chunk);
+    const int64_t items = work_items(a, a.slices, kTileRows, cs);
     const int64_t want = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
     if (want == 0) return NQ_OK;
     const int cap = grid_capacity(reinterpret_cast<const void*>(kern), kDecompressSmem);
     if (cap <= 0) return NQ_ERR_CUDA;
     const int grid = int(std::min<int64_t>(want, cap));
     kern<<<grid, kThreads, kDecompressSmem, a.stream>>>(idx, coset, scales, rope, map, a.slices, a.tokens,
-                                                        a.tpad, a.group, chunk, a.delta_chunk > 0);
+                                                        a.tpad, a.group, cs);
     return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
 }
 
 template <int D, int BITS, bool JOINT>
 static int launch_keys(const LaunchArgs& a, const uint8_t* idx, const uint16_t* coset, const __half* scales,
-                       const float4* rope, const CUtensorMap& map) {
+                       const float4* rope, const CUtensorMap& map, const ChainState& cs) {
     auto kern = decompress_key_kernel<D, BITS, JOINT>;
     constexpr int smem = KeyStage<D>::SMEM;
     if (!ensure_smem(reinterpret_cast<const void*>(kern), smem)) return NQ_ERR_CUDA;
-    const int chunk = a.delta_chunk > 0 ? a.delta_chunk : kTileRows;
     const int64_t ngroups = (a.slices + kKeyWarps - 1) / kKeyWarps;
-    const int64_t items = ngroups * ((a.tokens + chunk - 1) / chunk);
+    const int64_t items = work_items(a, ngroups, kTileRows, cs);
     if (items == 0) return NQ_OK;
     const int cap = grid_capacity_threads(reinterpret_cast<const void*>(kern), smem, kKeyThreads);
     if (cap <= 0) return NQ_ERR_CUDA;
     const int grid = int(std::min<int64_t>(items, cap));
     kern<<<grid, kKeyThreads, smem, a.stream>>>(idx, coset, scales, rope, map, a.slices, a.tokens, a.tpad,
-                                                a.group, chunk, a.delta_chunk > 0);
+                                                a.group, cs);
+    return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
+}
+
+// The starting sums of the groups of a delta-coded tensor whose chains are
+// longer than one group: group totals, then the chain scan.
+template <int BITS, int RB, int R>
+static int launch_chain_sums(const LaunchArgs& a, const uint8_t* idx, const uint16_t* coset, const ChainState& cs) {
+    const uint64_t groups = uint64_t(a.slices) * cs.geo.cps * cs.geo.gpc;
+    if (groups == 0) return NQ_OK;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return NQ_ERR_CUDA;
+    const int cap = 8 * sms;  // blocks of 8 warps, 8 resident per SM (the kernels hold few registers)
+    int grid = int(std::min<uint64_t>((groups + 7) / 8, uint64_t(cap)));
+    delta_group_kernel<BITS, RB, R><<<grid, 256, 0, a.stream>>>(idx, coset, a.slices, a.tpad, cs.geo, cs.gsum,
+                                                                cs.slot_words);
+    if (cudaGetLastError() != cudaSuccess) return NQ_ERR_CUDA;
+    const uint64_t chains = uint64_t(a.slices) * cs.geo.cps;
+    grid = int(std::min<uint64_t>((chains + 7) / 8, uint64_t(cap)));
+    delta_chain_kernel<BITS, RB><<<grid, 256, 0, a.stream>>>(a.slices, cs.geo, cs.gsum, cs.gexcl, cs.slot_words,
+                                                             coset != nullptr);
     return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
 }
 
 template <int D, int BITS, bool JOINT>
 static int launch_any(const LaunchArgs& a, const uint8_t* idx, const uint16_t* coset, const __half* scales,
-                      const float4* rope, const CUtensorMap& map) {
+                      const float4* rope, const CUtensorMap& map, int max_bits) {
+    constexpr int DP = PaddedDim<D>::value;
+    constexpr int RB = DP * BITS / 8;
+    constexpr int R = D == 64 ? kPairRows : kTileRows;
+    ChainState cs;
+    if (a.delta_chunk > 0) {
+        const ChainPlan cp = chain_plan(a.slices, a.tokens, D, max_bits, a.delta_chunk);
+        cs.delta = true;
+        cs.geo = cp.geo;
+        cs.slot_words = cp.slot_words;
+        if (cp.total > 0) {  // chains longer than a group: starting sums from the workspace
+            if (a.workspace == nullptr) return NQ_ERR_ARG;
+            cs.gsum = reinterpret_cast<uint32_t*>(a.workspace + cp.gsum);
+            cs.gexcl = reinterpret_cast<uint32_t*>(a.workspace + cp.gexcl);
+            const int st = launch_chain_sums<BITS, RB, R>(a, idx, coset, cs);
+            if (st != NQ_OK) return st;
+        }
+    }
     if constexpr (D != 64) {
-        if (rope != nullptr) return launch_keys<D, BITS, JOINT>(a, idx, coset, scales, rope, map);
-        return launch<D, BITS, JOINT>(a, idx, coset, scales, rope, map);
+        if (rope != nullptr) return launch_keys<D, BITS, JOINT>(a, idx, coset, scales, rope, map, cs);
+        return launch<D, BITS, JOINT>(a, idx, coset, scales, rope, map, cs);
     } else {
-        return launch_pair<D, BITS, JOINT>(a, idx, coset, scales, rope, map);
+        return launch_pair<D, BITS, JOINT>(a, idx, coset, scales, rope, map, cs);
     }
 }
 
 template <int D>
-static int dispatch_bits(const LaunchArgs& a, int bits, const uint8_t* idx, const uint16_t* coset,
+static int dispatch_bits(const LaunchArgs& a, int bits, int max_bits, const uint8_t* idx, const uint16_t* coset,
                          const __half* scales, const float4* rope, const CUtensorMap& map) {
     // no coset words: the strict joint format, whose block codes carry the coset bits
     const bool joint = coset == nullptr;
     switch (bits) {
         case 2:
-            return joint ? launch_any<D, 2, true>(a, idx, coset, scales, rope, map)
-                         : launch_any<D, 2, false>(a, idx, coset, scales, rope, map);
+            return joint ? launch_any<D, 2, true>(a, idx, coset, scales, rope, map, max_bits)
+                         : launch_any<D, 2, false>(a, idx, coset, scales, rope, map, max_bits);
         case 3:
-            return joint ? launch_any<D, 3, true>(a, idx, coset, scales, rope, map)
-                         : launch_any<D, 3, false>(a, idx, coset, scales, rope, map);
+            return joint ? launch_any<D, 3, true>(a, idx, coset, scales, rope, map, max_bits)
+                         : launch_any<D, 3, false>(a, idx, coset, scales, rope, map, max_bits);
         case 4:
-            return joint ? launch_any<D, 4, true>(a, idx, coset, scales, rope, map)
-                         : launch_any<D, 4, false>(a, idx, coset, scales, rope, map);
+            return joint ? launch_any<D, 4, true>(a, idx, coset, scales, rope, map, max_bits)
+                         : launch_any<D, 4, false>(a, idx, coset, scales, rope, map, max_bits);
         default:
             return NQ_ERR_UNSUPPORTED;
     }
 }
 
-int launch_decompress_tensor(const LaunchArgs& a, int head_dim, int bits, const uint8_t* idx,
-                             const uint16_t* coset, const uint16_t* scales, const float* rope,
-                             void* x_out) {
+int launch_decompress_tensor(const LaunchArgs& a, int head_dim, int bits, int max_bits, const uint8_t* idx,
+                             const uint16_t* coset, const uint16_t* scales, const float* rope, void* x_out) {
     CUtensorMap map;
     const int box_rows = head_dim != 64 ? kTileRows : kPairRows;
     if (!make_row_tile_map(&map, x_out, head_dim, a.tokens, a.slices, box_rows)) return NQ_ERR_CUDA;
@@ -649,11 +701,11 @@ int launch_decompress_tensor(const LaunchArgs& a, int head_dim, int bits, const 
     const float4* r = reinterpret_cast<const float4*>(rope);
     switch (head_dim) {
         case 64:
-            return dispatch_bits<64>(a, bits, idx, coset, sh, r, map);
+            return dispatch_bits<64>(a, bits, max_bits, idx, coset, sh, r, map);
         case 96:
-            return dispatch_bits<96>(a, bits, idx, coset, sh, r, map);
+            return dispatch_bits<96>(a, bits, max_bits, idx, coset, sh, r, map);
         case 128:
-            return dispatch_bits<128>(a, bits, idx, coset, sh, r, map);
+            return dispatch_bits<128>(a, bits, max_bits, idx, coset, sh, r, map);
         default:
             return NQ_ERR_UNSUPPORTED;
     }

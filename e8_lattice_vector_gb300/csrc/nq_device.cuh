@@ -595,6 +595,7 @@ struct RingSlots {
 // (slice, c) pair with one carry; the walk ends when slice reaches slices.
 template <int ROWS>
 struct TileWalkT {
+    static constexpr bool kGroups = false;  // single tiles, no delta groups
     int64_t slice, slices, dslice;
     int nchunks, chunk, tokens, c, dc, t0;
     __device__ TileWalkT(int64_t first, int64_t step, int64_t slices_, int tokens_, int chunk_)
@@ -628,6 +629,61 @@ struct TileWalkT {
     }
 };
 using TileWalk = TileWalkT<kTileRows>;
+
+// Compression work items: (slice, segment of `seg` tokens), item = slice *
+// nseg + c, walked like TileWalkT.  With a temporal delta whose chains restart
+// every `dchunk` tokens (0: no delta), a segment that begins inside a chain
+// needs the raw codes of the token before its first row: the walk then starts
+// one tile early, at t_begin - ROWS, with a halo tile that is encoded but not
+// stored.  `rem` is t0 modulo dchunk, kept by additions (one division per
+// segment): row 0 of a tile with rem == 0 starts a chain.  dchunk and seg are
+// multiples of 32 (ROWS divides both).
+template <int ROWS>
+struct SegWalk {
+    int64_t slice, slices, dslice;
+    int nseg, seg, tokens, c, dc, t0, dchunk, rem;
+    __device__ SegWalk(int64_t first, int64_t step, int64_t slices_, int tokens_, int seg_, int dchunk_)
+        : slices(slices_), seg(seg_), tokens(tokens_), dchunk(dchunk_) {
+        nseg = (tokens_ + seg_ - 1) / seg_;
+        slice = slices_;  // no work when there are no segments
+        dslice = 0;
+        c = dc = 0;
+        if (nseg > 0) {
+            slice = first / nseg;
+            c = int(first - slice * nseg);
+            dslice = step / nseg;
+            dc = int(step - dslice * nseg);
+        }
+        enter();
+    }
+    __device__ __forceinline__ void enter() {  // the first tile of segment c
+        t0 = c * seg;
+        rem = dchunk > 0 ? t0 % dchunk : 0;
+        if (rem != 0) {
+            t0 -= ROWS;
+            rem -= ROWS;
+        }
+    }
+    __device__ __forceinline__ bool valid() const { return slice < slices; }
+    __device__ __forceinline__ int t_begin() const { return c * seg; }
+    __device__ __forceinline__ int t_end() const { return min(c * seg + seg, tokens); }
+    __device__ __forceinline__ bool halo() const { return t0 < c * seg; }
+    __device__ __forceinline__ bool chain_start() const { return rem == 0; }
+    __device__ __forceinline__ void next() {
+        t0 += ROWS;
+        rem += ROWS;
+        if (rem == dchunk) rem = 0;
+        if (t0 >= t_end()) {
+            slice += dslice;
+            c += dc;
+            if (c >= nseg) {
+                c -= nseg;
+                ++slice;
+            }
+            enter();
+        }
+    }
+};
 
 // ----------------------------------------------------------- row records
 

@@ -20,6 +20,57 @@ struct PaddedDim {
     static constexpr int value = D <= 64 ? 64 : 128;
 };
 
+// Decompression with a temporal delta: the chained tiles of one tensor
+// (tiles of R rows, tpc tiles per chain -- delta_chunk / R, a slice's last
+// chain may be shorter) are decoded in runs of up to 32 consecutive tiles
+// ("groups") that never cross a chain; a warp walks a group's tiles in order
+// with the delta's running sum in registers.  A group that does not start its
+// chain takes its starting sum from the workspace (nq_chain.cuh).
+struct ChainGeom {
+    uint32_t tiles;  // tiles per slice
+    uint32_t tpc;    // tiles per chain
+    uint32_t cps;    // chains per slice
+    uint32_t gpc;    // groups per chain
+};
+
+// The decompression workspace: needed only when a chain is longer than one
+// group (0 bytes otherwise); per group one slot of slot_words words (the idx
+// row words, packed as in a record row, and a coset word, padded to 16 bytes
+// and sized for the wider of the two bit widths) for the group's total and one
+// for the sum of its chain's earlier groups, 256-byte aligned.
+struct ChainPlan {
+    ChainGeom geo{};
+    int slot_words = 0;
+    uint64_t groups = 0, gsum = 0, gexcl = 0, total = 0;
+};
+
+inline ChainPlan chain_plan(int64_t slices, int tokens, int head_dim, int max_bits, int delta_chunk) {
+    ChainPlan c;
+    if (delta_chunk <= 0 || slices <= 0 || tokens <= 0) return c;
+    const int rows = head_dim == 64 ? 16 : 32;  // the decompressors' tile
+    const int dp = head_dim <= 64 ? 64 : 128;
+    c.geo.tiles = uint32_t((tokens + rows - 1) / rows);
+    c.geo.tpc = uint32_t(delta_chunk / rows);
+    c.geo.cps = (c.geo.tiles + c.geo.tpc - 1) / c.geo.tpc;
+    c.geo.gpc = (std::min(c.geo.tpc, c.geo.tiles) + 31u) / 32u;
+    c.slot_words = (dp * max_bits / 32 + 1 + 3) / 4 * 4;
+    c.groups = uint64_t(slices) * c.geo.cps * c.geo.gpc;
+    if (c.geo.gpc <= 1) return c;  // every group starts its chain: no workspace
+    auto a256 = [](uint64_t v) { return (v + 255u) & ~uint64_t(255u); };
+    c.gsum = 0;
+    c.gexcl = a256(c.groups * c.slot_words * 4);
+    c.total = c.gexcl + a256(c.groups * c.slot_words * 4);
+    return c;
+}
+
+struct ChainState {
+    bool delta = false;          // a temporal delta: walk groups of tiles
+    uint32_t* gsum = nullptr;    // per group: its total (workspace)
+    uint32_t* gexcl = nullptr;   // per group: the sum of its chain's earlier groups (nullptr: one group per chain)
+    int slot_words = 0;
+    ChainGeom geo{};
+};
+
 struct LaunchArgs {
     int64_t slices;  // layers * batch * kv_heads
     int tokens;
@@ -27,6 +78,7 @@ struct LaunchArgs {
     int group;
     int delta_chunk;
     cudaStream_t stream;
+    uint8_t* workspace = nullptr;  // decompression with a delta: the running sums' scratch
 };
 
 // Blocks of kThreads that fit on the current device at once for `kernel` with
@@ -47,7 +99,8 @@ bool make_row_tile_map(CUtensorMap* map, void* base, int head_dim, int tokens, i
 int launch_compress_tensor(const LaunchArgs& a, int head_dim, int bits, int mode, const void* x,
                            const float* rope, uint8_t* idx, uint16_t* coset, uint16_t* scales);
 // coset == nullptr: the joint format.
-int launch_decompress_tensor(const LaunchArgs& a, int head_dim, int bits, const uint8_t* idx,
+// max_bits: the wider of the call's two bit widths (it sizes the workspace slots).
+int launch_decompress_tensor(const LaunchArgs& a, int head_dim, int bits, int max_bits, const uint8_t* idx,
                              const uint16_t* coset, const uint16_t* scales, const float* rope,
                              void* x_out);
 int launch_roundtrip_tensor(const LaunchArgs& a, int head_dim, int bits, bool strict, const void* x,

@@ -43,10 +43,10 @@ bool rope_ok(const nq_params* p, const float* rope_table) {
 
 // Plan, then check the pointers the loop will use.
 int prepare(const nq_shape* shape, const nq_params* params, const nq_layer_bits* per_layer,
-            std::vector<uint64_t>& offs, uint64_t* total) {
+            std::vector<uint64_t>& offs, uint64_t* total, uint64_t* ws = nullptr) {
     if (!shape) return NQ_ERR_ARG;
     offs.assign(size_t(shape->layers > 0 ? shape->layers : 0), 0);
-    return nq_plan_layers(shape, params, per_layer, offs.data(), total);
+    return nq_plan_layers(shape, params, per_layer, offs.data(), total, ws);
 }
 
 int copy(void* dst, const void* src, uint64_t bytes, cudaStream_t s) {
@@ -59,14 +59,14 @@ int copy(void* dst, const void* src, uint64_t bytes, cudaStream_t s) {
 extern "C" {
 
 int nq_plan_layers(const nq_shape* shape, const nq_params* params, const nq_layer_bits* per_layer,
-                   uint64_t* offsets, uint64_t* total_bytes) {
+                   uint64_t* offsets, uint64_t* total_bytes, uint64_t* workspace_bytes) {
     if (!shape || !params || !total_bytes) return NQ_ERR_ARG;
     nq_layout whole;
     int st = nq_plan(shape, params, &whole);  // validates the shape and the shared parameters
     if (st != NQ_OK) return st;
     if (shape->layers > 0 && (!per_layer || !offsets)) return NQ_ERR_ARG;
     const nq_shape s1 = one_layer(shape);
-    uint64_t off = 0;
+    uint64_t off = 0, ws = 0;
     for (int l = 0; l < shape->layers; ++l) {
         uint64_t bytes = 2 * layer_bytes(shape);
         if (!kept(per_layer[l])) {
@@ -75,11 +75,13 @@ int nq_plan_layers(const nq_shape* shape, const nq_params* params, const nq_laye
             st = nq_plan(&s1, &p, &L);
             if (st != NQ_OK) return st;
             bytes = L.total_bytes;
+            ws = std::max<uint64_t>(ws, L.workspace_bytes);
         }
         offsets[l] = off;
         off = align256(off + bytes);
     }
     *total_bytes = off;
+    if (workspace_bytes) *workspace_bytes = ws;
     return NQ_OK;
 }
 
@@ -115,17 +117,18 @@ int nq_compress_kv_layers(const void* k_f16, const void* v_f16, const float* rop
 
 int nq_decompress_kv_layers(const void* in, size_t in_bytes, const float* rope_table, const nq_shape* shape,
                             const nq_params* params, const nq_layer_bits* per_layer, void* k_f16_out,
-                            void* v_f16_out, void* stream) {
+                            void* v_f16_out, void* workspace, size_t workspace_bytes, void* stream) {
     std::vector<uint64_t> offs;
-    uint64_t total = 0;
-    int st = prepare(shape, params, per_layer, offs, &total);
+    uint64_t total = 0, ws = 0;
+    int st = prepare(shape, params, per_layer, offs, &total, &ws);
     if (st != NQ_OK) return st;
     const uint64_t lb = layer_bytes(shape);
     if (offs.empty() || lb == 0) return NQ_OK;
     if (!in || !k_f16_out || !v_f16_out || !aligned16(in) || !aligned16(k_f16_out) || !aligned16(v_f16_out))
         return NQ_ERR_ARG;
     if (!rope_ok(params, rope_table)) return NQ_ERR_ARG;
-    if (in_bytes < total) return NQ_ERR_SIZE;
+    if (ws > 0 && (!workspace || !aligned16(workspace))) return NQ_ERR_ARG;
+    if (in_bytes < total || workspace_bytes < ws) return NQ_ERR_SIZE;
     const nq_shape s1 = one_layer(shape);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     for (size_t l = 0; l < offs.size() && st == NQ_OK; ++l) {
@@ -138,7 +141,7 @@ int nq_decompress_kv_layers(const void* in, size_t in_bytes, const float* rope_t
             if (st == NQ_OK) st = copy(v, part + lb, lb, s);
         } else {
             const nq_params p = layer_params(params, per_layer[l]);
-            st = nq_decompress_kv(part, room, rope_table, &s1, &p, k, v, stream);
+            st = nq_decompress_kv(part, room, rope_table, &s1, &p, k, v, workspace, workspace_bytes, stream);
         }
     }
     return st;

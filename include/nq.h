@@ -97,7 +97,8 @@ typedef struct {
     float rope_theta;
 } nq_params;
 
-/* Byte offsets and sizes of the compressed buffer's sections. */
+/* Byte offsets and sizes of the compressed buffer's sections, and the size
+ * of the workspace that decompression with a temporal delta needs. */
 typedef struct {
     uint32_t version;
     uint32_t padded_dim;
@@ -107,6 +108,7 @@ typedef struct {
     uint64_t k_idx_row_bytes, v_idx_row_bytes, scales_per_row;
     uint64_t k_idx, k_coset, k_scale, v_idx, v_coset, v_scale;
     uint64_t total_bytes;
+    uint64_t workspace_bytes; /* nq_decompress_kv's workspace: 0 without a delta */
 } nq_layout;
 
 /* Validate shape and params and describe the compressed buffer.  Host only.
@@ -149,10 +151,28 @@ int nq_compress_kv(const void* k_f16, const void* v_f16, const float* rope_table
  * params) into K and V (device fp16, layout above): undo the delta, unpack,
  * unscale, inverse Hadamard, re-apply RoPE to keys, round to fp16 ("E8
  * walkthrough", quantize() dequantizes the lattice point; "What Makes This
- * Hard in Practice": RoPE removed before quantization and reapplied after). */
+ * Hard in Practice": RoPE removed before quantization and reapplied after).
+ *
+ * workspace: caller-owned device scratch of workspace_bytes >=
+ * nq_plan().workspace_bytes (16-byte aligned).  It is needed only when a
+ * delta chain is longer than 32 record tiles (1024 tokens; 512 at head_dim
+ * 64), up to the method's single chain per slice; otherwise the size is 0 and
+ * it may be NULL.  The decoder walks each chain in runs of up to 32 tiles,
+ * carrying the delta's running sum in registers; two light passes over the
+ * idx section first leave in the workspace, per run, the running sum of its
+ * chain's earlier rows (field-wise modulo 2^b, coset words by exclusive or).
+ * Its contents are overwritten by every call; calls that share a workspace
+ * must be ordered on one stream.  No kernel waits for another. */
 int nq_decompress_kv(const void* in, size_t in_bytes, const float* rope_table,
                      const nq_shape* shape, const nq_params* params, void* k_f16_out,
-                     void* v_f16_out, void* stream);
+                     void* v_f16_out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* The deferred status of the work enqueued on `stream`: waits for the stream
+ * to finish, then returns NQ_ERR_CUDA if the stream or an earlier launch
+ * failed (the CUDA error is left for the caller to inspect), else NQ_OK.  The
+ * other entry points return as soon as their work is enqueued, so a fault in
+ * a kernel surfaces here (or at the caller's next synchronisation). */
+int nq_get_status(void* stream);
 
 /* The round trip in one pass: K and V (device fp16) -> the reconstruction
  * decompress(compress(.)) written to k_f16_out / v_f16_out (device fp16, same
@@ -185,19 +205,21 @@ typedef struct {
 } nq_layer_bits;
 
 /* offsets: caller-owned host array of shape->layers entries; *total_bytes:
- * the buffer size.  Host only. */
+ * the buffer size; *workspace_bytes (may be NULL): the workspace that
+ * nq_decompress_kv_layers needs (the largest single layer's).  Host only. */
 int nq_plan_layers(const nq_shape* shape, const nq_params* params, const nq_layer_bits* per_layer,
-                   uint64_t* offsets, uint64_t* total_bytes);
+                   uint64_t* offsets, uint64_t* total_bytes, uint64_t* workspace_bytes);
 /* K, V (device fp16, layout above) -> `out` (device, out_bytes >= total).
  * per_layer: host array of shape->layers entries. */
 int nq_compress_kv_layers(const void* k_f16, const void* v_f16, const float* rope_table,
                           const nq_shape* shape, const nq_params* params, const nq_layer_bits* per_layer,
                           void* out, size_t out_bytes, void* stream);
-/* The inverse of nq_compress_kv_layers (same shape, params and table). */
+/* The inverse of nq_compress_kv_layers (same shape, params and table);
+ * workspace as for nq_decompress_kv, sized by nq_plan_layers. */
 int nq_decompress_kv_layers(const void* in, size_t in_bytes, const float* rope_table,
                             const nq_shape* shape, const nq_params* params,
                             const nq_layer_bits* per_layer, void* k_f16_out, void* v_f16_out,
-                            void* stream);
+                            void* workspace, size_t workspace_bytes, void* stream);
 /* nq_roundtrip_kv per layer; kept layers are copied (nothing to do in place). */
 int nq_roundtrip_kv_layers(const void* k_f16, const void* v_f16, const float* rope_table,
                            const nq_shape* shape, const nq_params* params,

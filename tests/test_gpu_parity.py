@@ -209,6 +209,13 @@ COMBOS = [
     ((1, 1, 3, 40, 64), 4, 2, 32, 0, 0, 0.0),
     ((1, 1, 2, 300, 128), 3, 2, 64, 1, 256, 1e4),
     ((1, 1, 2, 33, 128), 2, 2, 64, 0, 512, 1e4),
+    # long delta chains: decompression chains tiles by the look-back; chains longer than a
+    # compression segment start their segments with a halo tile
+    ((1, 1, 3, 1000, 128), 3, 2, 64, 0, 1024, 1e4),
+    ((1, 1, 3, 3000, 128), 2, 2, 64, 0, 3008, 1e4),
+    ((1, 2, 2, 2100, 96), 3, 2, 64, 1, 2112, 1e4),
+    ((1, 1, 2, 1500, 64), 2, 3, 64, 1, 1504, 5e5),
+    ((1, 1, 3, 500, 64), 4, 2, 32, 0, 512, 5e5),
     # strict joint format (no coset words)
     ((2, 1, 3, 77, 128), 2, 2, 64, 2, 0, 1e4),
     ((1, 2, 2, 130, 128), 3, 4, 32, 2, 32, 5e5),
@@ -520,3 +527,21 @@ def test_entropy_report_on_the_tiny_cache(nq):
             assert 0.0 < r["field_entropy_bits"] <= bits
             assert 0.0 <= r["byte_entropy_bits_per_byte"] <= 8.0
             assert r["raw_bits_per_coord"] == pytest.approx(bits + 1 / 8 + 16 * 2 / 128)
+
+
+def test_delta_status_clean_after_calls(nq):
+    """A delta-coded round trip through a reused workspace decodes the same
+    twice, and the stream reports no error."""
+    from e8_lattice_vector_gb300 import CodecParams
+
+    shape = (1, 1, 4, 700, 128)
+    p = CodecParams(3, 2, 64, 0, 704, 1e4)
+    K = torch.randn(shape, device="cuda").half()
+    V = torch.randn(shape, device="cuda").half()
+    rope = nq.RopeTable.build(700, 128, 1e4)
+    ws = nq.workspace(int(nq.plan(shape, p).workspace_bytes), K.device)
+    buf = nq.compress_kv(K, V, p, rope)
+    a = nq.decompress_kv(buf, shape, p, rope, ws=ws)
+    b = nq.decompress_kv(buf, shape, p, rope, ws=ws)
+    nq.get_status()  # raises on a deferred error
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])

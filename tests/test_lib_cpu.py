@@ -108,7 +108,18 @@ def test_compress_validates_before_touching_the_gpu(nq):
     assert L.nq_compress_kv(p17, p16, p16, ctypes.byref(shape), ctypes.byref(good), p16, 1 << 30, None) == nq.NQ_ERR_ARG
     # output too small
     assert L.nq_compress_kv(p16, p16, p16, ctypes.byref(shape), ctypes.byref(good), p16, 100, None) == nq.NQ_ERR_SIZE
-    assert L.nq_decompress_kv(p16, 100, p16, ctypes.byref(shape), ctypes.byref(good), p16, p16, None) == nq.NQ_ERR_SIZE
+    assert L.nq_decompress_kv(p16, 100, p16, ctypes.byref(shape), ctypes.byref(good), p16, p16, None, 0,
+                              None) == nq.NQ_ERR_SIZE
+    # with a long delta chain the workspace is required, aligned and large enough
+    shape = nq.Shape(1, 1, 8, 4096, 128)
+    dlt = nq.Params(2, 2, 64, 0, 4096, 1e4)
+    lay = nq.Layout()
+    assert L.nq_plan(ctypes.byref(shape), ctypes.byref(dlt), ctypes.byref(lay)) == 0 and lay.workspace_bytes > 0
+    big = 1 << 30
+    sh, dp = ctypes.byref(shape), ctypes.byref(dlt)
+    assert L.nq_decompress_kv(p16, big, p16, sh, dp, p16, p16, None, big, None) == nq.NQ_ERR_ARG
+    assert L.nq_decompress_kv(p16, big, p16, sh, dp, p16, p16, ctypes.c_void_p(24), big, None) == nq.NQ_ERR_ARG
+    assert L.nq_decompress_kv(p16, big, p16, sh, dp, p16, p16, p16, lay.workspace_bytes - 1, None) == nq.NQ_ERR_SIZE
     bad = nq.Params(2, 7, 64, 0, 0, 1e4)
     assert L.nq_compress_kv(p16, p16, p16, ctypes.byref(shape), ctypes.byref(bad), p16, 1 << 30, None) == nq.NQ_ERR_UNSUPPORTED
     # empty tensors are a no-op
@@ -194,13 +205,22 @@ def test_layers_validate_before_touching_the_gpu(nq):
     ok = (nq.LayerBits * 2)(nq.LayerBits(3, 2), nq.LayerBits(0, 0))
     half = (nq.LayerBits * 2)(nq.LayerBits(3, 0), nq.LayerBits(2, 2))
     sh, pr = ctypes.byref(shape), ctypes.byref(good)
-    assert L.nq_plan_layers(sh, pr, ok, offs, ctypes.byref(total)) == 0 and total.value > 0
-    assert L.nq_plan_layers(sh, pr, half, offs, ctypes.byref(total)) == nq.NQ_ERR_UNSUPPORTED
-    assert L.nq_plan_layers(sh, pr, None, offs, ctypes.byref(total)) == nq.NQ_ERR_ARG
+    ws = ctypes.c_uint64(7)
+    assert L.nq_plan_layers(sh, pr, ok, offs, ctypes.byref(total), ctypes.byref(ws)) == 0 and total.value > 0
+    assert ws.value == 0  # no delta, no workspace
+    assert L.nq_plan_layers(sh, pr, ok, offs, ctypes.byref(total), None) == 0
+    assert L.nq_plan_layers(sh, pr, half, offs, ctypes.byref(total), None) == nq.NQ_ERR_UNSUPPORTED
+    assert L.nq_plan_layers(sh, pr, None, offs, ctypes.byref(total), None) == nq.NQ_ERR_ARG
     p16 = ctypes.c_void_p(16)
     assert L.nq_compress_kv_layers(None, p16, p16, sh, pr, ok, p16, 1 << 30, None) == nq.NQ_ERR_ARG
     assert L.nq_compress_kv_layers(p16, p16, p16, sh, pr, ok, p16, 100, None) == nq.NQ_ERR_SIZE
-    assert L.nq_decompress_kv_layers(p16, 100, p16, sh, pr, ok, p16, p16, None) == nq.NQ_ERR_SIZE
+    assert L.nq_decompress_kv_layers(p16, 100, p16, sh, pr, ok, p16, p16, None, 0, None) == nq.NQ_ERR_SIZE
+    dlt = nq.Params(2, 2, 64, 0, 4096, 1e4)
+    sh = ctypes.byref(nq.Shape(2, 1, 8, 4096, 128))
+    assert L.nq_plan_layers(sh, ctypes.byref(dlt), ok, offs, ctypes.byref(total), ctypes.byref(ws)) == 0
+    assert ws.value > 0  # the compressed layer's workspace
+    assert L.nq_decompress_kv_layers(p16, 1 << 30, p16, sh, ctypes.byref(dlt), ok, p16, p16, p16, ws.value - 1,
+                                     None) == nq.NQ_ERR_SIZE
     assert L.nq_roundtrip_kv_layers(p16, p16, p16, sh, pr, half, p16, p16, None) == nq.NQ_ERR_UNSUPPORTED
     empty = nq.Shape(0, 1, 8, 64, 128)
     assert L.nq_compress_kv_layers(None, None, None, ctypes.byref(empty), pr, None, None, 0, None) == 0
@@ -209,7 +229,8 @@ def test_layers_validate_before_touching_the_gpu(nq):
     for table in (None, p17):
         assert L.nq_compress_kv_layers(p16, p16, table, sh, pr, ok_kept_first := (nq.LayerBits * 2)(
             nq.LayerBits(0, 0), nq.LayerBits(2, 2)), p16, 1 << 30, None) == nq.NQ_ERR_ARG
-        assert L.nq_decompress_kv_layers(p16, 1 << 30, table, sh, pr, ok_kept_first, p16, p16, None) == nq.NQ_ERR_ARG
+        assert L.nq_decompress_kv_layers(p16, 1 << 30, table, sh, pr, ok_kept_first, p16, p16, None, 0,
+                                         None) == nq.NQ_ERR_ARG
         assert L.nq_roundtrip_kv_layers(p16, p16, table, sh, pr, ok_kept_first, p16, p16, None) == nq.NQ_ERR_ARG
 
 
@@ -363,3 +384,34 @@ def test_binding_rejects_a_rope_table_on_another_device():
                lambda: nq.roundtrip_kv_layers(K, K, p, [(2, 2), (0, 0)], table, K_out=K, V_out=K)):
         with pytest.raises(ValueError, match="RopeTable is on cuda:0; the call runs on cuda:1"):
             fn()
+
+
+def test_workspace_plan_and_status_without_a_gpu(nq):
+    """Decompression walks delta chains in runs of up to 32 record tiles (32
+    rows; 16 at head_dim 64); only chains longer than one run need the
+    workspace: per run a slot of the idx row words plus a coset word for its
+    total and one for its starting sum.  nq_get_status answers through the C
+    ABI without a GPU (an error status, not a crash)."""
+    L = nq.lib()
+    for D, rows, kb, vb, chunk in ((128, 32, 3, 2, 96), (128, 32, 3, 2, 1024), (96, 32, 2, 2, 2048),
+                                   (64, 16, 4, 2, 4096)):
+        shape = nq.Shape(2, 1, 3, 1000, D)
+        lay = nq.Layout()
+        assert L.nq_plan(ctypes.byref(shape), ctypes.byref(nq.Params(kb, vb, 64, 0, 0, 1e4)), ctypes.byref(lay)) == 0
+        assert lay.workspace_bytes == 0
+        assert L.nq_plan(ctypes.byref(shape), ctypes.byref(nq.Params(kb, vb, 64, 0, chunk, 1e4)),
+                         ctypes.byref(lay)) == 0
+        tiles = (1000 + rows - 1) // rows
+        tpc = chunk // rows
+        gpc = (min(tpc, tiles) + 31) // 32
+        if gpc == 1:
+            assert lay.workspace_bytes == 0, (D, chunk)
+            continue
+        groups = 6 * ((tiles + tpc - 1) // tpc) * gpc
+        dp = 64 if D == 64 else 128
+        slot = (dp * max(kb, vb) // 32 + 1 + 3) // 4 * 4 * 4
+        assert lay.workspace_bytes >= 2 * groups * slot
+        assert lay.workspace_bytes % 256 == 0
+    import torch
+
+    assert L.nq_get_status(None) == (nq.NQ_OK if torch.cuda.is_available() else nq.NQ_ERR_CUDA)

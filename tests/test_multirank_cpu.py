@@ -63,3 +63,27 @@ def test_single_process_identity():
 
     assert bench.dist_max(3.5) == 3.5
     assert bench.whole_job_gbs(1, 2e9, 1000.0) == pytest.approx(2.0)
+
+
+def test_bench_starts_its_own_ranks(capfd):
+    """--gpus 2 without a torchrun environment: bench.launch_ranks starts two
+    ranks (torch.distributed.run, gloo on CPU); the stand-in rank reports the
+    whole-job line with n_gpus 2 and the slower rank's time."""
+    import json
+    import sys
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    env_before = os.environ.pop("WORLD_SIZE", None)
+    try:
+        rc = bench.launch_ranks(2, [], script=os.path.join(ROOT, "tests", "bench_rank_stub.py"))
+    finally:
+        if env_before is not None:
+            os.environ["WORLD_SIZE"] = env_before
+    out = capfd.readouterr().out
+    assert rc == 0, out
+    lines = [json.loads(l) for l in out.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    assert lines[0]["n_gpus"] == 2 and lines[0]["ms_per_step"] == 15.0
+    assert lines[0]["value"] == pytest.approx(2 * 1e9 / 15e-3 / 1e9)
