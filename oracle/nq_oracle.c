@@ -102,8 +102,8 @@ void orc_rope_apply(float* x, int head_dim, const float* cs_row) {
 
 /* ---------------------------------------------------------------- Hadamard */
 
-/* [QUANT "Handling outliers"]: rotated = vector @ H.T with H the Sylvester
- * Hadamard matrix; H is symmetric.  Reading: the unnormalised transform is
+/* [QUANT "Handling outliers"]: each vector is multiplied by the transpose of
+ * the Sylvester Hadamard matrix H, which is symmetric.  Reading: the unnormalised transform is
  * used; its factor sqrt(n) is absorbed by the group scale (compression) and
  * divided out exactly as a power of two (decompression). */
 static void butterfly_stage(float* x, int n, int h) {
@@ -173,7 +173,7 @@ uint16_t orc_group_scale(float amax, int bits, int dp) {
  *  - the fix-up coordinate is the first index of the largest score, the score
  *    being |e| for a step toward u and -|e| for a step away from it.
  *  - distance: sum of e_j^2 in j order by fmaf, plus the fix-up's cost
- *    1 - 2*score (the "extra cost" the prose names), evaluated as
+ *    1 - 2*score (the added cost of the flip the prose describes), evaluated as
  *    d + fmaf(-2, score, 1). */
 static float coset_candidate(const float* u, int half, int enforce_parity, int bits, float* r) {
     float hi;
@@ -238,7 +238,8 @@ void orc_e8_nearest(const float* u, float* r, int64_t n_blocks, int strict, int 
 
 /* Reading: coordinate i's b-bit code sits at bit i*b of the row's bit string,
  * least significant bit first, bytes little-endian [WALK "Bit Rate
- * Accounting": 3 bits x 8 dims = 24 bits per group, "packed uint8"]. */
+ * Accounting": b bits for each of a block's 8 coordinates, the indices packed
+ * into bytes]. */
 static unsigned get_field(const uint8_t* idx, int i, int bits) {
     unsigned v = 0;
     for (int q = 0; q < bits; ++q) {
