@@ -5,9 +5,11 @@ package is its thin Python binding.  Nothing here computes the method on the
 CPU: when the library is missing, calls raise.
 """
 from .codec import (CodecParams, RopeTable, code_histogram, compress_kv, compress_kv_layers, decompress_kv,
-                    decompress_kv_layers, e8_nearest, get_status, layer_profile, plan, plan_layers, roundtrip_kv,
-                    roundtrip_kv_layers, sections, shape_of, workspace)
+                    decompress_kv_layers, decompress_kv_static, e8_nearest, get_status, layer_profile, plan,
+                    plan_layers, roundtrip_kv, roundtrip_kv_layers, sections, shape_of, static_workspace_bytes,
+                    workspace)
 
 __all__ = ["CodecParams", "RopeTable", "code_histogram", "compress_kv", "compress_kv_layers", "decompress_kv",
-           "decompress_kv_layers", "e8_nearest", "get_status", "layer_profile", "plan", "plan_layers", "roundtrip_kv",
-           "roundtrip_kv_layers", "sections", "shape_of", "workspace"]
+           "decompress_kv_layers", "decompress_kv_static", "e8_nearest", "get_status", "layer_profile", "plan",
+           "plan_layers", "roundtrip_kv", "roundtrip_kv_layers", "sections", "shape_of", "static_workspace_bytes",
+           "workspace"]

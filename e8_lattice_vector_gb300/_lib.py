@@ -55,6 +55,9 @@ SIGNATURES = {
     "nq_decompress_kv": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
                                         ctypes.POINTER(Shape), ctypes.POINTER(Params), ctypes.c_void_p,
                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "nq_decompress_kv_static": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                                               ctypes.POINTER(Shape), ctypes.POINTER(Params), ctypes.c_void_p,
+                                               ctypes.c_void_p, ctypes.c_void_p]),
     "nq_get_status": (ctypes.c_int, [ctypes.c_void_p]),
     "nq_roundtrip_kv": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                        ctypes.POINTER(Shape), ctypes.POINTER(Params), ctypes.c_void_p,

@@ -227,6 +227,29 @@ def decompress_kv(buf, shape, params, rope=None, K_out=None, V_out=None, ws=None
     return K_out, V_out
 
 
+def decompress_kv_static(buf, shape, params, rope, K_out, V_out):
+    """decompress_kv through nq_decompress_kv_static: the delta scratch is the
+    library's static device array, so nothing is allocated, here or in the
+    library (K_out and V_out are required).  Raises NQError (NQ_ERR_SIZE) when
+    the call needs more scratch than the array holds
+    (plan(...).workspace_bytes > static_workspace_bytes())."""
+    shape = _norm_shape(shape)
+    _check_buf(buf)
+    _check_like(K_out, shape, buf.device, "K_out")
+    _check_like(V_out, shape, buf.device, "V_out")
+    rp = _rope_ptr(rope, params, shape[3], shape[4], buf.device)
+    _call(buf.device, "nq_decompress_kv_static", ctypes_void(buf.data_ptr()), int(buf.numel()), rp,
+          ctypes_ref(_cshape(shape)), ctypes_ref(params.c()), ctypes_void(K_out.data_ptr()),
+          ctypes_void(V_out.data_ptr()), _stream_handle(buf.device))
+    return K_out, V_out
+
+
+def static_workspace_bytes():
+    """Size of the static scratch behind decompress_kv_static (the header's
+    NQ_STATIC_WORKSPACE_BYTES)."""
+    return 8 << 20
+
+
 def get_status(device=None):
     """The deferred status of the work enqueued on the device's current
     stream (waits for it): raises NQError when the stream or an earlier launch

@@ -167,6 +167,29 @@ int nq_decompress_kv(const void* in, size_t in_bytes, const float* rope_table,
                      const nq_shape* shape, const nq_params* params, void* k_f16_out,
                      void* v_f16_out, void* workspace, size_t workspace_bytes, void* stream);
 
+/* nq_decompress_kv without a workspace argument: the delta scratch is a
+ * static device array of NQ_STATIC_WORKSPACE_BYTES owned by the library (one
+ * per device), and the call allocates nothing.  The pages have no counterpart
+ * of this call: it serves callers that cannot allocate device memory or hand
+ * over a workspace (a plug-in given only the cache and record pointers by an
+ * engine that owns all device memory in a pool fixed at start-up, a C host
+ * program without a device allocator).  Arguments, layout, ownership and
+ * results as nq_decompress_kv, bit for bit.
+ *
+ * Limit: NQ_ERR_SIZE when nq_plan().workspace_bytes exceeds
+ * NQ_STATIC_WORKSPACE_BYTES (enough for one delta chain per slice on 384
+ * slices of 131072 tokens at up to 4 bits; shorter chains or no delta need
+ * none).  The first call on a device that needs the scratch looks up its
+ * address (cudaGetSymbolAddress, with that device current) and keeps it for
+ * later calls; that first call should come before any stream capture.
+ * Nothing in the scratch has to start at zero: each call writes every word it
+ * reads.  Calls that overlap in time on one device race on the scratch (two
+ * host threads, or work on two streams): order them on one stream. */
+#define NQ_STATIC_WORKSPACE_BYTES (8u << 20)
+int nq_decompress_kv_static(const void* in, size_t in_bytes, const float* rope_table,
+                            const nq_shape* shape, const nq_params* params, void* k_f16_out,
+                            void* v_f16_out, void* stream);
+
 /* The deferred status of the work enqueued on `stream`: waits for the stream
  * to finish, then returns NQ_ERR_CUDA if the stream or an earlier launch
  * failed (the CUDA error is left for the caller to inspect), else NQ_OK.  The
