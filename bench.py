@@ -41,6 +41,8 @@ def _args():
     ap.add_argument("--config", default="llama31_8b")
     ap.add_argument("--strict", action="store_true", help="strict E8 parity instead of relaxed")
     ap.add_argument("--joint", action="store_true", help="strict E8 in the joint 8b-bit format (no coset words)")
+    ap.add_argument("--delta-chunk", type=int, default=None,
+                    help="temporal delta restart interval instead of the config's (0: none; >= tokens: one chain)")
     ap.add_argument("--e2e-steps", type=int, default=4)
     ap.add_argument("--fused-steps", type=int, default=10, help="timed nq_roundtrip_kv calls (0: skip)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
@@ -91,15 +93,14 @@ def _traffic_record(kernel):
 
 def _pick_params(cfg, a):
     """The config's first codec mode with the requested parity; --joint turns it
-    into the strict joint format."""
+    into the strict joint format, --delta-chunk sets the delta restart interval."""
+    from e8_lattice_vector_gb300 import CodecParams
+
     strict = a.strict or a.joint
     params = ([m for m in cfg.modes if bool(m.strict) == strict] or list(cfg.modes))[0]
-    if a.joint:
-        from e8_lattice_vector_gb300 import CodecParams
-
-        params = CodecParams(params.key_bits, params.value_bits, params.group_size, 2, params.delta_chunk,
-                             params.rope_theta)
-    return params
+    delta = params.delta_chunk if getattr(a, "delta_chunk", None) is None else a.delta_chunk
+    return CodecParams(params.key_bits, params.value_bits, params.group_size, 2 if a.joint else params.strict, delta,
+                       params.rope_theta)
 
 
 class ClockSampler:

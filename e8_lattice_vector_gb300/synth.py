@@ -4,7 +4,8 @@ This module only draws random numbers: it holds none of the codec's
 arithmetic and is shared, as plain input data, by the tests, the benchmark and
 the smoke check.  The models and datasets the method was measured on
 (Mistral-7B, Phi-3-mini, Llama-3.1-8B, Qwen2.5-14B on wikitext-2 / C4) are not
-available here; these caches stand in for them with the same shapes.
+available here; these caches stand in for them with the same shapes (plus one
+head_dim-64 cache shaped like Llama-3.2-1B's, for the head_dim-64 kernels).
 
 Recipe, per layer l (generator seeded with seed * 1000 + l on the target
 device):
@@ -67,6 +68,10 @@ CONFIGS = {
     "phi3mini": CacheConfig("phi3mini", 32, 2, 32, 2048, 96, 0.5, 0.0, 1.0, 1e4, "normal", 2,
                             (_p(3, 2, False, 256, 1e4),)),
     "llama31_8b": CacheConfig("llama31_8b", 32, 4, 8, 32768, 128, 0.7, 0.0, 1.0, 5e5, "student_t5", 3,
+                              (_p(2, 2, False, 0, 5e5), _p(2, 2, True, 0, 5e5))),
+    # head_dim 64 (the shape of Llama-3.2-1B's cache: 16 layers, 8 KV heads), for the kernels'
+    # head_dim-64 path; not one of the pages' measured models
+    "llama32_1b": CacheConfig("llama32_1b", 16, 1, 8, 32768, 64, 0.7, 0.0, 1.0, 5e5, "student_t5", 5,
                               (_p(2, 2, False, 0, 5e5), _p(2, 2, True, 0, 5e5))),
     "qwen25_14b": CacheConfig("qwen25_14b", 48, 1, 8, 131072, 128, 1.0, 0.01, 16.0, 1e6, "normal", 4,
                               (_p(3, 2, False, 256, 1e6), _p(3, 2, True, 256, 1e6),

@@ -428,7 +428,7 @@ def _full_size_check(nq, orc, cfg, K, V, params, rows, cs):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("name", ["mistral7b", "phi3mini", "llama31_8b", "qwen25_14b"])
+@pytest.mark.parametrize("name", ["mistral7b", "phi3mini", "llama31_8b", "qwen25_14b", "llama32_1b"])
 def test_full_size_sampled_parity(nq, orc, name):
     """Each full-size cache in every codec mode it is served in, compressed and
     decompressed by the same library calls the benchmark times; a sample of
@@ -445,7 +445,7 @@ def test_full_size_sampled_parity(nq, orc, name):
         _full_size_check(nq, orc, cfg, K, V, params, rows, cs)
 
 
-@pytest.mark.parametrize("name,kb,vb", [("mistral7b", 2, 2), ("phi3mini", 3, 2)])
+@pytest.mark.parametrize("name,kb,vb", [("mistral7b", 2, 2), ("phi3mini", 3, 2), ("llama32_1b", 2, 2)])
 def test_full_size_single_chain_delta(nq, orc, name, kb, vb):
     """The pages' temporal delta as one chain per slice (delta_chunk >= tokens)
     on a full-size cache: sampled rows deep in the chain (their predecessors
