@@ -9,7 +9,7 @@
 // tiles, up to the method's single chain per slice) needs the sum of every
 // stored row of its chain before it.  Two light passes give it that before the
 // decoder runs:
-//   1. group totals: a warp per group sums its tiles' rows (column sums);
+//   1. group totals: a block per group sums its tiles' rows (column sums);
 //   2. chain scan: a warp per chain scans its groups' totals into, per group,
 //      the sum of the chain's groups before it.
 // The states live in the caller's workspace: one slot of slot_words words per
@@ -123,12 +123,18 @@ struct GroupWalk {
     }
 };
 
-// Pass 1: group totals.  A warp per group; lane (u, sg) takes column unit u
-// of the rows of segment sg of each tile (the split of the decoder's tile
-// scan), reduces over the segments with xor shuffles, and sums over the
-// group's tiles.
+// Pass 1: group totals.  A block of kGroupWarps warps per group: warp w sums
+// tiles j0 + w, j0 + w + kGroupWarps, ... of the group (lane (u, sg) takes
+// column unit u of the rows of segment sg of each tile, the split of the
+// decoder's tile scan, and reduces over the segments with xor shuffles); the
+// warps' partial sums meet in shared memory.  Spreading a group over the
+// block keeps every warp's loads in flight at once (a warp walking all 32
+// tiles of a group waited on memory tile after tile when the groups were
+// few).
+constexpr int kGroupWarps = 8;
+
 template <int BITS, int RB, int R>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kGroupWarps * 32)
     delta_group_kernel(const uint8_t* __restrict__ idx, const uint16_t* __restrict__ coset, int64_t slices,
                        int tpad, ChainGeom geo, uint32_t* __restrict__ gsum, int slot_words) {
     using DU = DeltaUnit<BITS>;
@@ -138,17 +144,26 @@ __global__ void __launch_bounds__(256)
     constexpr int RPS = R / SEGS;
     constexpr int CW = RB / 4;
     static_assert(NU * SEGS == 32 && RPS * SEGS == R, "tile split");
-    const int lane = threadIdx.x & 31;
+    __shared__ unsigned part[kGroupWarps][NU][NV];
+    __shared__ unsigned part_c[kGroupWarps];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const int u = lane % NU, sg = lane / NU;
-    const uint64_t nwarps = (uint64_t(gridDim.x) * blockDim.x) >> 5;
-    for (GroupWalk<R> w((uint64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5, nwarps, uint64_t(slices), geo);
-         w.valid(); w.G += w.step, w.enter()) {
+    const uint64_t per = uint64_t(geo.cps) * geo.gpc;
+    const uint64_t total = uint64_t(slices) * per;
+    for (uint64_t G = blockIdx.x; G < total; G += gridDim.x) {
+        const uint64_t slice = G / per;
+        const uint32_t rest = uint32_t(G - slice * per);
+        const uint32_t c = rest / geo.gpc;
+        const uint32_t q = rest - c * geo.gpc;
+        const uint32_t j0 = c * geo.tpc + 32u * q;
+        const uint32_t j1 = min(min(j0 + 32u, (c + 1u) * geo.tpc), geo.tiles);
+        if (j0 >= j1) continue;  // past a short last chain (the same in the whole block)
         unsigned run[NV], run_c = 0u;
 #pragma unroll
         for (int n = 0; n < NV; ++n) run[n] = 0u;
 #pragma unroll 4
-        for (uint32_t j = w.j0; j < w.j1; ++j) {
-            const int64_t row0 = int64_t(w.slice) * tpad + int64_t(j) * R;
+        for (uint32_t j = j0 + wid; j < j1; j += kGroupWarps) {
+            const int64_t row0 = int64_t(slice) * tpad + int64_t(j) * R;
             const uint32_t* src = reinterpret_cast<const uint32_t*>(idx + (row0 + sg * RPS) * RB) + DU::U * u;
 #pragma unroll
             for (int i = 0; i < RPS; ++i) {
@@ -167,9 +182,31 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
             for (int d = 1; d < 32; d *= 2) run_c ^= __shfl_xor_sync(kFull, run_c, d);
         }
-        uint32_t* p = gsum + size_t(w.G) * slot_words;
-        if (sg == 0) unit_store<BITS>(p + DU::U * u, run);
-        if (coset != nullptr && lane == 0) p[CW] = run_c;
+        if (sg == 0)
+#pragma unroll
+            for (int n = 0; n < NV; ++n) part[wid][u][n] = run[n];
+        if (lane == 0) part_c[wid] = run_c;
+        __syncthreads();
+        if (wid == 0) {
+            uint32_t* p = gsum + size_t(G) * slot_words;
+            if (lane < NU) {
+                unsigned t[NV];
+#pragma unroll
+                for (int n = 0; n < NV; ++n) t[n] = part[0][lane][n];
+#pragma unroll
+                for (int w = 1; w < kGroupWarps; ++w)
+#pragma unroll
+                    for (int n = 0; n < NV; ++n) t[n] = DU::add(t[n], part[w][lane][n]);
+                unit_store<BITS>(p + DU::U * lane, t);
+            }
+            if (coset != nullptr && lane == 0) {
+                unsigned t = 0u;
+#pragma unroll
+                for (int w = 0; w < kGroupWarps; ++w) t ^= part_c[w];
+                p[CW] = t;
+            }
+        }
+        __syncthreads();  // the partial sums are read before the next group's
     }
 }
 

@@ -633,9 +633,9 @@ static int launch_chain_sums(const LaunchArgs& a, const uint8_t* idx, const uint
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return NQ_ERR_CUDA;
     const int cap = 8 * sms;  // blocks of 8 warps, 8 resident per SM (the kernels hold few registers)
-    int grid = int(std::min<uint64_t>((groups + 7) / 8, uint64_t(cap)));
-    delta_group_kernel<BITS, RB, R><<<grid, 256, 0, a.stream>>>(idx, coset, a.slices, a.tpad, cs.geo, cs.gsum,
-                                                                cs.slot_words);
+    int grid = int(std::min<uint64_t>(groups, uint64_t(cap)));  // a block per group
+    delta_group_kernel<BITS, RB, R><<<grid, kGroupWarps * 32, 0, a.stream>>>(idx, coset, a.slices, a.tpad, cs.geo,
+                                                                             cs.gsum, cs.slot_words);
     if (cudaGetLastError() != cudaSuccess) return NQ_ERR_CUDA;
     const uint64_t chains = uint64_t(a.slices) * cs.geo.cps;
     grid = int(std::min<uint64_t>((chains + 7) / 8, uint64_t(cap)));
