@@ -36,6 +36,41 @@ int check(const nq_shape* s, const nq_params* p) {
 
 int pad_tokens(int tokens) { return (tokens + 31) / 32 * 32; }
 
+// A stream of the library's own per device, with a fork and a join event:
+// the value tensor's delta run totals (a pure read of its idx section) run on
+// it while the key tensor's decoder runs on the caller's stream, so the
+// re-read overlaps the decoder instead of following it.  Created on first
+// use with the device current; the mutex also keeps one call's fork/join
+// pair from interleaving with another thread's.
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+constexpr int kMaxSideDevices = 64;
+std::mutex g_side_mu;
+SideStream g_side[kMaxSideDevices];
+
+SideStream* side_stream_locked() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxSideDevices) return nullptr;
+    SideStream& ss = g_side[dev];
+    if (ss.stream == nullptr) {
+        cudaStream_t st = nullptr;
+        cudaEvent_t f = nullptr, j = nullptr;
+        if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+        if (cudaEventCreateWithFlags(&f, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&j, cudaEventDisableTiming) != cudaSuccess) {
+            if (f) cudaEventDestroy(f);
+            cudaStreamDestroy(st);
+            return nullptr;
+        }
+        ss.stream = st;
+        ss.fork = f;
+        ss.join = j;
+    }
+    return &ss;
+}
+
 // The coset words of a tensor, or null in the strict joint format (strict = 2),
 // whose block codes carry the coset bit themselves.
 uint16_t* coset_section(uint8_t* base, uint64_t off, const nq_params* p) {
@@ -338,15 +373,52 @@ int nq_decompress_kv(const void* in, size_t in_bytes, const float* rope_table,
     a.stream = static_cast<cudaStream_t>(stream);
     const uint8_t* base = static_cast<const uint8_t*>(in);
     const int max_bits = std::max(params->key_bits, params->value_bits);
-    st = nq::launch_decompress_tensor(a, shape->head_dim, params->key_bits, max_bits, base + L.k_idx,
-                                      nq::coset_section(base, L.k_coset, params),
-                                      reinterpret_cast<const uint16_t*>(base + L.k_scale),
-                                      rope ? rope_table : nullptr, k_f16_out);
+    auto keys = [&](const nq::LaunchArgs& la) {
+        return nq::launch_decompress_tensor(la, shape->head_dim, params->key_bits, max_bits, base + L.k_idx,
+                                            nq::coset_section(base, L.k_coset, params),
+                                            reinterpret_cast<const uint16_t*>(base + L.k_scale),
+                                            rope ? rope_table : nullptr, k_f16_out);
+    };
+    auto values = [&](const nq::LaunchArgs& la) {
+        return nq::launch_decompress_tensor(la, shape->head_dim, params->value_bits, max_bits, base + L.v_idx,
+                                            nq::coset_section(base, L.v_coset, params),
+                                            reinterpret_cast<const uint16_t*>(base + L.v_scale), nullptr,
+                                            v_f16_out);
+    };
+    if (L.workspace_bytes > 0) {
+        // Long delta chains: key run totals and scan; then the value run totals
+        // on the side stream (they overwrite only the totals, which the key
+        // scan has consumed) while the keys decode (they read only the scan's
+        // results); then, joined, the value scan and decoder.
+        std::lock_guard<std::mutex> lock(nq::g_side_mu);
+        nq::SideStream* ss = nq::side_stream_locked();
+        if (ss != nullptr) {
+            nq::LaunchArgs ka = a, va = a;
+            ka.stages = nq::kStageRunTotals | nq::kStageChainScan;
+            st = keys(ka);
+            if (st != NQ_OK) return st;
+            if (cudaEventRecord(ss->fork, a.stream) != cudaSuccess ||
+                cudaStreamWaitEvent(ss->stream, ss->fork, 0) != cudaSuccess)
+                return NQ_ERR_CUDA;
+            va.stream = ss->stream;
+            va.stages = nq::kStageRunTotals;
+            const int sv = values(va);
+            ka.stages = nq::kStageDecode;
+            const int sk = keys(ka);
+            // join even after a failed launch, so the caller's stream never runs ahead of the side stream
+            if (cudaEventRecord(ss->join, ss->stream) != cudaSuccess ||
+                cudaStreamWaitEvent(a.stream, ss->join, 0) != cudaSuccess)
+                return NQ_ERR_CUDA;
+            if (sv != NQ_OK) return sv;
+            if (sk != NQ_OK) return sk;
+            va.stream = a.stream;
+            va.stages = nq::kStageChainScan | nq::kStageDecode;
+            return values(va);
+        }
+    }
+    st = keys(a);
     if (st != NQ_OK) return st;
-    return nq::launch_decompress_tensor(a, shape->head_dim, params->value_bits, max_bits, base + L.v_idx,
-                                        nq::coset_section(base, L.v_coset, params),
-                                        reinterpret_cast<const uint16_t*>(base + L.v_scale), nullptr,
-                                        v_f16_out);
+    return values(a);
 }
 
 int nq_get_status(void* stream) {

@@ -634,9 +634,12 @@ static int launch_chain_sums(const LaunchArgs& a, const uint8_t* idx, const uint
         return NQ_ERR_CUDA;
     const int cap = 8 * sms;  // blocks of 8 warps, 8 resident per SM (the kernels hold few registers)
     int grid = int(std::min<uint64_t>(groups, uint64_t(cap)));  // a block per group
-    delta_group_kernel<BITS, RB, R><<<grid, kGroupWarps * 32, 0, a.stream>>>(idx, coset, a.slices, a.tpad, cs.geo,
-                                                                             cs.gsum, cs.slot_words);
-    if (cudaGetLastError() != cudaSuccess) return NQ_ERR_CUDA;
+    if (a.stages & kStageRunTotals) {
+        delta_group_kernel<BITS, RB, R><<<grid, kGroupWarps * 32, 0, a.stream>>>(idx, coset, a.slices, a.tpad,
+                                                                                 cs.geo, cs.gsum, cs.slot_words);
+        if (cudaGetLastError() != cudaSuccess) return NQ_ERR_CUDA;
+    }
+    if (!(a.stages & kStageChainScan)) return NQ_OK;
     const uint64_t chains = uint64_t(a.slices) * cs.geo.cps;
     grid = int(std::min<uint64_t>((chains + 7) / 8, uint64_t(cap)));
     delta_chain_kernel<BITS, RB><<<grid, 256, 0, a.stream>>>(a.slices, cs.geo, cs.gsum, cs.gexcl, cs.slot_words,
@@ -660,10 +663,13 @@ static int launch_any(const LaunchArgs& a, const uint8_t* idx, const uint16_t* c
             if (a.workspace == nullptr) return NQ_ERR_ARG;
             cs.gsum = reinterpret_cast<uint32_t*>(a.workspace + cp.gsum);
             cs.gexcl = reinterpret_cast<uint32_t*>(a.workspace + cp.gexcl);
-            const int st = launch_chain_sums<BITS, RB, R>(a, idx, coset, cs);
-            if (st != NQ_OK) return st;
+            if (a.stages & (kStageRunTotals | kStageChainScan)) {
+                const int st = launch_chain_sums<BITS, RB, R>(a, idx, coset, cs);
+                if (st != NQ_OK) return st;
+            }
         }
     }
+    if (!(a.stages & kStageDecode)) return NQ_OK;
     if constexpr (D != 64) {
         if (rope != nullptr) return launch_keys<D, BITS, JOINT>(a, idx, coset, scales, rope, map, cs);
         return launch<D, BITS, JOINT>(a, idx, coset, scales, rope, map, cs);

@@ -79,7 +79,14 @@ struct LaunchArgs {
     int delta_chunk;
     cudaStream_t stream;
     uint8_t* workspace = nullptr;  // decompression with a delta: the running sums' scratch
+    unsigned stages = 7u;          // decompression: which of kStageRunTotals | kStageChainScan | kStageDecode to launch
 };
+
+// The launches of one tensor's decompression, in stream order: the run totals
+// and the chain scan (only for delta chains longer than a run of tiles), then
+// the decoder.  A call can split them so that the value tensor's run totals
+// overlap the key tensor's decoder.
+constexpr unsigned kStageRunTotals = 1u, kStageChainScan = 2u, kStageDecode = 4u;
 
 // Blocks of kThreads that fit on the current device at once for `kernel` with
 // `smem` bytes of dynamic shared memory; -1 when it cannot be queried.

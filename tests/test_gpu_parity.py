@@ -468,6 +468,35 @@ def test_full_size_single_chain_delta(nq, orc, name, kb, vb):
     _full_size_check(nq, orc, cfg, K, V, params, rows, cs)
 
 
+def test_long_chains_on_a_user_stream_back_to_back(nq):
+    """Long delta chains decompressed on a non-default stream, three calls in
+    a row into different outputs with one workspace and no synchronisation in
+    between (the value run totals of each call run on the library's side
+    stream): every result equals the one decompressed alone on the default
+    stream."""
+    from e8_lattice_vector_gb300 import CodecParams
+
+    shape = (2, 1, 4, 3000, 128)
+    p = CodecParams(3, 2, 64, 0, 3008, 1e4)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(77)
+    caches = [((torch.randn(shape, generator=g, device="cuda") * 2).half(),
+               torch.randn(shape, generator=g, device="cuda").half()) for _ in range(3)]
+    rope = nq.RopeTable.build(shape[3], shape[4], p.rope_theta)
+    bufs = [nq.compress_kv(K, V, p, rope) for K, V in caches]
+    ref = [nq.decompress_kv(b, shape, p, rope) for b in bufs]
+    torch.cuda.synchronize()
+    ws = nq.workspace(int(nq.plan(shape, p).workspace_bytes), "cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        outs = [nq.decompress_kv(b, shape, p, rope, ws=ws) for b in bufs]
+    s.synchronize()
+    for (Kr, Vr), (Ko, Vo) in zip(ref, outs):
+        assert torch.equal(Kr.view(torch.int16), Ko.view(torch.int16))
+        assert torch.equal(Vr.view(torch.int16), Vo.view(torch.int16))
+
+
 @pytest.mark.parametrize("name,kb,vb", [("mistral7b", 2, 2), ("phi3mini", 3, 2)])
 def test_full_size_joint_format(nq, orc, name, kb, vb):
     """The strict joint format on a full-size cache: sampled rows re-encoded by
