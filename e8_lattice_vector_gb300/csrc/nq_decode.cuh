@@ -66,6 +66,19 @@ __device__ __forceinline__ void store_rows(const float (&y)[N], uint32_t ob, int
     }
 }
 
+// The inverse rotation of the thread's unscaled slots (two-thread layout), the
+// stages as pair_decode_codes below describes them.
+template <int D>
+__device__ __forceinline__ void pair_inverse_rotation(float (&y)[D / 2], float sgn) {
+    using PM = PairMap<D>;
+    constexpr int HALF = PM::HALF;
+    constexpr int Q = PM::Q;
+#pragma unroll
+    for (int h = 1; h < Q; h *= 2) fwht_stage<HALF>(y, h);
+    stage_signed<HALF>(y, sgn);
+    stage_exchange<HALF>(y);
+}
+
 // The thread's half of a two-thread row: block codes (its NBT blocks, coset
 // bits cwl with bit k = block k, scales of its 32-subgroups) -> coordinates
 // in PairMap slots.  The inverse transform (textbook order) runs its bits
@@ -75,16 +88,10 @@ __device__ __forceinline__ void store_rows(const float (&y)[N], uint32_t ob, int
 template <int D, int BITS>
 __device__ __forceinline__ void pair_decode_codes(const unsigned (&blk)[D / 16], unsigned cwl,
                                                   const float (&scf)[D / 64], float sgn, float (&y)[D / 2]) {
-    using PM = PairMap<D>;
-    constexpr int HALF = PM::HALF;
-    constexpr int Q = PM::Q;
-    constexpr int NBT = PM::NBT;
+    constexpr int NBT = PairMap<D>::NBT;
 #pragma unroll
     for (int k = 0; k < NBT; ++k) unscale_block<BITS>(blk[k], (cwl >> k) & 1u, scf[(8 * k) / 32], &y[8 * k]);
-#pragma unroll
-    for (int h = 1; h < Q; h *= 2) fwht_stage<HALF>(y, h);
-    stage_signed<HALF>(y, sgn);
-    stage_exchange<HALF>(y);
+    pair_inverse_rotation<D>(y, sgn);
 }
 
 // RoPE re-apply of slot pairs (2qq, 2qq + Q) and (2qq + 1, 2qq + 1 + Q) (the

@@ -293,8 +293,13 @@ __device__ __forceinline__ int e8_general(const float (&u)[8], bool strict, floa
 // with a tie for the maximal score or a maximal score <= 2^-100 (every
 // coordinate nearly an integer or past the box edge) is not handled here
 // either.
-template <int BITS, bool STRICT>
-__device__ __forceinline__ bool e8_fast(const float (&u)[8], unsigned& code, unsigned& coset) {
+//
+// POINT: instead of the code, write the chosen lattice point itself into u
+// (r0 - hb cs + m ind cs per coordinate: exact multiples of 1/2), for a caller
+// that dequantizes at once (the one-pass round trip); the code accumulators
+// are then not formed.  The point is the one the code names.
+template <int BITS, bool STRICT, bool POINT, typename U>
+__device__ __forceinline__ bool e8_fast_core(U& u, unsigned& code, unsigned& coset) {
     using C = Code<BITS>;
     constexpr float L = float(C::L);
     constexpr float Lp[4] = {1.0f, L, L * L, L * L * L};
@@ -327,8 +332,10 @@ __device__ __forceinline__ bool e8_fast(const float (&u)[8], unsigned& code, uns
         const float2 cl = make_float2(copysignf(0.5f * Lp[j], e0.x), copysignf(0.5f * Lp[j], e0.y));
         clv[j] = cl.x;
         clv[j + 4] = cl.y;
-        A = __ffma2_rn(r0, make_float2(Lp[j], Lp[j]), A);
-        B = __fadd2_rn(B, cl);
+        if constexpr (!POINT) {
+            A = __ffma2_rn(r0, make_float2(Lp[j], Lp[j]), A);
+            B = __fadd2_rn(B, cl);
+        }
         s0[j] = fminf(fabsf(e0.x), __fsub_rn(C::HI0, fabsf(uu.x)));
         s0[j + 4] = fminf(fabsf(e0.y), __fsub_rn(C::HI0, fabsf(uu.y)));
         x0 ^= __float_as_uint(t.x) ^ __float_as_uint(t.y);
@@ -367,6 +374,12 @@ __device__ __forceinline__ bool e8_fast(const float (&u)[8], unsigned& code, uns
     // branch), applied if needed.
     const bool fix = half ? odd1 : odd0;
     const float smax = half ? smax1 : smax0;
+    // POINT: the fix-up step m and the half-integer shift hb, needed in the loop
+    float mpt = 0.0f, hbpt = 0.0f;
+    if constexpr (POINT) {
+        mpt = fix ? (half ? 2.0f : -2.0f) : 0.0f;
+        hbpt = half ? 1.0f : 0.0f;
+    }
     float2 G = make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -377,6 +390,15 @@ __device__ __forceinline__ bool e8_fast(const float (&u)[8], unsigned& code, uns
         asm("fma.rn.sat.f32 %0, %1, 0fFF000000, 0f3F800000;" : "=f"(ind.x) : "f"(dlt.x));
         asm("fma.rn.sat.f32 %0, %1, 0fFF000000, 0f3F800000;" : "=f"(ind.y) : "f"(dlt.y));
         G = __ffma2_rn(ind, make_float2(clv[j], clv[j + 4]), G);
+        if constexpr (POINT) {  // r0 again (magic rounding), cs = cl / L^j, then r0 + cs (m ind - hb)
+            const float2 uu = make_float2(u[j], u[j + 4]);
+            const float2 r0 = fsub2(__fadd2_rn(uu, M2), M2);
+            const float2 csj = __fmul2_rn(make_float2(clv[j], clv[j + 4]), make_float2(1.0f / Lp[j], 1.0f / Lp[j]));
+            const float2 w = __ffma2_rn(ind, make_float2(mpt, mpt), make_float2(-hbpt, -hbpt));
+            const float2 pt = __ffma2_rn(csj, w, r0);
+            u[j] = pt.x;
+            u[j + 4] = pt.y;
+        }
     }
     // A unique maximum leaves one term +-L^k / 2, a power of two, in exactly one
     // half-block; ties leave sums of distinct +-L^j / 2 (L >= 4), which are
@@ -394,16 +416,30 @@ __device__ __forceinline__ bool e8_fast(const float (&u)[8], unsigned& code, uns
         unique = one && (__float_as_uint(__fadd_rn(G.x, G.y)) & 0x7fffffu) == 0u;
     }
     ok = ok && (!fix || (smax > 7.88860905e-31f && unique));  // 2^-100
-    const float m = fix ? (half ? 2.0f : -2.0f) : 0.0f;
-    const float hb = half ? 1.0f : 0.0f;
+    if constexpr (!POINT) {
+        const float m = fix ? (half ? 2.0f : -2.0f) : 0.0f;
+        const float hb = half ? 1.0f : 0.0f;
 
-    // integer codes m0 = r0 + (L/2 - 1), half-integer codes m1 = r1 + (L - 1)/2,
-    // per half-block an exact integer below 2^16 in the low bits of 2^23 + m
-    // (every intermediate is a multiple of 1/2 below 2^24, so all of this is exact)
-    const float2 f = __fadd2_rn(fsub2(A, __fmul2_rn(B, make_float2(hb, hb))), __fmul2_rn(make_float2(m, m), G));
-    code = (__float_as_uint(f.x) & 0xffffu) | ((__float_as_uint(f.y) & 0xffffu) << (4 * BITS));
+        // integer codes m0 = r0 + (L/2 - 1), half-integer codes m1 = r1 + (L - 1)/2,
+        // per half-block an exact integer below 2^16 in the low bits of 2^23 + m
+        // (every intermediate is a multiple of 1/2 below 2^24, so all of this is exact)
+        const float2 f = __fadd2_rn(fsub2(A, __fmul2_rn(B, make_float2(hb, hb))), __fmul2_rn(make_float2(m, m), G));
+        code = (__float_as_uint(f.x) & 0xffffu) | ((__float_as_uint(f.y) & 0xffffu) << (4 * BITS));
+    }
     coset = half ? 1u : 0u;
     return ok;
+}
+
+template <int BITS, bool STRICT>
+__device__ __forceinline__ bool e8_fast(const float (&u)[8], unsigned& code, unsigned& coset) {
+    return e8_fast_core<BITS, STRICT, false>(u, code, coset);
+}
+
+// The fast path's lattice point in place of u (coordinates, not codes).
+template <int BITS, bool STRICT>
+__device__ __forceinline__ bool e8_fast_point(float (&u)[8], unsigned& coset) {
+    unsigned unused;
+    return e8_fast_core<BITS, STRICT, true>(u, unused, coset);
 }
 
 // Block code of a general-path point.

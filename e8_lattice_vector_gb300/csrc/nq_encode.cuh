@@ -63,18 +63,17 @@ __device__ __forceinline__ void load_pair_tile(const __half* __restrict__ x, int
     }
 }
 
-// Rotation, group scales and E8 codes of the thread's half of a row
-// (two-thread layout): block codes blk (the thread's NBT blocks), their coset
-// bits cwl (bit k = block k) and the fp16 scale bits of its 32-subgroups.
-template <int D, int BITS, bool STRICT>
-__device__ __forceinline__ void pair_encode_codes(float (&y)[D / 2], int hf, float sgn, int group,
-                                                  unsigned (&blk)[D / 16], unsigned& cwl,
-                                                  unsigned short (&sc)[D / 64]) {
+// Rotation and group scales of the thread's half of a row (two-thread
+// layout): the fp16 scale bits sc and reciprocals inv of its 32-subgroups;
+// returns whether every scaled coordinate is inside the box (the fast
+// decoder's condition).
+template <int D, int BITS>
+__device__ __forceinline__ bool pair_rotate_scale(float (&y)[D / 2], float sgn, int group,
+                                                  unsigned short (&sc)[D / 64], float (&inv)[D / 64]) {
     constexpr int DP = D;
     using PM = PairMap<DP>;
     constexpr int HALF = PM::HALF;
     constexpr int Q = PM::Q;
-    constexpr int NBT = PM::NBT;
     constexpr int NSUB = HALF / 32;  // 32-coordinate subgroups per thread
     using C = Code<BITS>;
     constexpr float STEP = float(DP) * C::H;
@@ -102,7 +101,6 @@ __device__ __forceinline__ void pair_encode_codes(float (&y)[D / 2], int hf, flo
 #pragma unroll
         for (int s = 0; s < NSUB; ++s) amax[s] = fmaxf(amax[s], o);
     }
-    float inv[NSUB];
     bool fast = true;
     if (NSUB == 2 && span >= 2) {  // one scale group covers both subgroups: one scale, one reciprocal
         const unsigned short v = group_scale(amax[0], STEP, 1.0f / STEP);
@@ -122,6 +120,22 @@ __device__ __forceinline__ void pair_encode_codes(float (&y)[D / 2], int hf, flo
             fast = fast && (__fmul_rn(amax[s], inv[s]) < C::H);
         }
     }
+
+    return fast;
+}
+
+// Rotation, group scales and E8 codes of the thread's half of a row
+// (two-thread layout): block codes blk (the thread's NBT blocks), their coset
+// bits cwl (bit k = block k) and the fp16 scale bits of its 32-subgroups.
+template <int D, int BITS, bool STRICT>
+__device__ __forceinline__ void pair_encode_codes(float (&y)[D / 2], int hf, float sgn, int group,
+                                                  unsigned (&blk)[D / 16], unsigned& cwl,
+                                                  unsigned short (&sc)[D / 64]) {
+    using PM = PairMap<D>;
+    constexpr int Q = PM::Q;
+    constexpr int NBT = PM::NBT;
+    float inv[D / 64];
+    const bool fast = pair_rotate_scale<D, BITS>(y, sgn, group, sc, inv);
 
     // ---- E8 nearest point per 8-block -> block codes
     // Fast path for every block without a branch, then the general path for

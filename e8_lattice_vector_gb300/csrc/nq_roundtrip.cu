@@ -28,18 +28,44 @@ constexpr int kRtPairSmem = kWarpsPerBlock * kRtStages * kPairTileBytes + 1024;
 // ------------------------------------------------------ two threads per row
 
 // Encode + decode of the thread's half of row r (PairMap slots, RoPE removed).
+// No codes are formed: the fast decoder hands over each block's lattice point,
+// which is scaled straight back into the block's slots (the very product the
+// decompressor forms from the code: (code - offset) is the point's coordinate
+// exactly).  A block the fast decoder declines goes through the general path
+// at once and its code is unscaled as in decompression.
 template <int D, int BITS, bool STRICT>
 __device__ __forceinline__ void pair_round_trip(float (&y)[D / 2], int hf, float sgn, int group) {
+    constexpr int Q = PairMap<D>::Q;
     constexpr int NBT = PairMap<D>::NBT;
     constexpr int NSUB = D / 64;
     unsigned short sc[NSUB];
-    unsigned blk[NBT];
-    unsigned cwl;
-    pair_encode_codes<D, BITS, STRICT>(y, hf, sgn, group, blk, cwl, sc);
+    float inv[NSUB];
+    const bool fast = pair_rotate_scale<D, BITS>(y, sgn, group, sc, inv);
     float scf[NSUB];
 #pragma unroll
     for (int s = 0; s < NSUB; ++s) scf[s] = __half2float(__ushort_as_half(sc[s]));
-    pair_decode_codes<D, BITS>(blk, cwl, scf, sgn, y);
+#pragma unroll
+    for (int k = 0; k < NBT; ++k) {
+        float u[8];
+        pair_block_u<Q>(y, inv, sgn, k, u);
+        unsigned c;
+        const bool ok = e8_fast_point<BITS, STRICT>(u, c);
+        const float s = scf[(8 * k) / 32];
+        if (fast && ok) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 v = __fmul2_rn(make_float2(u[j], u[j + 4]), make_float2(s, s));
+                y[8 * k + j] = v.x;
+                y[8 * k + j + 4] = v.y;
+            }
+        } else {
+            pair_block_u<Q>(y, inv, sgn, k, u);
+            const uint2 res = e8_slow<BITS, STRICT>(make_float4(u[0], u[1], u[2], u[3]),
+                                                    make_float4(u[4], u[5], u[6], u[7]));
+            unscale_block<BITS>(res.x, res.y, s, &y[8 * k]);
+        }
+    }
+    pair_inverse_rotation<D>(y, sgn);
 }
 
 // Values, keys without RoPE, and keys of head_dim 96 (RoPE from the global
