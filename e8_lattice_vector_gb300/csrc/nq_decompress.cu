@@ -59,9 +59,14 @@ __device__ __forceinline__ void load_records(const uint8_t* __restrict__ idx, co
 // 32-lane scan of every block of every row.
 // rows: shared address of row 0 of the tile's ROWS idx rows (RB bytes each);
 // carry: the lane's unit in the previous tile's last row (unused when first).
-template <int BITS, int RB, int ROWS = 32>
+// With COSET, the lanes of unit 0 also undo the coset words' delta (exclusive
+// or) down their segment's rows of the coset column at `cosets` (one 16-bit
+// word per row), riding on the same segment scan; carry_c: the previous
+// tile's last raw coset word (unused when first), updated to this tile's.
+template <int BITS, int RB, int ROWS = 32, bool COSET = false>
 __device__ __forceinline__ void undelta_tile(uint32_t rows, int lane, bool first,
-                                             unsigned (&carry)[DeltaUnit<BITS>::NV]) {
+                                             unsigned (&carry)[DeltaUnit<BITS>::NV], uint32_t cosets = 0,
+                                             unsigned* carry_c = nullptr) {
     using DU = DeltaUnit<BITS>;
     constexpr int NV = DU::NV;
     constexpr int NU = RB / (4 * DU::U);  // units per row
@@ -73,6 +78,19 @@ __device__ __forceinline__ void undelta_tile(uint32_t rows, int lane, bool first
     unsigned v[RPS][NV];
 #pragma unroll
     for (int i = 0; i < RPS; ++i) DU::load(base + i * RB, v[i]);
+    unsigned c[RPS], crun = 0u;
+#pragma unroll
+    for (int i = 0; i < RPS; ++i) c[i] = 0u;
+    const uint32_t cbase = cosets + uint32_t(2 * sg * RPS);
+    if constexpr (COSET) {
+        if (u == 0) {
+#pragma unroll
+            for (int i = 0; i < RPS; ++i) c[i] = lds16(cbase + 2 * i);
+#pragma unroll
+            for (int i = 1; i < RPS; ++i) c[i] ^= c[i - 1];
+            crun = c[RPS - 1];
+        }
+    }
 #pragma unroll
     for (int i = 1; i < RPS; ++i)
 #pragma unroll
@@ -86,6 +104,10 @@ __device__ __forceinline__ void undelta_tile(uint32_t rows, int lane, bool first
         for (int n = 0; n < NV; ++n) {
             const unsigned t = __shfl_up_sync(kFull, run[n], d * NU);
             if (sg >= d) run[n] = DU::add(run[n], t);
+        }
+        if constexpr (COSET) {
+            const unsigned t = __shfl_up_sync(kFull, crun, d * NU);
+            if (sg >= d) crun ^= t;
         }
     }
 #pragma unroll
@@ -102,6 +124,19 @@ __device__ __forceinline__ void undelta_tile(uint32_t rows, int lane, bool first
     }
 #pragma unroll
     for (int n = 0; n < NV; ++n) carry[n] = __shfl_sync(kFull, v[RPS - 1][n], u + (SEGS - 1) * NU);
+    if constexpr (COSET) {
+        unsigned exc = __shfl_up_sync(kFull, crun, NU);
+        if (sg == 0) exc = 0u;
+        if (!first) exc ^= *carry_c;
+        if (u == 0) {
+#pragma unroll
+            for (int i = 0; i < RPS; ++i) {
+                c[i] ^= exc;
+                sts16(cbase + 2 * i, c[i]);
+            }
+        }
+        *carry_c = __shfl_sync(kFull, c[RPS - 1], (SEGS - 1) * NU);
+    }
 }
 
 // One record row (the lane's row of a 32-row record tile in `stage`) ->
@@ -117,13 +152,14 @@ __device__ __forceinline__ void decode_row(uint32_t stage, const uint8_t* stage_
     using RP = RowPack<BITS, NB>;
     constexpr int RB = DP * BITS / 8;
 
-    // ---- undo the temporal delta of the idx tile in place (every lane takes part)
+    // ---- undo the temporal delta of the idx tile and its coset words in place
+    //      (every lane takes part)
     if (delta) {
         constexpr int NV = DeltaUnit<BITS>::NV;
         unsigned cu[NV];
 #pragma unroll
         for (int n = 0; n < NV; ++n) cu[n] = carry[n];
-        undelta_tile<BITS, RB>(stage + kRecIdx, lane, first, cu);
+        undelta_tile<BITS, RB, 32, !JOINT>(stage + kRecIdx, lane, first, cu, stage + kRecCoset, &carry_c);
 #pragma unroll
         for (int n = 0; n < NV; ++n) carry[n] = cu[n];
         __syncwarp();
@@ -158,16 +194,7 @@ __device__ __forceinline__ void decode_row(uint32_t stage, const uint8_t* stage_
     unsigned blk[NB];
     RP::unpack(w, blk);
 
-    // ---- the coset words' delta: an exclusive-or scan over the tile + carry
-    if (delta && !JOINT) {
-#pragma unroll
-        for (int off = 1; off < 32; off *= 2) {
-            const unsigned vc = __shfl_up_sync(kFull, cw, off);
-            if (lane >= off) cw ^= vc;
-        }
-        if (!first) cw ^= carry_c;
-        carry_c = __shfl_sync(kFull, cw, 31);
-    }
+    // (the coset words' delta was undone with the idx tile, in shared memory)
 
     if constexpr (JOINT) {  // strict joint format: the coset bits come out of the block codes
 #pragma unroll
@@ -491,7 +518,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             const uint8_t* gstage = gbase + (stage - base);
             const int t = cur.t0 + r;
 
-            // ---- undo the temporal delta of the idx tile in place (every lane takes part)
+            // ---- undo the temporal delta of the idx tile and its coset words in place
+    //      (every lane takes part)
             bool first = false;  // row 0 starts its chain: no carry
             if constexpr (decltype(cur)::kGroups) {
                 if (cur.group_start()) {
