@@ -310,9 +310,9 @@ __device__ __forceinline__ bool e8_fast_core(U& u, unsigned& code, unsigned& cos
     // clv_j = cs_j L^(j mod 4) with cs_j = copysign(1/2, e~0_j): the sign bit
     // of e~0_j on the power of two L^(j mod 4) / 2 (one logic op, exact); the
     // weights restart at each half-block, whose code is a field of its own
-    float eb1[8], s0[8], clv[8];
+    float eb1[8], s0[8], clv[8];  // eb1: |e~1| (strict)
     // S = sum |e~0_j| in two accumulators; the strict decoder sums
-    // cs_j e~0_j = |e~0_j| / 2 instead (it needs cs_j for e~1 anyway), an
+    // -2 cs_j e~0_j = -|e~0_j| instead (it needs -2 cs_j for |e~1| anyway), an
     // exact rescaling of each term
     float2 S = make_float2(0.0f, 0.0f);
     // A = 2^23 + (L/2 - 1) SUML + sum r0_j L^j: 2^23 plus the integer code
@@ -340,11 +340,13 @@ __device__ __forceinline__ bool e8_fast_core(U& u, unsigned& code, unsigned& cos
         s0[j + 4] = fminf(fabsf(e0.y), __fsub_rn(C::HI0, fabsf(uu.y)));
         x0 ^= __float_as_uint(t.x) ^ __float_as_uint(t.y);
         if (STRICT) {
-            const float2 cs = make_float2(copysignf(0.5f, e0.x), copysignf(0.5f, e0.y));
-            S = __ffma2_rn(cs, e0, S);  // |e~0| / 2 per coordinate (exact products)
-            const float2 e1 = fsub2(e0, cs);
-            eb1[j] = e1.x;
-            eb1[j + 4] = e1.y;
+            // -2 copysign(1/2, e~0) = -2 cl / L^j (exact; no sign operations)
+            const float2 m2cs = __fmul2_rn(cl, make_float2(-2.0f / Lp[j], -2.0f / Lp[j]));
+            S = __ffma2_rn(m2cs, e0, S);  // -|e~0| per coordinate (exact products)
+            // |e~1| = |e~0 - cs| = 1/2 - |e~0|, rounded once: the magnitude of e~0 - cs
+            const float2 a1 = __ffma2_rn(m2cs, e0, make_float2(0.5f, 0.5f));
+            eb1[j] = a1.x;
+            eb1[j + 4] = a1.y;
             xs ^= __float_as_uint(e0.x) ^ __float_as_uint(e0.y);
         } else {
             S.x = __fadd_rn(S.x, fabsf(e0.x));
@@ -354,11 +356,10 @@ __device__ __forceinline__ bool e8_fast_core(U& u, unsigned& code, unsigned& cos
     const float smax0 = fmax3(fmax3(s0[0], s0[1], s0[2]), fmax3(s0[3], s0[4], s0[5]), fmaxf(s0[6], s0[7]));
     float smax1 = 0.0f;
     if (STRICT)
-        smax1 = fmax3(fmax3(fabsf(eb1[0]), fabsf(eb1[1]), fabsf(eb1[2])),
-                      fmax3(fabsf(eb1[3]), fabsf(eb1[4]), fabsf(eb1[5])), fmaxf(fabsf(eb1[6]), fabsf(eb1[7])));
+        smax1 = fmax3(fmax3(eb1[0], eb1[1], eb1[2]), fmax3(eb1[3], eb1[4], eb1[5]), fmaxf(eb1[6], eb1[7]));
     const bool odd0 = (x0 & 1u) != 0;
     const bool odd1 = STRICT && (((x0 ^ (xs >> 31)) & 1u) != 0);  // + number of e~0 < 0
-    float D = STRICT ? __fmaf_rn(2.0f, __fadd_rn(S.x, S.y), -2.0f) : __fsub_rn(__fadd_rn(S.x, S.y), 2.0f);  // sum |e~0| - 2
+    float D = STRICT ? __fsub_rn(-2.0f, __fadd_rn(S.x, S.y)) : __fsub_rn(__fadd_rn(S.x, S.y), 2.0f);  // sum |e~0| - 2
     if (odd0) D = __fadd_rn(D, __fmaf_rn(-2.0f, smax0, 1.0f));
     if (odd1) D = __fsub_rn(D, __fmaf_rn(-2.0f, smax1, 1.0f));
     bool ok = fabsf(D) > BAND;
@@ -383,7 +384,7 @@ __device__ __forceinline__ bool e8_fast_core(U& u, unsigned& code, unsigned& cos
     float2 G = make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const float2 sj = (STRICT && half) ? make_float2(fabsf(eb1[j]), fabsf(eb1[j + 4]))
+        const float2 sj = (STRICT && half) ? make_float2(eb1[j], eb1[j + 4])
                                            : make_float2(s0[j], s0[j + 4]);
         const float2 dlt = fsub2(make_float2(smax, smax), sj);
         float2 ind;
