@@ -1,9 +1,11 @@
 // nq_roundtrip.cu -- the round trip in one pass: fp16 rows -> RoPE removal
-// (keys) -> Hadamard -> group scale -> E8 codes -> unscale -> inverse
-// Hadamard -> RoPE re-apply -> fp16 rows, with no compressed intermediate in
-// memory.  The reconstruction equals decompress(compress(x)) bit for bit: the
-// codes, cosets and scales are the compressor's (the temporal delta is
-// lossless and has no effect here) and the decode is the decompressor's.
+// (keys) -> Hadamard -> group scale -> E8 nearest point -> scaled point ->
+// inverse Hadamard -> RoPE re-apply -> fp16 rows, with no compressed
+// intermediate in memory and no codes formed.  The reconstruction equals
+// decompress(compress(x)) bit for bit: the lattice points and scales are the
+// ones the compressor encodes (the temporal delta is lossless and has no
+// effect here), a point's coordinate is exactly the decompressor's
+// (code - offset), and the rest of the decode is the decompressor's.
 //
 // The streaming is the compressor's: fp16 tiles arrive in a shared-memory
 // ring by cp.async; each reconstructed tile is written back into the ring
