@@ -424,8 +424,15 @@ __device__ __forceinline__ bool e8_fast_core(U& u, unsigned& code, unsigned& cos
         // integer codes m0 = r0 + (L/2 - 1), half-integer codes m1 = r1 + (L - 1)/2,
         // per half-block an exact integer below 2^16 in the low bits of 2^23 + m
         // (every intermediate is a multiple of 1/2 below 2^24, so all of this is exact)
-        const float2 f = __fadd2_rn(fsub2(A, __fmul2_rn(B, make_float2(hb, hb))), __fmul2_rn(make_float2(m, m), G));
-        code = (__float_as_uint(f.x) & 0xffffu) | ((__float_as_uint(f.y) & 0xffffu) << (4 * BITS));
+        // (two fused steps, each exact: every intermediate is an integer-valued float below 2^24)
+        const float2 f = __ffma2_rn(G, make_float2(m, m), __ffma2_rn(B, make_float2(-hb, -hb), A));
+        const unsigned fx = __float_as_uint(f.x), fy = __float_as_uint(f.y);
+        if constexpr (BITS == 2)  // 8-bit half codes, the bits above them zero: one byte permutation
+            code = __byte_perm(fx, fy, 0x1140);
+        else if constexpr (BITS == 4)  // 16-bit half codes
+            code = __byte_perm(fx, fy, 0x5410);
+        else
+            code = (fx & 0xffffu) | ((fy & 0xffffu) << (4 * BITS));
     }
     coset = half ? 1u : 0u;
     return ok;
