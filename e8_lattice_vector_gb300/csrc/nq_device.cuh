@@ -374,7 +374,7 @@ __device__ __forceinline__ bool e8_fast_core(U& u, unsigned& code, unsigned& cos
     // over 4-7).  A tie goes to the general path.  Computed for every block (no
     // branch), applied if needed.
     const bool fix = half ? odd1 : odd0;
-    const float smax = half ? smax1 : smax0;
+    const float smax = STRICT ? (half ? smax1 : smax0) : smax0;  // relaxed: a fix-up means the integer coset
     // POINT: the fix-up step m and the half-integer shift hb, needed in the loop
     float mpt = 0.0f, hbpt = 0.0f;
     if constexpr (POINT) {

@@ -152,7 +152,7 @@ __device__ __forceinline__ void pair_encode_codes(float (&y)[D / 2], int hf, flo
         declined |= unsigned(!ok) << k;
     }
     if (!fast) declined = (1u << NBT) - 1u;
-    if (declined) {
+    if (__any_sync(kFull, declined != 0u)) {  // warp-uniform: most tiles of most warps skip this
 #pragma unroll
         for (int k = 0; k < NBT; ++k) {
             if (!((declined >> k) & 1u)) continue;
