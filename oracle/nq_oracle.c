@@ -136,7 +136,8 @@ void orc_fwht_forward(float* x, int n) {
 static uint16_t half_next_up(uint16_t v) { return (uint16_t)(v + 1); }   /* v >= 0 finite */
 static uint16_t half_next_down(uint16_t v) { return (uint16_t)(v - 1); } /* v > 0 */
 
-/* [WALK "Python Implementation" quantize(): sc = amax / (levels/2)].
+/* [WALK "Python Implementation" quantize(): the scale is the absolute maximum
+ * over half the number of levels].
  * Reading: the divisor is (levels - 1)/2 so that the half-integer grid of the
  * box holds exactly 2^bits levels (the pages' levels/2 box holds more lattice
  * points than b bits can index).  The scale is stored as binary16, one per
