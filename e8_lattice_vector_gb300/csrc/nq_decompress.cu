@@ -263,6 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     else
                         first = true;
                 }
+            } else {
+                first = cur.t0 == cur.t_begin();  // chains of one chunk: its first tile
             }
             const uint8_t* stage_gen = smem + (stage - smem_u32(smem));
             float y[DP];
@@ -277,8 +279,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             cur.next();
         }
     };
+    // plain tiles without a delta; whole chunks, tile after tile, when every
+    // chain fits one run; runs of a chain's tiles (carry from the workspace)
+    // else.  Three call sites: the first keeps its chunk a constant.
     if (!cs.delta)
         run(TileWalk(warp, nwarps, slices, tokens, kTileRows));
+    else if (cs.gexcl == nullptr)
+        run(TileWalk(warp, nwarps, slices, tokens, int(cs.geo.tpc) * kTileRows));
     else
         run(GroupWalk<kTileRows>(warp, nwarps, slices, cs.geo));
     cp_async_wait<0>();
@@ -379,6 +386,8 @@ __global__ void __launch_bounds__(kKeyThreads, 1)
                         else
                             first = true;
                     }
+                } else {
+                    first = cur.t0 == cur.t_begin();
                 }
                 const uint32_t rec = stage + KS::TABLE + wib * kRecStage;
                 float y[DP];
@@ -397,6 +406,8 @@ __global__ void __launch_bounds__(kKeyThreads, 1)
     };
     if (!cs.delta)
         run(TileWalk(blockIdx.x, gridDim.x, ngroups, tokens, kTileRows));
+    else if (cs.gexcl == nullptr)
+        run(TileWalk(blockIdx.x, gridDim.x, ngroups, tokens, int(cs.geo.tpc) * kTileRows));
     else
         run(GroupWalk<kTileRows>(blockIdx.x, gridDim.x, ngroups, cs.geo));
     cp_async_wait<0>();
@@ -518,8 +529,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             const uint8_t* gstage = gbase + (stage - base);
             const int t = cur.t0 + r;
 
-            // ---- undo the temporal delta of the idx tile and its coset words in place
-    //      (every lane takes part)
+            // ---- undo the temporal delta of the idx tile in place (every lane takes part)
             bool first = false;  // row 0 starts its chain: no carry
             if constexpr (decltype(cur)::kGroups) {
                 if (cur.group_start()) {
