@@ -41,15 +41,26 @@ struct Code {
 };
 
 // Field-wise (a - b) mod 2^b and (a + b) mod 2^b of 8 packed b-bit fields.
+// Two-bit fields take a bit-level form: the low bit is a0 ^ b0, and the high
+// bit a1 ^ b1 ^ k with k the borrow (~a0 & b0) or carry (a0 & b0) of the low
+// bit, shifted into its own field only (three logic and shift operations
+// instead of the masked integer add's five).  Wider fields mask the high bit
+// of each field so that a carry or borrow stays inside it.
 template <int BITS>
 __device__ __forceinline__ unsigned swar_sub(unsigned a, unsigned b) {
     constexpr unsigned H = Code<BITS>::FIELD_HI;
-    return ((a | H) - (b & ~H)) ^ ((a ^ ~b) & H);
+    if constexpr (BITS == 2)
+        return a ^ b ^ ((~a & b & (H >> 1)) << 1);
+    else
+        return ((a | H) - (b & ~H)) ^ ((a ^ ~b) & H);
 }
 template <int BITS>
 __device__ __forceinline__ unsigned swar_add(unsigned a, unsigned b) {
     constexpr unsigned H = Code<BITS>::FIELD_HI;
-    return ((a & ~H) + (b & ~H)) ^ ((a ^ b) & H);
+    if constexpr (BITS == 2)
+        return a ^ b ^ ((a & b & (H >> 1)) << 1);
+    else
+        return ((a & ~H) + (b & ~H)) ^ ((a ^ b) & H);
 }
 
 // Strict-E8 joint enumeration of a block in exactly 8b bits.  In both cosets
@@ -74,10 +85,11 @@ __device__ __forceinline__ unsigned joint_split(unsigned joint, unsigned& coset)
     return (joint & ((1u << SH) - 1u)) | (((hi << 1) | parity) << SH);
 }
 
-// Field-wise (a + b) mod 4 of the 16 two-bit fields of a packed word.
+// Field-wise (a + b) mod 4 of the 16 two-bit fields of a packed word (the
+// bit-level form of swar_add<2>).
 __device__ __forceinline__ unsigned swar_add_word2(unsigned a, unsigned b) {
-    constexpr unsigned H = 0xAAAAAAAAu;  // high bit of every field
-    return ((a & ~H) + (b & ~H)) ^ ((a ^ b) & H);
+    constexpr unsigned LO = 0x55555555u;  // low bit of every field
+    return a ^ b ^ ((a & b & LO) << 1);
 }
 
 // ------------------------------------------------------------------ Hadamard
