@@ -15,7 +15,7 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libnq.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["nq_api.cu", "nq_compress.cu", "nq_compress_delta.cu", "nq_decompress.cu", "nq_roundtrip.cu", "nq_stats.cu", "nq_layers.cu", "nq_noalloc.cu"]
+SOURCES = ["nq_api.cu", "nq_compress.cu", "nq_compress_delta.cu", "nq_decompress.cu", "nq_decompress_delta.cu", "nq_roundtrip.cu", "nq_stats.cu", "nq_layers.cu", "nq_noalloc.cu"]
 HEADERS = sorted(f for f in os.listdir(CSRC) if f.endswith((".cuh", ".h")))
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -296,4 +296,16 @@ __device__ __forceinline__ void load_group_carry(const ChainState& cs, uint64_t 
     carry_c = has_coset ? p[CW] : 0u;
 }
 
+// The same for the column layout of the three-bit 32-row decoders (one block
+// code per lane): the 24-bit code of block column c, bytes 3c..3c+2 of the
+// slot's packed row (the byte above it is the next code's; the sums ignore it).
+__device__ __forceinline__ void load_group_carry24(const ChainState& cs, uint64_t G, int c, unsigned& carry,
+                                                   unsigned& carry_c, bool has_coset) {
+    constexpr int CW = 48 / 4;
+    const uint32_t* p = cs.gexcl + size_t(G) * cs.slot_words;
+    const int w = (3 * c) >> 2;  // c = 15: the second word is the coset word (in the slot)
+    carry = __byte_perm(p[w], p[w + 1], 0x3210u + 0x1111u * ((3u * uint32_t(c)) & 3u));
+    carry_c = has_coset ? p[CW] : 0u;
+}
+
 }  // namespace nq
