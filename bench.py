@@ -41,6 +41,7 @@ def _args():
     ap.add_argument("--config", default="llama31_8b")
     ap.add_argument("--strict", action="store_true", help="strict E8 parity instead of relaxed")
     ap.add_argument("--joint", action="store_true", help="strict E8 in the joint 8b-bit format (no coset words)")
+    ap.add_argument("--bits", default=None, help="K,V code widths (e.g. 2,2): the config's first mode with them")
     ap.add_argument("--delta-chunk", type=int, default=None,
                     help="temporal delta restart interval instead of the config's (0: none; >= tokens: one chain)")
     ap.add_argument("--e2e-steps", type=int, default=4)
@@ -92,12 +93,19 @@ def _traffic_record(kernel):
 
 
 def _pick_params(cfg, a):
-    """The config's first codec mode with the requested parity; --joint turns it
-    into the strict joint format, --delta-chunk sets the delta restart interval."""
+    """The config's first codec mode with the requested parity (and code widths,
+    --bits); --joint turns it into the strict joint format, --delta-chunk sets
+    the delta restart interval."""
     from e8_lattice_vector_gb300 import CodecParams
 
     strict = a.strict or a.joint
-    params = ([m for m in cfg.modes if bool(m.strict) == strict] or list(cfg.modes))[0]
+    modes = list(cfg.modes)
+    if getattr(a, "bits", None):
+        kb, vb = (int(x) for x in a.bits.split(","))
+        modes = [m for m in modes if (m.key_bits, m.value_bits) == (kb, vb)]
+        if not modes:
+            raise SystemExit("config %s has no K%dV%d mode" % (cfg.name, kb, vb))
+    params = ([m for m in modes if bool(m.strict) == strict] or modes)[0]
     delta = params.delta_chunk if getattr(a, "delta_chunk", None) is None else a.delta_chunk
     return CodecParams(params.key_bits, params.value_bits, params.group_size, 2 if a.joint else params.strict, delta,
                        params.rope_theta)
