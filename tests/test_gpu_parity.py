@@ -216,11 +216,16 @@ COMBOS = [
     ((1, 2, 2, 2100, 96), 3, 2, 64, 1, 2112, 1e4),
     ((1, 1, 2, 1500, 64), 2, 3, 64, 1, 1504, 5e5),
     ((1, 1, 3, 500, 64), 4, 2, 32, 0, 512, 5e5),
+    # three-bit values along a long chain (the value decoder's column carry from the workspace)
+    ((1, 1, 3, 1100, 96), 2, 3, 32, 0, 1120, 5e5),
     # strict joint format (no coset words)
     ((2, 1, 3, 77, 128), 2, 2, 64, 2, 0, 1e4),
     ((1, 2, 2, 130, 128), 3, 4, 32, 2, 32, 5e5),
     ((2, 2, 2, 100, 96), 3, 2, 64, 2, 32, 1e4),
     ((1, 1, 4, 65, 64), 4, 3, 64, 2, 0, 1e4),
+    # joint format along long chains: three-bit keys and values, four-bit keys
+    ((1, 1, 2, 2100, 128), 3, 3, 64, 2, 2112, 1e4),
+    ((1, 1, 2, 1300, 128), 4, 2, 64, 2, 1312, 5e5),
 ]
 
 
