@@ -8,16 +8,19 @@
 // aligned thanks to the per-slice padding of the record rows, so they stream
 // through a 3-stage shared-memory ring by cp.async; keys run in blocks of
 // warps that also stage the tile's RoPE table rows once for the block.
-// Without a temporal delta every tile is a work item; with one, a run of up
-// to 32 consecutive tiles of a chain is, walked in order.  The delta is undone
-// in place on the record tile, column-wise (field-wise addition modulo 2^b),
-// plus the running sum of the chain's earlier rows, carried in registers from
-// tile to tile; a run that does not start its chain takes its starting sum
-// from the workspace, where two light passes over the idx section leave it
-// (nq_chain.cuh).  Coset words by an exclusive-or warp scan.  The reconstructed fp16 rows
-// are written into a swizzled shared-memory tile and leave by one TMA tensor
-// store per 64 columns, which clips the rows past the end of the slice and the
-// columns past head_dim.  head_dim 64 uses two threads per row (16-row tiles).
+// Without a temporal delta every tile is a work item; with one, a chain of at
+// most one chunk, or else a run of up to 32 consecutive tiles of a chain, is,
+// walked in order (the kernels are instantiated with and without a delta).
+// The delta is undone in place on the record tile, column-wise (field-wise
+// addition modulo 2^b), plus the running sum of the chain's earlier rows,
+// carried in registers from tile to tile; a run that does not start its chain
+// takes its starting sum from the workspace, where two light passes over the
+// idx section leave it (nq_chain.cuh).  Three-bit tiles come back unpacked, one
+// word per block code.  Coset words ride on the column scan (an exclusive-or
+// warp scan for three-bit tiles).  The reconstructed fp16 rows are written
+// into a swizzled shared-memory tile and leave by one TMA tensor store per 64
+// columns, which clips the rows past the end of the slice and the columns past
+// head_dim.  (head_dim 64, two threads per row: nq_decompress.cu.)
 #pragma once
 
 #include <type_traits>
@@ -80,8 +83,9 @@ __device__ __forceinline__ void scan_down(unsigned (&v)[N][NV], int n, unsigned 
 
 // LOWLAT trades additions for a shorter chain: the total by a separate tree
 // while the serial running sums proceed beside it, and the offset added to
-// every value (2N - 1 more additions in all, the chain from the loads to the
-// offset log2 N levels long and the one after it a single addition).  For
+// every value (N - 1 more additions than the Brent-Kung form; the chain from
+// the loads to the offset log2 N levels long, the one after it a single
+// addition).  For
 // decoders whose warps wait for each other at a barrier every tile, where the
 // chain is not hidden by other warps' work.
 template <typename DU, bool LOWLAT, int N, int NV>
@@ -115,7 +119,8 @@ __device__ __forceinline__ void scan_offset(unsigned (&v)[N][NV], int n, unsigne
 // The delta is undone in place on the 32-row idx tile in shared memory, down
 // its columns: lane l takes column unit l % NU (a 32-bit word of 16 two-bit or
 // 8 four-bit fields, or a 3-word group holding four 24-bit block codes at 3
-// bits) of the rows of segment l / NU; it forms the running field-wise sums
+// bits: the 16-row tiles of head_dim 64; 32-row three-bit tiles go by
+// undelta_tile24) of the rows of segment l / NU; it forms the running field-wise sums
 // (mod 2^b) down its segment, adds the exclusive sum of the segments above
 // (a shuffle scan over the segments) and the carry of the chunk's earlier
 // tiles, and writes the codes back.  Far fewer shuffles and additions than a
