@@ -450,16 +450,24 @@ def test_full_size_sampled_parity(nq, orc, name):
         _full_size_check(nq, orc, cfg, K, V, params, rows, cs)
 
 
-@pytest.mark.parametrize("name,kb,vb", [("mistral7b", 2, 2), ("phi3mini", 3, 2), ("llama32_1b", 2, 2)])
+@pytest.mark.parametrize("name,kb,vb", [("mistral7b", 2, 2), ("phi3mini", 3, 2), ("llama32_1b", 2, 2),
+                                        ("qwen25_14b", 3, 2), ("many_short_slices", 3, 2)])
 def test_full_size_single_chain_delta(nq, orc, name, kb, vb):
     """The pages' temporal delta as one chain per slice (delta_chunk >= tokens)
     on a full-size cache: sampled rows deep in the chain (their predecessors
     span many tiles) are checked against the oracle, and their reconstructions
-    need every earlier delta row of the slice."""
+    need every earlier delta row of the slice.  The Qwen2.5-14B shape is the
+    benchmarked single-chain case; the last one (6144 slices of 1536 tokens,
+    two runs per chain, the second one short) has the most runs."""
+    import dataclasses
+
     from e8_lattice_vector_gb300 import CodecParams
     from e8_lattice_vector_gb300.synth import CONFIGS, make_cache
 
-    cfg = CONFIGS[name]
+    if name == "many_short_slices":
+        cfg = dataclasses.replace(CONFIGS["mistral7b"], name=name, layers=24, batch=1, kv_heads=256, tokens=1536)
+    else:
+        cfg = CONFIGS[name]
     K, V = make_cache(cfg, device="cuda")
     T = cfg.tokens
     chain = (T + 31) // 32 * 32
