@@ -123,7 +123,8 @@ struct GroupWalk {
     }
 };
 
-// Pass 1: group totals.  A block of kGroupWarps warps per group: warp w sums
+// Pass 1: group totals (every group but the last of its chain: no starting
+// sum includes that one).  A block of kGroupWarps warps per group: warp w sums
 // tiles j0 + w, j0 + w + kGroupWarps, ... of the group (lane (u, sg) takes
 // column unit u of the rows of segment sg of each tile, the split of the
 // decoder's tile scan, and reduces over the segments with xor shuffles); the
@@ -157,7 +158,9 @@ __global__ void __launch_bounds__(kGroupWarps * 32)
         const uint32_t q = rest - c * geo.gpc;
         const uint32_t j0 = c * geo.tpc + 32u * q;
         const uint32_t j1 = min(min(j0 + 32u, (c + 1u) * geo.tpc), geo.tiles);
-        if (j0 >= j1) continue;  // past a short last chain (the same in the whole block)
+        // past a short last chain, or the last group of its chain, whose total no
+        // starting sum needs (the same in the whole block)
+        if (j0 >= j1 || j1 == min((c + 1u) * geo.tpc, geo.tiles)) continue;
         unsigned run[NV], run_c = 0u;
 #pragma unroll
         for (int n = 0; n < NV; ++n) run[n] = 0u;
@@ -237,16 +240,17 @@ __global__ void __launch_bounds__(256)
         for (uint32_t q0 = 0; q0 < ng; q0 += 32u) {
             const uint32_t q = q0 + lane;
             const bool ok = q < ng;
-            const uint32_t* src = gsum + size_t(ch * geo.gpc + (ok ? q : 0u)) * slot_words;
+            const bool has_total = q + 1u < ng;  // the chain's last group has none (nothing needs it)
+            const uint32_t* src = gsum + size_t(ch * geo.gpc + (has_total ? q : 0u)) * slot_words;
             unsigned v[NU][NV], vc = 0u;
 #pragma unroll
             for (int x = 0; x < NU; ++x) {
                 unit_load<BITS>(src + DU::U * x, v[x]);
-                if (!ok)
+                if (!has_total)
 #pragma unroll
                     for (int n = 0; n < NV; ++n) v[x][n] = 0u;
             }
-            if (has_coset && ok) vc = src[CW];
+            if (has_coset && has_total) vc = src[CW];
 #pragma unroll
             for (int d = 1; d < 32; d *= 2) {
 #pragma unroll
