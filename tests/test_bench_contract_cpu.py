@@ -57,3 +57,29 @@ def test_kernel_source_hash_ignores_comments_only(tmp_path):
     assert ha == bench._kernel_src_hash()
     assert hb == ha
     assert hc != ha
+
+
+def test_mode_selection_by_code_widths_and_parity():
+    """--bits picks a config's mode by its code widths, --strict / --joint by its
+    parity, --delta-chunk overrides the restart interval; a width pair the
+    config does not serve is an error."""
+    sys.path.insert(0, ROOT)
+    import argparse
+
+    import bench
+    from e8_lattice_vector_gb300.synth import CONFIGS
+
+    def pick(name, **kw):
+        a = argparse.Namespace(strict=False, joint=False, delta_chunk=None, bits=None)
+        for k, v in kw.items():
+            setattr(a, k, v)
+        return bench._pick_params(CONFIGS[name], a)
+
+    p = pick("qwen25_14b")
+    assert (p.key_bits, p.value_bits, p.strict, p.delta_chunk) == (3, 2, 0, 256)
+    p = pick("qwen25_14b", bits="2,2", strict=True)
+    assert (p.key_bits, p.value_bits, p.strict) == (2, 2, 1)
+    p = pick("llama31_8b", joint=True, delta_chunk=32768)
+    assert (p.key_bits, p.value_bits, p.strict, p.delta_chunk) == (2, 2, 2, 32768)
+    with pytest.raises(SystemExit):
+        pick("llama31_8b", bits="4,4")
